@@ -1,0 +1,46 @@
+"""The oracle still reproduces its recorded outputs (tests/golden/oracle_regression.json)."""
+import json
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _arr(dt, hexes, shape):
+    if dt == 0:
+        return np.array([int(h, 16) for h in hexes], np.uint32).view(np.float32).reshape(shape)
+    return np.array([int(h, 16) for h in hexes], np.uint16).reshape(shape)
+
+
+def test_golden_regression(orc):
+    data = json.load(open(os.path.join(HERE, "golden", "oracle_regression.json")))
+    assert data["cases"]
+    for c in data["cases"]:
+        dt = c["dtype"]
+        if c["op"] == "bn":
+            shape = (c["batch"], c["c"], c["hw"])
+            x = _arr(dt, c["x"], shape)
+            g = _arr(dt, c["gamma"], (c["c"],))
+            b = _arr(dt, c["beta"], (c["c"],))
+            r = orc.batchnorm_train(dt, x, g, b, running_mean=[0.0] * c["c"],
+                                    running_var=[1.0] * c["c"], eps=np.float32(c["eps"]),
+                                    momentum=np.float32(c["momentum"]))
+            assert np.array_equal(r["y"], _arr(dt, c["y"], shape))
+            for k in ("save_mean", "save_rstd", "running_mean", "running_var"):
+                assert np.array_equal(r[k], np.array(c[k]))
+            continue
+        shape = (c["rows"], c["n"])
+        x = _arr(dt, c["x"], shape)
+        if c["op"] == "ln":
+            r = orc.layernorm(dt, x, _arr(dt, c["gamma"], (c["n"],)),
+                              _arr(dt, c["beta"], (c["n"],)), eps=np.float32(c["eps"]))
+            assert np.array_equal(r["mean"], np.array(c["mean"]))
+        elif c["op"] == "rms":
+            r = orc.rmsnorm(dt, x, _arr(dt, c["w"], (c["n"],)), eps=np.float32(c["eps"]))
+        else:
+            r = orc.add_rmsnorm(dt, x, _arr(dt, c["residual"], shape),
+                                _arr(dt, c["w"], (c["n"],)), eps=np.float32(c["eps"]))
+            assert np.array_equal(r["residual_out"], _arr(dt, c["residual_out"], shape))
+        assert np.array_equal(r["y"], _arr(dt, c["y"], shape))
+        assert np.array_equal(r["rstd"], np.array(c["rstd"]))
