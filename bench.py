@@ -1,0 +1,528 @@
+#!/usr/bin/env python3
+"""Benchmark of the row-wise normalization library on one or more GPUs.
+
+Default workload: fused residual-add + RMSNorm, bf16, x and residual
+[4096, 4096], w [4096], eps 1e-6 (seeded synthetic inputs).  Metric: achieved
+HBM GB/s of algorithmic bytes (read x and residual once, write residual_out
+and y once, read w) and us/call.
+
+Timing: inputs are resident in HBM before the timed region; R rotating input
+sets whose total size exceeds 2x L2 are used round-robin, so every call reads
+cold inputs.  The K steps are captured in CUDA graphs and replayed between two
+CUDA events on the launching stream, after W warm-up steps, bracketed by a
+barrier and torch.cuda.synchronize().  SM clocks and throttle reasons are
+sampled (NVML) during the timed region.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl nrm|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import glob
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from row_wise_normalization_reduce_gb300 import workloads as W  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call, add+RMSNorm 4096x4096 bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# bytes
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(w: W.Workload, stats: bool = True) -> int:
+    """Bytes an ideal kernel moves per call: every input read once, every output
+    written once (parameters and statistics included)."""
+    es = torch.tensor([], dtype=w.torch_dtype).element_size()
+    if w.op == "bn":
+        b, c = w.shape[0], w.shape[1]
+        n = int(np.prod(w.shape))
+        return 2 * n * es + 2 * c * es + 2 * c * 4 + 4 * c * 4
+    rows, n = w.shape
+    t = rows * n * es
+    if w.op == "ln":
+        return 2 * t + 2 * n * es + (2 * rows * 4 if stats else 0)
+    if w.op == "rms":
+        return 2 * t + n * es + (rows * 4 if stats else 0)
+    if w.op == "add_rms":
+        return 4 * t + n * es + (rows * 4 if stats else 0)
+    raise ValueError(w.op)
+
+
+# ---------------------------------------------------------------------------
+# clocks (NVML through ctypes; nvidia-smi as a fallback)
+# ---------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+           0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+           0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+           0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []  # (t, sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
+                                        props.pci_device_id)
+            h = ctypes.c_void_p()
+            if nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + bus)
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._handle = nvml, h
+        except OSError:
+            self._nvml = None
+
+    def _poll(self):
+        nvml, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            ok = nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+            ok = ok and get_reasons(h, ctypes.byref(rs)) == 0
+            if ok:
+                self.samples.append((time.perf_counter(), clk.value, rs.value))
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is None:
+            return
+        self._stop.clear()
+        self._thread = threading.Thread(target=self._poll, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self, t0=None, t1=None):
+        if self._nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        window = "timed"
+        if len(s) < 3:
+            s, window = self.samples, "warmup+timed"
+        mask = 0
+        for _, _, r in s:
+            mask |= r
+        reasons = [name for bit, name in REASONS.items() if mask & bit and bit != 0x1]
+        return {"sm_mhz": statistics.median([c for _, c, _ in s]) if s else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(s),
+                "window": window, "source": "nvml"}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic record (profiles/ncu_traffic.json), valid only for unchanged kernels
+# ---------------------------------------------------------------------------
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_normalization_reduce_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if f.endswith((".cu", ".cuh", ".cpp", ".h")):
+            h.update(os.path.basename(f).encode())
+            h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        rec = json.load(open(path)).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("csrc_hash") != csrc_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def measured_peak():
+    try:
+        p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Step:
+    """One call of the hot path on rotating, pre-filled device buffers."""
+
+    def __init__(self, w: W.Workload, device, l2_bytes: int):
+        import row_wise_normalization_reduce_gb300 as nrm
+        self.nrm = nrm
+        self.w = w
+        inp = W.make_inputs(w)
+        per_set = algorithmic_bytes(w)
+        self.nsets = max(2, int(np.ceil(3 * l2_bytes / per_set)) + 1)
+        dev = lambda t: t.to(device)  # noqa: E731
+        self.params = {k: dev(v) for k, v in inp.items() if k not in ("x", "residual")}
+        self.sets = []
+        for i in range(self.nsets):
+            s = {"x": dev(inp["x"])}
+            if w.op == "add_rms":
+                s["residual"] = dev(inp["residual"])
+                s["residual_out"] = torch.empty_like(s["x"])
+            s["y"] = torch.empty_like(s["x"])
+            rows = inp["x"].shape[0]
+            if w.op == "bn":
+                c = w.shape[1]
+                s["save_mean"] = torch.empty(c, device=device)
+                s["save_rstd"] = torch.empty(c, device=device)
+                s["ws"] = torch.empty(nrm.bn_fwd_train_workspace_size(w.shape[0], c, int(
+                    np.prod(w.shape[2:]))), device=device, dtype=torch.uint8)
+            else:
+                s["rstd"] = torch.empty(rows, device=device)
+                if w.op == "ln":
+                    s["mean"] = torch.empty(rows, device=device)
+            self.sets.append(s)
+        self.i = 0
+        self.launches_per_step = 2 if w.op == "bn" else 1
+        self.host_inputs = inp
+
+    def __call__(self):
+        s = self.sets[self.i % self.nsets]
+        self.i += 1
+        self.run(s)
+
+    def run(self, s):
+        nrm, w, p = self.nrm, self.w, self.params
+        if w.op == "add_rms":
+            nrm.add_rms_fwd(s["x"], s["residual"], p["w"], w.eps, residual_out=s["residual_out"],
+                            out=s["y"], rstd=s["rstd"])
+        elif w.op == "ln":
+            nrm.ln_fwd(s["x"], p["gamma"], p["beta"], w.eps, out=s["y"], mean=s["mean"],
+                       rstd=s["rstd"])
+        elif w.op == "rms":
+            nrm.rms_fwd(s["x"], p["w"], w.eps, out=s["y"], rstd=s["rstd"])
+        else:
+            nrm.bn_fwd_train(s["x"], p["gamma"], p["beta"], p["running_mean"], p["running_var"],
+                             w.eps, w.momentum, out=s["y"], save_mean=s["save_mean"],
+                             save_rstd=s["save_rstd"], workspace=s["ws"])
+
+
+def capture(step: Step, n: int, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            step()
+    return g
+
+
+def time_graphs(step: Step, k: int, warmup: int, stream, chunk=1000, dist=None):
+    """Replay exactly k steps from CUDA graphs; return (seconds, t0, t1)."""
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    full, rem = divmod(k, chunk)
+    g_full = capture(step, chunk, stream) if full else None
+    g_rem = capture(step, rem, stream) if rem else None
+    g_warm = capture(step, max(warmup, 1), stream)
+    torch.cuda.synchronize()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    return ev0.elapsed_time(ev1) / 1e3, t0, t1
+
+
+def time_e2e(w: W.Workload, device, steps: int):
+    """Through the public API with host buffers: per step, H2D copy of the step's
+    inputs from pinned memory, the call, D2H copy of its outputs."""
+    import row_wise_normalization_reduce_gb300 as nrm
+    inp = W.make_inputs(w)
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    dev = {k: torch.empty_like(v, device=device) for k, v in inp.items()}
+    params = [k for k in dev if k not in ("x", "residual")]
+    for k in params:
+        dev[k].copy_(host[k])
+    if w.op == "add_rms":
+        outs = {"residual_out": torch.empty_like(dev["x"]), "y": torch.empty_like(dev["x"])}
+    else:
+        outs = {"y": torch.empty_like(dev["x"])}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    in_keys = ["x"] + (["residual"] if w.op == "add_rms" else [])
+    h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    stream = torch.cuda.current_stream(device)
+
+    def one():
+        for k in in_keys:
+            dev[k].copy_(host[k], non_blocking=True)
+        if w.op == "add_rms":
+            nrm.add_rms_fwd(dev["x"], dev["residual"], dev["w"], w.eps,
+                            residual_out=outs["residual_out"], out=outs["y"])
+        elif w.op == "ln":
+            nrm.ln_fwd(dev["x"], dev["gamma"], dev["beta"], w.eps, out=outs["y"],
+                       want_stats=False)
+        elif w.op == "rms":
+            nrm.rms_fwd(dev["x"], dev["w"], w.eps, out=outs["y"])
+        for k, v in outs.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        one()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sec = ev0.elapsed_time(ev1) / 1e3 / steps
+    return sec, h2d, d2h
+
+
+def l2_size(device_index) -> int:
+    try:
+        return int(torch.cuda.get_device_properties(device_index).L2_cache_size)
+    except AttributeError:
+        return 126 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_time(w: W.Workload, rows_sample: int, reps: int, threads: int):
+    """Time the CPU oracle on the first rows_sample rows of the workload,
+    partitioned by rows over `threads` threads (the oracle code itself unchanged).
+    Returns (seconds per rep, bytes per rep)."""
+    import concurrent.futures as cf
+    import oracle
+    orc = oracle.default()
+    inp = W.make_inputs(w)
+    to_np = (lambda t: t.numpy() if t.dtype == torch.float32
+             else t.view(torch.int16).numpy().view(np.uint16))
+    dt = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}[w.torch_dtype]
+    x = to_np(inp["x"][:rows_sample].contiguous())
+    rows = x.shape[0]
+    res = to_np(inp["residual"][:rows_sample].contiguous()) if w.op == "add_rms" else None
+    prm = {k: to_np(v) for k, v in inp.items() if k not in ("x", "residual")}
+    chunks = np.array_split(np.arange(rows), threads)
+
+    def work(idx):
+        if len(idx) == 0:
+            return
+        a, b = idx[0], idx[-1] + 1
+        if w.op == "add_rms":
+            orc.add_rmsnorm(dt, x[a:b], res[a:b], prm["w"], eps=w.eps)
+        elif w.op == "ln":
+            orc.layernorm(dt, x[a:b], prm["gamma"], prm["beta"], eps=w.eps)
+        elif w.op == "rms":
+            orc.rmsnorm(dt, x[a:b], prm["w"], eps=w.eps)
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, chunks))  # warm-up
+        times = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            list(ex.map(work, chunks))
+            times.append(time.perf_counter() - t0)
+    frac = rows / w.shape[0]
+    return statistics.median(times), algorithmic_bytes(w) * frac
+
+
+# ---------------------------------------------------------------------------
+def emit(line: dict):
+    print(json.dumps(line), flush=True)
+
+
+def base_line(args, w, world):
+    return {"metric": METRIC, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded torch.Generator)"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    # size each step so the whole run stays within about two minutes
+    probe_rows = min(w.shape[0], threads)
+    t_probe, _ = oracle_time(w, probe_rows, 1, threads)
+    budget = 120.0 / (args.steps + args.warmup)
+    rows = int(max(1, min(w.shape[0], probe_rows * budget / max(t_probe, 1e-9))))
+    if args.warmup:
+        oracle_time(w, rows, args.warmup, threads)
+    sec, nbytes = oracle_time(w, rows, max(args.steps, 1), threads)
+    gbs = nbytes / sec / 1e9
+    line = base_line(args, w, world)
+    line.update({
+        "impl": "reference", "value": gbs, "ms_per_step": sec * 1e3,
+        "config": {"workload": w.name, "shape": list(w.shape), "dtype": w.dtype,
+                   "sample_rows": rows, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {w.shape[0]} rows per step, fp64 oracle, "
+                                   f"rows split over {threads} threads"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    })
+    emit(line)
+
+
+def secondary(args, device, stream, l2):
+    out = []
+    for w in (W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384,
+              W.BN_F32_32x64x56x56, W.LN_F32_64x1024):
+        st = Step(w, device, l2)
+        k = 2000
+        sec, _, _ = time_graphs(st, k, 20, stream)
+        per = sec / k
+        b = algorithmic_bytes(w)
+        peak, _ = measured_peak()
+        out.append({"workload": w.name, "us_per_call": per * 1e6, "gbs": b / per / 1e9,
+                    "frac_of_measured_peak": b / per / 1e9 / peak,
+                    "frac_of_8tbs": b / per / 1e9 / 8000.0, "bytes": b,
+                    "launches_per_call": st.launches_per_step})
+        del st
+        torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="nrm", choices=["nrm", "reference"])
+    ap.add_argument("--workload", default=W.ADD_RMS_BF16_4096x4096.name, choices=list(W.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    w = W.BY_NAME[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import row_wise_normalization_reduce_gb300 as nrm
+    nrm.lib()
+    stream = torch.cuda.Stream(device)
+    l2 = l2_size(local)
+
+    step = Step(w, device, l2)
+    sampler = ClockSampler(local)
+    sampler.start()
+    sec, t0, t1 = time_graphs(step, args.steps, args.warmup, stream, dist=dist)
+    sampler.stop()
+    if dist is not None:
+        t = torch.tensor([sec], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    per_step = sec / args.steps
+    nbytes = algorithmic_bytes(w)
+    value = world * args.steps * nbytes / sec / 1e9
+    peak, peak_src = measured_peak()
+    kernel_gbs = nbytes / (per_step / step.launches_per_step) / 1e9 if step.launches_per_step == 1 \
+        else nbytes / per_step / 1e9
+    traffic = ncu_traffic(w.name)
+
+    e2e = None
+    if not args.no_e2e and w.op != "bn":
+        es, h2d, d2h = time_e2e(w, device, 20)
+        e2e = {"value": world * nbytes / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": es * 1e3}
+
+    sec_lines = None
+    if rank == 0 and not args.no_secondary:
+        sec_lines = secondary(args, device, stream, l2)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and w.op != "bn":
+        rows = w.shape[0]
+        cs, cb = oracle_time(w, rows, 3, 1)
+        cpu = {"value": cb / cs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "us_per_call": cs * 1e6,
+               "sample": f"the full {rows}-row workload, fp64 oracle, one thread, "
+                         f"median of 3 after 1 warm-up"}
+
+    if rank == 0:
+        line = base_line(args, w, world)
+        line.update({
+            "value": value, "ms_per_step": per_step * 1e3, "us_per_call": per_step * 1e6,
+            "config": {"workload": w.name, "shape": list(w.shape), "dtype": w.dtype,
+                       "eps": w.eps, "parallelism": f"replicas x{world} (rows are independent)",
+                       "l2": f"cold: {step.nsets} rotating input sets "
+                             f"({step.nsets * nbytes / 1e6:.0f} MB) > L2 ({l2 / 1e6:.0f} MB)",
+                       "timing": "CUDA graphs replaying exactly K calls between CUDA events"},
+            "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": kernel_gbs / peak, "peak_source": peak_src,
+                         "frac_of_nominal_8tbs": kernel_gbs / 8000.0,
+                         "algorithmic_bytes_per_launch": nbytes, "traffic": traffic},
+            "gpu_launches": args.steps * step.launches_per_step,
+            "clocks": sampler.summary(t0, t1),
+            "plan": nrm.PLAN_NAMES.get(nrm.last_plan()[0]),
+        })
+        if e2e is not None:
+            line["e2e"] = e2e
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if sec_lines is not None:
+            line["secondary"] = sec_lines
+        emit(line)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

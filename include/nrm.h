@@ -1,0 +1,200 @@
+/*
+ * nrm.h -- C ABI of the row-wise normalization library for GB300 (sm_103a).
+ *
+ * Four forward operators, each one asynchronous launch sequence on the
+ * caller's CUDA stream:
+ *   ln_fwd        LayerNorm over the rows of a [rows, N] tensor
+ *   rms_fwd       RMSNorm over the rows of a [rows, N] tensor
+ *   add_rms_fwd   fused residual add + RMSNorm (pre-norm residual stream)
+ *   bn_fwd_train  BatchNorm2d training forward over an NCHW tensor
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every data pointer is CALLER-OWNED DEVICE memory of the current
+ *   CUDA device (cudaGetDevice at call time).  The library allocates nothing
+ *   and keeps no per-call state; it only caches device attributes.  A host
+ *   pointer is not detected unless pointer checks are switched on
+ *   (nrm_set_pointer_checks); without them it makes the kernel fault.
+ * Layout.  Row operators: row-major [rows, N], contiguous (row stride N).
+ *   BatchNorm: NCHW with H*W flattened to HW; element (n, c, k) at
+ *   ((n*C + c)*HW + k).  Parameters (gamma, beta, w) are [N] (rows ops) or
+ *   [C] (BatchNorm) in the I/O type; statistics are always binary32.
+ * Types.  dtype is an nrm_dtype: binary32, binary16 or bfloat16 for the
+ *   data and the parameters.  All arithmetic is binary32; every output is
+ *   rounded once to its type, round-to-nearest-even.
+ * Optional pointers.  gamma/w NULL means 1, beta NULL means 0; NULL mean,
+ *   rstd, save_mean, save_rstd means "do not write"; NULL running_mean or
+ *   running_var means "no running-statistic update".
+ * Alignment.  Any alignment and any N are accepted.  The vectorised kernels
+ *   (16-byte loads and stores) run when every row pointer is 16-byte aligned
+ *   and N is a multiple of 16/sizeof(element); otherwise a scalar kernel runs.
+ * Aliasing.  Outputs may not overlap inputs or each other, with one
+ *   exception: add_rms_fwd accepts residual_out == residual (the residual
+ *   stream updated in place).  Any other overlap returns NRM_ERR_ALIAS.
+ * Errors.  Arguments are validated before anything is launched; an invalid
+ *   call returns a non-zero nrm_status and launches nothing.  After the
+ *   launch, cudaGetLastError is checked (NRM_ERR_LAUNCH).  Errors raised
+ *   later by the kernels (for example a fault from a bad pointer) surface on
+ *   the stream, as with any CUDA launch.
+ * Streams.  Calls are asynchronous on `stream` (0 = legacy default stream)
+ *   and never synchronize.  Calls are thread-safe.
+ * Empty input.  rows == 0 is a no-op that returns NRM_OK (row operators),
+ *   whatever the pointers (empty tensors may have NULL data).
+ */
+#ifndef NRM_H
+#define NRM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NRM_F32 = 0,   /* IEEE binary32 */
+    NRM_F16 = 1,   /* IEEE binary16 */
+    NRM_BF16 = 2   /* bfloat16 */
+} nrm_dtype;
+
+typedef enum {
+    NRM_OK = 0,
+    NRM_ERR_NULL = 1,          /* a required pointer is NULL */
+    NRM_ERR_SHAPE = 2,         /* negative extent, N < 1, size overflow, BN count < 2 */
+    NRM_ERR_DTYPE = 3,         /* dtype is not an nrm_dtype */
+    NRM_ERR_ALIAS = 4,         /* an output overlaps an input or another output */
+    NRM_ERR_VALUE = 5,         /* eps < 0 or not finite; momentum outside [0, 1];
+                                  a pointer not aligned to its element size */
+    NRM_ERR_UNSUPPORTED = 6,   /* valid but not provided (e.g. a forced plan that
+                                  cannot run this shape) */
+    NRM_ERR_WORKSPACE = 7,     /* BatchNorm workspace NULL, too small or misaligned */
+    NRM_ERR_DEVICE = 8,        /* no current CUDA device or attribute query failed */
+    NRM_ERR_LAUNCH = 9,        /* cudaGetLastError reported a launch failure */
+    NRM_ERR_POINTER = 10       /* pointer checks on, and a pointer is not device
+                                  memory of the current device */
+} nrm_status;
+
+/*
+ * LayerNorm forward over each row of x[rows, N]:
+ *   mean = (1/N) sum_i x_i,   var = (1/N) sum_i (x_i - mean)^2   (biased)
+ *   y_i  = (x_i - mean) / sqrt(var + eps) * gamma_i + beta_i
+ * Definition: CUDA handbook LayerNorm walkthrough (lpnh.cn/news/2756757), §1;
+ * optional gamma/beta and the statistics outputs as in its §2 and §7.
+ *   x      [rows, N] dtype, read only
+ *   gamma  [N] dtype or NULL (= 1);  beta [N] dtype or NULL (= 0)
+ *   y      [rows, N] dtype, written; must not overlap x
+ *   mean   [rows] binary32 or NULL;  rstd [rows] binary32 = 1/sqrt(var+eps), or NULL
+ *   eps    >= 0, finite
+ * Returns an nrm_status.
+ */
+int ln_fwd(const void *x, const void *gamma, const void *beta, void *y,
+           float *mean, float *rstd, int64_t rows, int64_t N, float eps,
+           int dtype, cudaStream_t stream);
+
+/*
+ * RMSNorm forward over each row of x[rows, N]:
+ *   y_i = x_i / sqrt((1/N) sum_j x_j^2 + eps) * w_i
+ * Definition: CUDA fused RMSNorm kernel page (diycv.top), §0.3 and §1-§2.
+ *   x [rows, N] dtype;  w [N] dtype or NULL (= 1);  y [rows, N] dtype
+ *   rstd [rows] binary32 = 1/sqrt(mean(x^2)+eps), or NULL
+ */
+int rms_fwd(const void *x, const void *w, void *y, float *rstd,
+            int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream);
+
+/*
+ * Fused pre-norm path over each row:
+ *   residual_out = round_to_dtype(binary32(x) + binary32(residual))
+ *   y            = RMSNorm(residual_out, w)
+ * The statistics use the rounded residual_out, the value the residual stream
+ * carries on.  Definition: CUDA fused RMSNorm kernel page (diycv.top), §2 and §3.2.
+ *   x, residual   [rows, N] dtype, read only
+ *   w             [N] dtype or NULL (= 1)
+ *   residual_out  [rows, N] dtype, written; may be the same pointer as residual
+ *   y             [rows, N] dtype, written
+ *   rstd          [rows] binary32, or NULL
+ */
+int add_rms_fwd(const void *x, const void *residual, const void *w,
+                void *residual_out, void *y, float *rstd,
+                int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace bn_fwd_train needs for this shape (0 on invalid
+ * arguments).  The workspace holds per-(n, c) partial statistics; its content
+ * on entry does not matter and it is scratch on exit.
+ */
+size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype);
+
+/*
+ * BatchNorm2d training forward over x[batch, C, HW] (NCHW).  Per channel c,
+ * over all n and k (cnt = batch*HW):
+ *   mean_c = (1/cnt) sum x,   var_c = (1/cnt) sum (x - mean_c)^2   (biased)
+ *   y = (x - mean_c) / sqrt(var_c + eps) * gamma_c + beta_c
+ *   save_mean[c] = mean_c,   save_rstd[c] = 1/sqrt(var_c + eps)
+ *   running_mean[c] = (1 - momentum)*running_mean[c] + momentum*mean_c
+ *   running_var[c]  = (1 - momentum)*running_var[c]  + momentum*var_c*cnt/(cnt-1)
+ * Definition: BatchNorm CUDA implementation walkthrough (jianying88.com/news/30214),
+ * §2.1 (forward) and §2.4 (training statistics, running mean).  The page gives
+ * no running-variance rule; the unbiased update above is the torch.nn.BatchNorm2d
+ * convention that page sets out to replace.
+ *   x            [batch, C, HW] dtype (binary32 only in this version)
+ *   gamma, beta  [C] dtype or NULL
+ *   y            [batch, C, HW] dtype, must not overlap x
+ *   save_mean, save_rstd        [C] binary32 or NULL
+ *   running_mean, running_var   [C] binary32, read and updated in place, or NULL
+ *   batch >= 1, C >= 1, HW >= 1, batch*HW >= 2; eps >= 0; 0 <= momentum <= 1
+ *   workspace    device memory, 16-byte aligned, at least
+ *                bn_fwd_train_workspace_size(batch, C, HW, dtype) bytes, owned
+ *                by the caller; calls that share one workspace must be ordered
+ *                on the GPU (same stream or events), or they race.
+ */
+int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y,
+                 float *save_mean, float *save_rstd, float *running_mean,
+                 float *running_var, int64_t batch, int64_t C, int64_t HW,
+                 float eps, float momentum, int dtype, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char *nrm_status_string(int status);
+
+/*
+ * Kernel plans of the row operators, for tests and measurements.  The
+ * default, NRM_PLAN_AUTO, lets the library pick by N, dtype and alignment.
+ */
+typedef enum {
+    NRM_PLAN_AUTO = 0,
+    NRM_PLAN_GENERIC = 1,   /* one CTA per row, scalar, two reads of the row */
+    NRM_PLAN_WARP = 2,      /* one warp per row, row held in registers */
+    NRM_PLAN_CTA = 3        /* one CTA per row, row held in registers */
+} nrm_plan;
+
+/*
+ * Force a plan (and, where non-zero, the CTA size and the 16-byte packs per
+ * thread) for every later row-operator call in this process; plan 0 restores
+ * automatic choice.  A forced plan that cannot run a given call makes that
+ * call return NRM_ERR_UNSUPPORTED.  Returns NRM_OK or NRM_ERR_UNSUPPORTED for
+ * an unknown plan.  Process-wide; not meant to change while calls run.
+ */
+int nrm_force_plan(int plan, int threads, int packs);
+
+/*
+ * Plan, CTA size and packs per thread chosen by this thread's most recent
+ * successful row-operator call (written to the non-NULL pointers).
+ */
+void nrm_last_plan(int *plan, int *threads, int *packs);
+
+/*
+ * Switch pointer checks on (1) or off (0, the default).  When on, every call
+ * asks cudaPointerGetAttributes about each non-NULL pointer and returns
+ * NRM_ERR_POINTER, before launching, if one is not device (or managed) memory
+ * of the current device.  Costs a few microseconds per call.  Returns the
+ * previous setting.
+ */
+int nrm_set_pointer_checks(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NRM_H */

@@ -1,1 +1,16 @@
-"""Row-wise normalization reduce for GB300 (sm_103a)."""
+"""Row-wise normalization reduce for GB300 (sm_103a).
+
+LayerNorm, RMSNorm, fused residual-add + RMSNorm and BatchNorm2d training
+forward, computed by the hand-written CUDA kernels of libnrm.so (C ABI in
+include/nrm.h).  This package is the thin Python binding over that library.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH, NRM_BF16, NRM_F16, NRM_F32, PLAN_AUTO, PLAN_CTA, PLAN_GENERIC, PLAN_NAMES,
+    PLAN_WARP, NrmError, add_rms_fwd, bn_fwd_train, bn_fwd_train_workspace_size, force_plan,
+    last_plan, lib, ln_fwd, rms_fwd, set_pointer_checks, status_string)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libnrm.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force, verbose=verbose)

@@ -1,0 +1,229 @@
+"""ctypes binding of libnrm.so (include/nrm.h).
+
+Argument marshalling only: every step of every operator runs in the CUDA
+library.  torch provides the device memory and the current stream.  If the
+library is missing the first call raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnrm.so")
+
+NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
+PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA = 0, 1, 2, 3
+PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta"}
+
+_DT = {torch.float32: NRM_F32, torch.float16: NRM_F16, torch.bfloat16: NRM_BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_INT = ctypes.c_int
+
+
+class NrmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+def _declare(lib):
+    lib.ln_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _INT, _P]
+    lib.rms_fwd.argtypes = [_P, _P, _P, _P, _I64, _I64, _F, _INT, _P]
+    lib.add_rms_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _INT, _P]
+    lib.bn_fwd_train_workspace_size.argtypes = [_I64, _I64, _I64, _INT]
+    lib.bn_fwd_train_workspace_size.restype = ctypes.c_size_t
+    lib.bn_fwd_train.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _INT,
+                                 _P, ctypes.c_size_t, _P]
+    for f in ("ln_fwd", "rms_fwd", "add_rms_fwd", "bn_fwd_train"):
+        getattr(lib, f).restype = _INT
+    lib.nrm_status_string.argtypes = [_INT]
+    lib.nrm_status_string.restype = ctypes.c_char_p
+    lib.nrm_force_plan.argtypes = [_INT, _INT, _INT]
+    lib.nrm_force_plan.restype = _INT
+    lib.nrm_last_plan.argtypes = [ctypes.POINTER(_INT)] * 3
+    lib.nrm_last_plan.restype = None
+    lib.nrm_set_pointer_checks.argtypes = [_INT]
+    lib.nrm_set_pointer_checks.restype = _INT
+    return lib
+
+
+def lib():
+    """The loaded libnrm.so (ctypes.CDLL).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it first "
+                        "(python -c 'import __graft_entry__ as g; g.build()')")
+                _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nrm_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise NrmError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _param(p, n, dtype, device, name):
+    if p is None:
+        return None
+    _cuda(p, name)
+    if p.dtype != dtype or p.numel() != n or p.device != device:
+        raise ValueError(f"{name} must be [{n}] {dtype} on {device}")
+    return p
+
+
+def _rows_view(x: torch.Tensor):
+    n = x.shape[-1]
+    return x.numel() // n if n else 0, n
+
+
+# ---------------------------------------------------------------------------
+# Operators (same names as the C ABI).
+# ---------------------------------------------------------------------------
+def ln_fwd(x, gamma=None, beta=None, eps=1e-5, *, out=None, mean=None, rstd=None,
+           want_stats=True, stream=None):
+    """LayerNorm over the last dimension of x.  Returns (y, mean, rstd)."""
+    _cuda(x, "x")
+    rows, n = _rows_view(x)
+    gamma = _param(gamma, n, x.dtype, x.device, "gamma")
+    beta = _param(beta, n, x.dtype, x.device, "beta")
+    y = torch.empty_like(x) if out is None else out
+    if want_stats:
+        mean = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32) if mean is None else mean
+        rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32) if rstd is None else rstd
+    with torch.cuda.device(x.device):
+        st = lib().ln_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                          rows, n, eps, _dtype_code(x),
+                          stream if stream is not None else _stream(x.device))
+    _check(st, "ln_fwd")
+    return y, mean, rstd
+
+
+def rms_fwd(x, w=None, eps=1e-6, *, out=None, rstd=None, want_stats=False, stream=None):
+    """RMSNorm over the last dimension of x.  Returns (y, rstd or None)."""
+    _cuda(x, "x")
+    rows, n = _rows_view(x)
+    w = _param(w, n, x.dtype, x.device, "w")
+    y = torch.empty_like(x) if out is None else out
+    if want_stats and rstd is None:
+        rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+    with torch.cuda.device(x.device):
+        st = lib().rms_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), rows, n, eps, _dtype_code(x),
+                           stream if stream is not None else _stream(x.device))
+    _check(st, "rms_fwd")
+    return y, rstd
+
+
+def add_rms_fwd(x, residual, w=None, eps=1e-6, *, residual_out=None, out=None, rstd=None,
+                want_stats=False, stream=None):
+    """residual_out = x + residual (rounded to x.dtype); y = RMSNorm(residual_out, w).
+    Returns (residual_out, y, rstd or None).  Pass residual_out=residual to update
+    the residual stream in place."""
+    _cuda(x, "x")
+    _cuda(residual, "residual")
+    if residual.shape != x.shape or residual.dtype != x.dtype:
+        raise ValueError("residual must match x in shape and dtype")
+    rows, n = _rows_view(x)
+    w = _param(w, n, x.dtype, x.device, "w")
+    ro = torch.empty_like(x) if residual_out is None else residual_out
+    y = torch.empty_like(x) if out is None else out
+    if want_stats and rstd is None:
+        rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+    with torch.cuda.device(x.device):
+        st = lib().add_rms_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(ro), _ptr(y), _ptr(rstd),
+                               rows, n, eps, _dtype_code(x),
+                               stream if stream is not None else _stream(x.device))
+    _check(st, "add_rms_fwd")
+    return ro, y, rstd
+
+
+def bn_fwd_train_workspace_size(batch, c, hw, dtype=torch.float32) -> int:
+    return lib().bn_fwd_train_workspace_size(batch, c, hw, _DT[dtype])
+
+
+def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, eps=1e-5,
+                 momentum=0.1, *, out=None, save_mean=None, save_rstd=None, workspace=None,
+                 stream=None):
+    """BatchNorm2d training forward over NCHW x.  Returns (y, save_mean, save_rstd);
+    running_mean / running_var (binary32) are updated in place when given."""
+    _cuda(x, "x")
+    if x.dim() < 2:
+        raise ValueError("x must be [batch, C, ...]")
+    batch, c = x.shape[0], x.shape[1]
+    hw = x.numel() // (batch * c) if batch * c else 0
+    gamma = _param(gamma, c, x.dtype, x.device, "gamma")
+    beta = _param(beta, c, x.dtype, x.device, "beta")
+    for t, name in ((running_mean, "running_mean"), (running_var, "running_var")):
+        if t is not None:
+            _cuda(t, name)
+            if t.dtype != torch.float32 or t.numel() != c:
+                raise ValueError(f"{name} must be [{c}] float32")
+    y = torch.empty_like(x) if out is None else out
+    save_mean = torch.empty(c, device=x.device, dtype=torch.float32) if save_mean is None else save_mean
+    save_rstd = torch.empty(c, device=x.device, dtype=torch.float32) if save_rstd is None else save_rstd
+    need = lib().bn_fwd_train_workspace_size(batch, c, hw, _dtype_code(x))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    with torch.cuda.device(x.device):
+        st = lib().bn_fwd_train(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(save_mean),
+                                _ptr(save_rstd), _ptr(running_mean), _ptr(running_var), batch, c,
+                                hw, eps, momentum, _dtype_code(x), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(),
+                                stream if stream is not None else _stream(x.device))
+    _check(st, "bn_fwd_train")
+    return y, save_mean, save_rstd
+
+
+# ---------------------------------------------------------------------------
+# Plan control (tests and measurements).
+# ---------------------------------------------------------------------------
+def force_plan(plan: int = PLAN_AUTO, threads: int = 0, packs: int = 0):
+    _check(lib().nrm_force_plan(plan, threads, packs), "nrm_force_plan")
+
+
+def last_plan():
+    p, t, k = _INT(), _INT(), _INT()
+    lib().nrm_last_plan(ctypes.byref(p), ctypes.byref(t), ctypes.byref(k))
+    return p.value, t.value, k.value
+
+
+def set_pointer_checks(enable: bool) -> bool:
+    return bool(lib().nrm_set_pointer_checks(1 if enable else 0))

@@ -1,0 +1,380 @@
+// api.cpp -- the C ABI (include/nrm.h): argument validation, the per-shape
+// plan choice and the launches.  Argument checks follow the extension
+// boundary of the CUDA fused RMSNorm kernel page (diycv.top, §5: device,
+// contiguity, shape and type checks, current stream, launch check) and the
+// edge-case list of the LayerNorm walkthrough (lpnh.cn/news/2756757, §7:
+// N not a multiple of the vector width, optional gamma/beta, no in-place
+// y == x, check the launch).
+#include <cuda_runtime_api.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <initializer_list>
+#include <mutex>
+
+#include "nrm.h"
+#include "nrm_internal.h"
+
+using namespace nrm;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Device attributes, queried once per device.
+// ---------------------------------------------------------------------------
+struct DevInfo {
+    int sms = 0;
+    bool ok = false;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+int device_info(DevInfo *out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NRM_ERR_DEVICE;
+    }
+    std::call_once(g_dev_once[dev], [dev]() {
+        DevInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            d.sms > 0)
+            d.ok = true;
+        else
+            cudaGetLastError();
+        g_dev[dev] = d;
+    });
+    if (!g_dev[dev].ok) return NRM_ERR_DEVICE;
+    *out = g_dev[dev];
+    return NRM_OK;
+}
+
+std::atomic<int> g_force_kind{0}, g_force_threads{0}, g_force_packs{0};
+std::atomic<int> g_pointer_checks{0};
+thread_local int t_last_kind = 0, t_last_threads = 0, t_last_packs = 0;
+
+size_t elem_size(int dtype) { return dtype == NRM_F32 ? 4 : 2; }
+bool dtype_ok(int dtype) { return dtype == NRM_F32 || dtype == NRM_F16 || dtype == NRM_BF16; }
+
+// [p, p + bytes) as integers, for overlap tests.
+struct Span {
+    uintptr_t lo = 0, hi = 0;
+    bool live() const { return hi > lo; }
+};
+Span span(const void *p, size_t bytes) {
+    Span s;
+    if (p && bytes) {
+        s.lo = reinterpret_cast<uintptr_t>(p);
+        s.hi = s.lo + bytes;
+    }
+    return s;
+}
+bool overlap(const Span &a, const Span &b) {
+    return a.live() && b.live() && a.lo < b.hi && b.lo < a.hi;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_pointer(const void *p) {
+    if (!p) return NRM_OK;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return NRM_ERR_POINTER;
+    }
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (attr.type == cudaMemoryTypeManaged) return NRM_OK;
+    if (attr.type != cudaMemoryTypeDevice || attr.device != dev) return NRM_ERR_POINTER;
+    return NRM_OK;
+}
+
+int check_pointers(std::initializer_list<const void *> ps) {
+    if (!g_pointer_checks.load(std::memory_order_relaxed)) return NRM_OK;
+    for (const void *p : ps) {
+        int st = check_pointer(p);
+        if (st != NRM_OK) return st;
+    }
+    return NRM_OK;
+}
+
+bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.f; }
+
+// ---------------------------------------------------------------------------
+// Plan choice for the row operators.
+// ---------------------------------------------------------------------------
+int round_up_pow2(int64_t v) {
+    int r = 1;
+    while (r < v && r < (1 << 20)) r <<= 1;
+    return r;
+}
+
+// Vectorized plans need every row pointer 16-byte aligned and N a multiple of
+// the pack width (16 bytes of elements).
+int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *plan) {
+    (void)op;
+    const int64_t V = 16 / (int64_t)elem_size(dtype);
+    const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16) &&
+                        (!a.res || aligned(a.res, 16)) && (!a.res_out || aligned(a.res_out, 16)) &&
+                        (!a.p0 || aligned(a.p0, 16)) && (!a.p1 || aligned(a.p1, 16));
+    const int64_t P = vec_ok ? a.N / V : 0;
+    const int64_t kMaxGrid = 0x7fffffff;
+
+    int kind = g_force_kind.load(std::memory_order_relaxed);
+    int fthreads = g_force_threads.load(std::memory_order_relaxed);
+    int fpacks = g_force_packs.load(std::memory_order_relaxed);
+
+    if (kind == PLAN_AUTO) {
+        if (!vec_ok)
+            kind = PLAN_GENERIC;
+        else if (P <= 32 * 8 && a.rows >= 4 * (int64_t)dev.sms)
+            kind = PLAN_WARP;
+        else if (P <= 1024 * 4)
+            kind = PLAN_CTA;
+        else
+            kind = PLAN_GENERIC;
+        fthreads = fpacks = 0;
+    }
+
+    Plan p{kind, 0, 0, 0};
+    switch (kind) {
+    case PLAN_GENERIC: {
+        p.threads = fthreads ? fthreads : (a.N >= 4096 ? 512 : 256);
+        p.packs = 1;
+        p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
+        break;
+    }
+    case PLAN_WARP: {
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        int packs = fpacks;
+        if (!packs) {
+            const int64_t need = (P + 31) / 32;
+            packs = need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
+        }
+        if ((int64_t)packs * 32 < P) return NRM_ERR_UNSUPPORTED;
+        p.threads = 128;
+        p.packs = packs;
+        const int64_t g = (a.rows + 3) / 4;
+        p.grid = g < kMaxGrid ? g : kMaxGrid;
+        break;
+    }
+    case PLAN_CTA: {
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        int packs = fpacks, threads = fthreads;
+        if (!packs) packs = P <= 512 ? 1 : P <= 1024 ? 2 : 4;
+        if (!threads) {
+            threads = round_up_pow2((P + packs - 1) / packs);
+            if (threads < 128) threads = 128;
+        }
+        if (threads > 1024 || (int64_t)threads * packs < P) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
+        break;
+    }
+    default:
+        return NRM_ERR_UNSUPPORTED;
+    }
+    *plan = p;
+    return NRM_OK;
+}
+
+int run_row(Op op, const RowArgs &a, int dtype, cudaStream_t stream) {
+    DevInfo dev;
+    int st = device_info(&dev);
+    if (st != NRM_OK) return st;
+    Plan plan;
+    st = choose_plan(op, a, dtype, dev, &plan);
+    if (st != NRM_OK) return st;
+    cudaError_t e;
+    switch (op) {
+    case OP_LN: e = launch_ln(a, plan, dtype, stream); break;
+    case OP_RMS: e = launch_rms(a, plan, dtype, stream); break;
+    default: e = launch_add_rms(a, plan, dtype, stream); break;
+    }
+    if (e == cudaErrorInvalidConfiguration) {
+        cudaGetLastError();
+        return NRM_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return NRM_ERR_LAUNCH;
+    t_last_kind = plan.kind;
+    t_last_threads = plan.threads;
+    t_last_packs = plan.packs;
+    return NRM_OK;
+}
+
+// Shared validation of the row operators: extents, type, alignment to the
+// element size, eps.  Fills the byte size of one [rows, N] tensor.
+int validate_rows(int64_t rows, int64_t N, float eps, int dtype, size_t *tensor_bytes) {
+    if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
+    if (rows < 0 || N < 1) return NRM_ERR_SHAPE;
+    const size_t es = elem_size(dtype);
+    if (rows > 0 && (uint64_t)N > (uint64_t)INT64_MAX / (uint64_t)rows / es) return NRM_ERR_SHAPE;
+    if (!eps_ok(eps)) return NRM_ERR_VALUE;
+    *tensor_bytes = (size_t)rows * (size_t)N * es;
+    return NRM_OK;
+}
+
+int check_elem_alignment(std::initializer_list<const void *> ps, size_t es) {
+    for (const void *p : ps)
+        if (p && !aligned(p, es)) return NRM_ERR_VALUE;
+    return NRM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
+           float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    size_t tb = 0;
+    int st = validate_rows(rows, N, eps, dtype, &tb);
+    if (st != NRM_OK) return st;
+    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
+    if (!x || !y) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({mean, rstd}, 4)) != NRM_OK) return st;
+    const Span sx = span(x, tb), sy = span(y, tb), sg = span(gamma, N * es),
+               sb = span(beta, N * es), sm = span(mean, rows * 4), sr = span(rstd, rows * 4);
+    for (const Span &o : {sy, sm, sr})
+        for (const Span &i : {sx, sg, sb})
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    if (overlap(sy, sm) || overlap(sy, sr) || overlap(sm, sr)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, gamma, beta, y, mean, rstd})) != NRM_OK) return st;
+    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps};
+    return run_row(OP_LN, a, dtype, stream);
+}
+
+int rms_fwd(const void *x, const void *w, void *y, float *rstd, int64_t rows, int64_t N,
+            float eps, int dtype, cudaStream_t stream) {
+    size_t tb = 0;
+    int st = validate_rows(rows, N, eps, dtype, &tb);
+    if (st != NRM_OK) return st;
+    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
+    if (!x || !y) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x, w, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({rstd}, 4)) != NRM_OK) return st;
+    const Span sx = span(x, tb), sy = span(y, tb), sw = span(w, N * es), sr = span(rstd, rows * 4);
+    for (const Span &o : {sy, sr})
+        for (const Span &i : {sx, sw})
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    if (overlap(sy, sr)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, w, y, rstd})) != NRM_OK) return st;
+    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps};
+    return run_row(OP_RMS, a, dtype, stream);
+}
+
+int add_rms_fwd(const void *x, const void *residual, const void *w, void *residual_out, void *y,
+                float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    size_t tb = 0;
+    int st = validate_rows(rows, N, eps, dtype, &tb);
+    if (st != NRM_OK) return st;
+    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
+    if (!x || !residual || !residual_out || !y) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x, residual, w, residual_out, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({rstd}, 4)) != NRM_OK) return st;
+    const Span sx = span(x, tb), sres = span(residual, tb), sw = span(w, N * es),
+               sro = span(residual_out, tb), sy = span(y, tb), sr = span(rstd, rows * 4);
+    // residual_out may be exactly residual (in-place residual stream)
+    const bool inplace = residual_out == residual;
+    for (const Span &i : {sx, sw})
+        for (const Span &o : {sro, sy, sr})
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    if (!inplace && overlap(sro, sres)) return NRM_ERR_ALIAS;
+    if (overlap(sy, sres) || overlap(sr, sres)) return NRM_ERR_ALIAS;
+    if (overlap(sro, sy) || overlap(sro, sr) || overlap(sy, sr)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, residual, w, residual_out, y, rstd})) != NRM_OK) return st;
+    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps};
+    return run_row(OP_ADD_RMS, a, dtype, stream);
+}
+
+size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
+    if (!dtype_ok(dtype) || batch < 1 || C < 1 || HW < 1) return 0;
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / 8 / (uint64_t)C) return 0;
+    return (size_t)batch * (size_t)C * 8;
+}
+
+int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
+                 float *save_rstd, float *running_mean, float *running_var, int64_t batch,
+                 int64_t C, int64_t HW, float eps, float momentum, int dtype, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+    if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
+    if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
+    const size_t es = elem_size(dtype);
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / es)
+        return NRM_ERR_SHAPE;
+    if (batch * HW < 2) return NRM_ERR_SHAPE;
+    if (!eps_ok(eps) || !(momentum >= 0.f && momentum <= 1.f)) return NRM_ERR_VALUE;
+    if (!x || !y) return NRM_ERR_NULL;
+    if (dtype != NRM_F32) return NRM_ERR_UNSUPPORTED;
+    int st;
+    if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({save_mean, save_rstd, running_mean, running_var}, 4)) != NRM_OK)
+        return st;
+    const size_t need = bn_fwd_train_workspace_size(batch, C, HW, dtype);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
+    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es;
+    const Span sx = span(x, tb), sy = span(y, tb), sg = span(gamma, C * es), sb = span(beta, C * es),
+               ssm = span(save_mean, C * 4), ssr = span(save_rstd, C * 4),
+               srm = span(running_mean, C * 4), srv = span(running_var, C * 4),
+               sws = span(workspace, need);
+    const Span outs[] = {sy, ssm, ssr, srm, srv, sws};
+    const Span ins[] = {sx, sg, sb};
+    for (const Span &o : outs)
+        for (const Span &i : ins)
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    for (int i = 0; i < 6; ++i)
+        for (int j = i + 1; j < 6; ++j)
+            if (overlap(outs[i], outs[j])) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var,
+                              workspace})) != NRM_OK)
+        return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
+             static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
+             running_mean, running_var, batch, C, HW, eps, momentum, workspace};
+    const cudaError_t e = launch_bn_train_f32(a, dev.sms, stream);
+    return e == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
+}
+
+const char *nrm_status_string(int status) {
+    switch (status) {
+    case NRM_OK: return "ok";
+    case NRM_ERR_NULL: return "a required pointer is NULL";
+    case NRM_ERR_SHAPE: return "invalid shape (negative extent, N < 1, size overflow, or BatchNorm count < 2)";
+    case NRM_ERR_DTYPE: return "unknown dtype";
+    case NRM_ERR_ALIAS: return "an output overlaps an input or another output";
+    case NRM_ERR_VALUE: return "invalid value (eps, momentum, or a pointer not aligned to its element size)";
+    case NRM_ERR_UNSUPPORTED: return "not supported for these arguments";
+    case NRM_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+    case NRM_ERR_DEVICE: return "no usable current CUDA device";
+    case NRM_ERR_LAUNCH: return "kernel launch failed";
+    case NRM_ERR_POINTER: return "a pointer is not device memory of the current device";
+    default: return "unknown status";
+    }
+}
+
+int nrm_force_plan(int plan, int threads, int packs) {
+    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_CTA || threads < 0 || packs < 0)
+        return NRM_ERR_UNSUPPORTED;
+    g_force_kind.store(plan);
+    g_force_threads.store(plan ? threads : 0);
+    g_force_packs.store(plan ? packs : 0);
+    return NRM_OK;
+}
+
+void nrm_last_plan(int *plan, int *threads, int *packs) {
+    if (plan) *plan = t_last_kind;
+    if (threads) *threads = t_last_threads;
+    if (packs) *packs = t_last_packs;
+}
+
+int nrm_set_pointer_checks(int enable) { return g_pointer_checks.exchange(enable ? 1 : 0); }
+
+}  // extern "C"

@@ -1,0 +1,191 @@
+// nrm_device.cuh -- device building blocks of the normalization kernels:
+// 16-byte vector I/O with binary32 conversion, and the reduction engine
+// (warp shuffles, CTA combine through shared memory) for sums and for
+// (count, mean, M2) statistics.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nrm {
+
+// ---------------------------------------------------------------------------
+// Vector I/O.  A "pack" is 16 bytes: 4 binary32 or 8 half-width values.  The
+// fused RMSNorm page (diycv.top, §3.1) packs 4 elements per access; on GB300
+// a full 16-byte access per thread is the widest single load/store.
+// ---------------------------------------------------------------------------
+template <typename T> struct IO;
+
+template <> struct IO<float> {
+    static constexpr int V = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float *f) {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static float to_f(float v) { return v; }
+    __device__ __forceinline__ static float from_f(float v) { return v; }
+};
+
+template <> struct IO<__half> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float *f) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 t = __half22float2(h);
+            f[2 * i] = t.x; f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ static float to_f(__half v) { return __half2float(v); }
+    __device__ __forceinline__ static __half from_f(float v) { return __float2half_rn(v); }
+};
+
+template <> struct IO<__nv_bfloat16> {
+    static constexpr int V = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float *f) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // a bfloat16 is the top half of a binary32: widening is a shift
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Streaming 16-byte load of data read once (no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte load of data every CTA re-reads (parameters): keep it cached.
+__device__ __forceinline__ uint4 ld_param(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Streaming 16-byte store (evict-first in the caches).
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+// ---------------------------------------------------------------------------
+// Reduction engine.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum_down(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_down_sync(0xffffffffu, v, o);
+    return v;  // complete in lane 0
+}
+
+// Partial statistics of a set of values: count, mean, and M2 = sum of squared
+// deviations from that mean.
+struct Stats {
+    float n, mean, m2;
+};
+
+// Pairwise combine of two partial statistics (the parallel form of the
+// Welford update; LLM-ops page, smarter.xin, "Welford combine" section):
+//   n = na + nb, d = mb - ma, mean = ma + d*nb/n, M2 = M2a + M2b + d^2*na*nb/n.
+// An empty side (n = 0) leaves the other unchanged.
+__device__ __forceinline__ Stats combine(const Stats &a, const Stats &b) {
+    const float n = a.n + b.n;
+    if (n == 0.f) return a;
+    const float fb = b.n / n;
+    const float d = b.mean - a.mean;
+    Stats r;
+    r.n = n;
+    r.mean = fmaf(d, fb, a.mean);
+    r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+    return r;
+}
+
+__device__ __forceinline__ Stats warp_stats_down(Stats s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Stats t;
+        t.n = __shfl_down_sync(0xffffffffu, s.n, o);
+        t.mean = __shfl_down_sync(0xffffffffu, s.mean, o);
+        t.m2 = __shfl_down_sync(0xffffffffu, s.m2, o);
+        s = combine(s, t);
+    }
+    return s;  // complete in lane 0
+}
+
+// Broadcast lane 0's value to the whole warp.
+__device__ __forceinline__ float warp_bcast0(float v) { return __shfl_sync(0xffffffffu, v, 0); }
+
+// Butterfly sums: every lane ends with the same bits (a + b == b + a exactly in
+// IEEE arithmetic, so partners at each level compute identical values).
+__device__ __forceinline__ float warp_sum_all(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float2 warp_sum_all(float2 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    return v;
+}
+
+// CTA-wide sum returned to every thread, with one __syncthreads: warps reduce
+// by butterfly, lane 0 of each warp publishes its partial, then every warp
+// reduces the NW partials by butterfly (same data, same order, so every
+// thread gets the same bits).  `slot` must not be rewritten until every thread
+// has passed the next __syncthreads of the CTA (callers alternate two slots).
+template <int NW>
+__device__ __forceinline__ float cta_sum_all(float v, float *slot) {
+    static_assert(NW >= 1 && NW <= 32, "1..32 warps");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_all(v);
+    if (NW == 1) return v;
+    if (lane == 0) slot[warp] = v;
+    __syncthreads();
+    return warp_sum_all(lane < NW ? slot[lane] : 0.f);
+}
+template <int NW>
+__device__ __forceinline__ float2 cta_sum_all(float2 v, float2 *slot) {
+    static_assert(NW >= 1 && NW <= 32, "1..32 warps");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_all(v);
+    if (NW == 1) return v;
+    if (lane == 0) slot[warp] = v;
+    __syncthreads();
+    return warp_sum_all(lane < NW ? slot[lane] : make_float2(0.f, 0.f));
+}
+
+}  // namespace nrm

@@ -1,0 +1,61 @@
+// nrm_internal.h -- host-side declarations shared by the C ABI (api.cpp) and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nrm {
+
+enum Op { OP_LN = 0, OP_RMS = 1, OP_ADD_RMS = 2 };
+enum DType { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+enum PlanKind { PLAN_AUTO = 0, PLAN_GENERIC = 1, PLAN_WARP = 2, PLAN_CTA = 3 };
+
+// Everything a row kernel needs.  Pointers are device pointers; unused ones
+// are NULL.  p0 = gamma (LayerNorm) or w (RMS ops); p1 = beta.
+struct RowArgs {
+    const void *x;
+    const void *res;      // add+RMS only
+    const void *p0;
+    const void *p1;
+    void *res_out;        // add+RMS only
+    void *y;
+    float *mean;          // LayerNorm only
+    float *rstd;
+    int64_t rows;
+    int64_t N;
+    float eps;
+};
+
+struct Plan {
+    int kind;      // PlanKind
+    int threads;   // CTA size
+    int packs;     // 16-byte packs per thread (WARP: per lane)
+    int64_t grid;  // CTAs launched
+};
+
+// Launch a row operator with a fully specified plan.  Returns a cudaError_t
+// from the launch (cudaSuccess or the launch error), or
+// cudaErrorInvalidConfiguration when the template set has no such plan.
+cudaError_t launch_ln(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
+cudaError_t launch_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
+cudaError_t launch_add_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
+
+// BatchNorm training forward (binary32).  ws holds batch*C float2 partials.
+struct BnArgs {
+    const float *x;
+    const float *gamma;
+    const float *beta;
+    float *y;
+    float *save_mean;
+    float *save_rstd;
+    float *running_mean;
+    float *running_var;
+    int64_t batch, C, HW;
+    float eps, momentum;
+    void *ws;
+};
+cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s);
+
+}  // namespace nrm

@@ -1,0 +1,139 @@
+"""The C-ABI library loads and exports every function include/nrm.h declares,
+and rejects invalid arguments before touching a GPU (no GPU needed: the
+pointers below are never dereferenced, and no call here reaches a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nrm.h")
+
+OK, NULL, SHAPE, DTYPE, ALIAS, VALUE, UNSUP, WS, DEVICE, LAUNCH, POINTER = range(11)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import row_wise_normalization_reduce_gb300 as nrm
+    if not os.path.exists(nrm.LIB_PATH):
+        nrm.build()
+    return nrm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_four_operators():
+    names = declared_functions()
+    for f in ("ln_fwd", "rms_fwd", "add_rms_fwd", "bn_fwd_train"):
+        assert f in names
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"libnrm.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for s in range(11):
+        text = lib.nrm_status_string(s).decode()
+        assert text and text != "unknown status"
+    assert lib.nrm_status_string(999).decode() == "unknown status"
+
+
+A = 0x10000  # fake, aligned addresses (never dereferenced)
+
+
+def test_row_ops_validate_before_launch(lib):
+    # null required pointers
+    assert lib.ln_fwd(None, None, None, A, None, None, 4, 8, 1e-5, 0, None) == NULL
+    assert lib.rms_fwd(A, None, None, None, 4, 8, 1e-5, 0, None) == NULL
+    assert lib.add_rms_fwd(A, None, None, A * 4, A * 8, None, 4, 8, 1e-6, 2, None) == NULL
+    # shapes, dtype, eps
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, -1, 8, 1e-5, 0, None) == SHAPE
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 4, 0, 1e-5, 0, None) == SHAPE
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 2 ** 40, 2 ** 40, 1e-5, 0, None) == SHAPE
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 4, 8, 1e-5, 7, None) == DTYPE
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 4, 8, -1.0, 0, None) == VALUE
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 4, 8, float("nan"), 0, None) == VALUE
+    assert lib.rms_fwd(A, None, A * 4, None, 4, 8, float("inf"), 1, None) == VALUE
+    # misaligned to the element size
+    assert lib.ln_fwd(A + 1, None, None, A * 4, None, None, 4, 8, 1e-5, 2, None) == VALUE
+    assert lib.ln_fwd(A, None, None, A * 4, A * 8 + 2, None, 4, 8, 1e-5, 2, None) == VALUE
+    # rows == 0 is a no-op that needs no device
+    assert lib.ln_fwd(A, None, None, A * 4, None, None, 0, 8, 1e-5, 0, None) == OK
+    assert lib.add_rms_fwd(A, A * 2, None, A * 3, A * 4, None, 0, 8, 1e-6, 2, None) == OK
+
+
+def test_aliasing_rules(lib):
+    rows, n = 4, 64
+    tb = rows * n * 2
+    x, res, ro, y = A, A + 4 * tb, A + 8 * tb, A + 12 * tb
+    # y == x, or y overlapping x
+    assert lib.ln_fwd(x, None, None, x, None, None, rows, n, 1e-5, 2, None) == ALIAS
+    assert lib.ln_fwd(x, None, None, x + tb - 16, None, None, rows, n, 1e-5, 2, None) == ALIAS
+    assert lib.rms_fwd(x, None, y, y + 16, rows, n, 1e-6, 2, None) == ALIAS
+    # stats overlapping an input
+    assert lib.ln_fwd(x, None, None, y, x + 64, None, rows, n, 1e-5, 2, None) == ALIAS
+    # residual_out may be exactly residual, but not partially overlap it
+    assert lib.add_rms_fwd(x, res, None, res + 16, y, None, rows, n, 1e-6, 2, None) == ALIAS
+    assert lib.add_rms_fwd(x, res, None, ro, x, None, rows, n, 1e-6, 2, None) == ALIAS
+    assert lib.add_rms_fwd(x, res, None, ro, ro, None, rows, n, 1e-6, 2, None) == ALIAS
+    # valid calls get as far as the device query (no GPU in this container) or run
+    st = lib.add_rms_fwd(x, res, None, res, y, None, rows, n, 1e-6, 2, None)
+    assert st in (OK, DEVICE)
+
+
+def test_bn_validation(lib):
+    b, c, hw = 2, 3, 5
+    need = lib.bn_fwd_train_workspace_size(b, c, hw, 0)
+    assert need == b * c * 8
+    assert lib.bn_fwd_train_workspace_size(0, c, hw, 0) == 0
+    assert lib.bn_fwd_train_workspace_size(b, c, hw, 9) == 0
+    x, y, ws = A, A * 16, A * 64
+    args = dict(g=None, be=None, sm=None, sr=None, rm=None, rv=None)
+
+    def call(x=x, y=y, batch=b, C=c, HW=hw, eps=1e-5, mom=0.1, dt=0, ws=ws, wsb=need):
+        return lib.bn_fwd_train(x, args["g"], args["be"], y, args["sm"], args["sr"], args["rm"],
+                                args["rv"], batch, C, HW, eps, mom, dt, ws, wsb, None)
+
+    assert call(x=None) == NULL
+    assert call(batch=0) == SHAPE
+    assert call(batch=1, HW=1) == SHAPE          # count 1: unbiased variance undefined
+    assert call(eps=-1.0) == VALUE
+    assert call(mom=1.5) == VALUE
+    assert call(dt=5) == DTYPE
+    assert call(dt=2) == UNSUP
+    assert call(ws=None) == WS
+    assert call(wsb=need - 1) == WS
+    assert call(ws=ws + 8) == WS
+    assert call(y=x) == ALIAS
+    assert call(ws=x) == ALIAS
+    assert call() in (OK, DEVICE)
+
+
+def test_force_plan_api(lib):
+    assert lib.nrm_force_plan(99, 0, 0) == UNSUP
+    assert lib.nrm_force_plan(-1, 0, 0) == UNSUP
+    assert lib.nrm_force_plan(3, 256, 2) == OK
+    assert lib.nrm_force_plan(0, 0, 0) == OK
+    assert lib.nrm_set_pointer_checks(0) in (0, 1)
+
+
+def test_product_path_has_no_oracle_dependency():
+    # the package and the CUDA sources never name the oracle
+    pkg = os.path.join(ROOT, "row_wise_normalization_reduce_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "oracle." not in text, f

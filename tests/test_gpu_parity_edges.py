@@ -1,0 +1,212 @@
+"""GPU parity on edge cases: row lengths around every pack and plan boundary,
+empty and single rows, misaligned pointers (scalar path), absent parameters,
+constant rows, every plan forced on the same inputs, 3-D inputs, guard bands
+around outputs, BatchNorm corner shapes.  All compared element by element with
+the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import bits as B
+import runners as RN
+from row_wise_normalization_reduce_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+import row_wise_normalization_reduce_gb300 as nrm  # noqa: E402
+
+DTYPES = ["f32", "f16", "bf16"]
+
+
+@pytest.fixture(autouse=True)
+def _auto_plan():
+    nrm.build()
+    nrm.force_plan(nrm.PLAN_AUTO)
+    yield
+    nrm.force_plan(nrm.PLAN_AUTO)
+
+
+def _check(orc, op, inp, eps=1e-5):
+    gpu = RN.run_gpu(op, inp, eps)
+    ref = RN.run_oracle(orc, op, inp, eps)
+    return RN.compare(op, inp, gpu, ref)
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 255, 256, 1000, 1024, 4096, 8192, 16384, 32768,
+                               65536])
+def test_row_lengths(orc, op, dt, n):
+    rows = 3 if n >= 16384 else 37
+    inp = W.generic_rows(op, dt, rows, n, seed=n + 17, scale=2.0, shift=1.0)
+    _check(orc, op, inp)
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("rows", [0, 1, 3, 64, 4097])
+def test_row_counts(orc, op, rows):
+    inp = W.generic_rows(op, "bf16", rows, 512, seed=rows + 5)
+    if rows == 0:
+        d = {k: v.cuda() for k, v in inp.items()}
+        if op == "ln":
+            y, m, r = nrm.ln_fwd(d["x"], d["gamma"], d["beta"])
+            assert y.numel() == 0
+        elif op == "rms":
+            y, _ = nrm.rms_fwd(d["x"], d["w"])
+        else:
+            nrm.add_rms_fwd(d["x"], d["residual"], d["w"])
+        return
+    _check(orc, op, inp)
+
+
+PLANS = [(nrm.PLAN_GENERIC, 128, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_GENERIC, 512, 0),
+         (nrm.PLAN_WARP, 128, 8), (nrm.PLAN_CTA, 128, 2), (nrm.PLAN_CTA, 256, 1),
+         (nrm.PLAN_CTA, 256, 2), (nrm.PLAN_CTA, 512, 1), (nrm.PLAN_CTA, 1024, 1),
+         (nrm.PLAN_CTA, 256, 4), (nrm.PLAN_CTA, 512, 4), (nrm.PLAN_CTA, 1024, 4),
+         (nrm.PLAN_CTA, 1024, 2), (nrm.PLAN_CTA, 512, 2)]
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("plan", PLANS, ids=lambda p: f"{nrm.PLAN_NAMES[p[0]]}{p[1]}x{p[2]}")
+def test_forced_plans(orc, op, dt, plan):
+    # N = 1000 elements: a ragged number of packs for every dtype that fits
+    # every plan above (fp32: 250 packs, 16-bit: 125 packs)
+    n = 1000 if dt == "f32" else 2000
+    if plan[0] == nrm.PLAN_WARP:
+        n = 1000 if dt == "f32" else 1000
+    inp = W.generic_rows(op, dt, 67, n, seed=3, scale=1.5, shift=0.5)
+    nrm.force_plan(*plan)
+    _check(orc, op, inp)
+    got = nrm.last_plan()
+    assert got[0] == plan[0]
+
+
+def test_forced_plan_that_cannot_run():
+    nrm.force_plan(nrm.PLAN_WARP, 128, 1)
+    x = torch.randn(4, 4096, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(nrm.NrmError) as e:
+        nrm.rms_fwd(x)
+    assert e.value.status == 6
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_misaligned_pointers_use_scalar_path(orc, op, dt):
+    rows, n = 9, 512
+    inp = W.generic_rows(op, dt, rows, n, seed=11)
+    d = {}
+    for k, v in inp.items():
+        buf = torch.empty(v.numel() + 1, dtype=v.dtype, device="cuda")
+        view = buf[1:].view(v.shape)
+        view.copy_(v.cuda())
+        d[k] = view
+    if op == "ln":
+        y, mean, rstd = nrm.ln_fwd(d["x"], d["gamma"], d["beta"], 1e-5)
+        gpu = {"y": y, "mean": mean, "rstd": rstd}
+    elif op == "rms":
+        y, rstd = nrm.rms_fwd(d["x"], d["w"], 1e-5, want_stats=True)
+        gpu = {"y": y, "rstd": rstd}
+    else:
+        ro, y, rstd = nrm.add_rms_fwd(d["x"], d["residual"], d["w"], 1e-5, want_stats=True)
+        gpu = {"residual_out": ro, "y": y, "rstd": rstd}
+    assert nrm.last_plan()[0] == nrm.PLAN_GENERIC
+    torch.cuda.synchronize()
+    gpu = {k: B.torch_to_np(v.cpu()) for k, v in gpu.items()}
+    RN.compare(op, inp, gpu, RN.run_oracle(orc, op, inp, 1e-5))
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+def test_absent_parameters(orc, op):
+    inp = W.generic_rows(op, "bf16", 33, 768, seed=2)
+    for k in ("gamma", "beta", "w"):
+        inp.pop(k, None)
+    _check(orc, op, inp)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_constant_rows_give_beta_exactly(dt):
+    n = 4096
+    inp = W.generic_rows("ln", dt, 8, n, seed=9)
+    for i, c in enumerate([0.0, 1.0, 1000.0, -7.5, 3.25, 0.125, -1000.0, 42.0]):
+        inp["x"][i] = c
+    d = {k: v.cuda() for k, v in inp.items()}
+    for plan in [(nrm.PLAN_AUTO, 0, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_CTA, 1024, 1)]:
+        nrm.force_plan(*plan)
+        y, mean, _ = nrm.ln_fwd(d["x"], d["gamma"], d["beta"], 1e-5)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), inp["beta"].expand(8, n)), plan
+        assert torch.equal(mean.cpu(), inp["x"][:, 0].float())
+
+
+def test_zero_residual_equals_rms():
+    inp = W.generic_rows("rms", "bf16", 64, 4096, seed=4)
+    d = {k: v.cuda() for k, v in inp.items()}
+    y1, r1 = nrm.rms_fwd(d["x"], d["w"], 1e-6, want_stats=True)
+    ro, y2, r2 = nrm.add_rms_fwd(d["x"], torch.zeros_like(d["x"]), d["w"], 1e-6, want_stats=True)
+    assert torch.equal(ro, d["x"])
+    assert torch.equal(y1, y2) and torch.equal(r1, r2)
+
+
+def test_3d_input(orc):
+    inp = W.generic_rows("rms", "f16", 4 * 24, 1024, seed=6)
+    x3 = inp["x"].view(4, 24, 1024).cuda()
+    y, rstd = nrm.rms_fwd(x3, inp["w"].cuda(), 1e-6, want_stats=True)
+    assert y.shape == (4, 24, 1024) and rstd.shape == (4, 24)
+    gpu = {"y": B.torch_to_np(y.view(96, 1024).cpu()), "rstd": rstd.view(96).cpu().numpy()}
+    RN.compare("rms", inp, gpu, RN.run_oracle(orc, "rms", inp, 1e-6))
+
+
+@pytest.mark.parametrize("op", ["ln", "add_rms"])
+def test_guard_bands_untouched(op):
+    rows, n, guard = 17, 1000, 256
+    inp = W.generic_rows(op, "bf16", rows, n, seed=8)
+    d = {k: v.cuda() for k, v in inp.items()}
+    poison = -12345.0
+
+    def guarded(shape, dtype):
+        full = torch.full((int(np.prod(shape)) + 2 * guard,), poison, dtype=dtype, device="cuda")
+        return full, full[guard:guard + int(np.prod(shape))].view(shape)
+
+    fy, y = guarded((rows, n), torch.bfloat16)
+    fs, s = guarded((rows,), torch.float32)
+    if op == "ln":
+        fm, m = guarded((rows,), torch.float32)
+        nrm.ln_fwd(d["x"], d["gamma"], d["beta"], out=y, mean=m, rstd=s)
+        fulls = [fy, fs, fm]
+    else:
+        fr, r = guarded((rows, n), torch.bfloat16)
+        nrm.add_rms_fwd(d["x"], d["residual"], d["w"], residual_out=r, out=y, rstd=s)
+        fulls = [fy, fs, fr]
+    torch.cuda.synchronize()
+    for f in fulls:
+        assert torch.all(f[:guard] == poison) and torch.all(f[-guard:] == poison)
+
+
+# ---- BatchNorm ------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(1, 1, 7, 7), (1, 3, 5, 5), (2, 4, 3, 3), (8, 16, 28, 28),
+                                   (4, 8, 1, 1), (3, 5, 13, 11), (64, 3, 8, 8)])
+def test_bn_shapes(orc, shape):
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape)
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    ref = RN.run_oracle(orc, "bn", inp, 1e-5, 0.1)
+    RN.compare("bn", inp, gpu, ref)
+
+
+def test_bn_large_mean_channel(orc):
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(4, 3, 16, 16))
+    inp["x"][:, 1] += 1000.0
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    ref = RN.run_oracle(orc, "bn", inp, 1e-5, 0.1)
+    RN.compare("bn", inp, gpu, ref)
+
+
+def test_bn_without_optionals(orc):
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(2, 5, 6, 6))
+    x = inp["x"].cuda()
+    y, sm, sr = nrm.bn_fwd_train(x, None, None, None, None, 1e-5, 0.1)
+    torch.cuda.synchronize()
+    n = RN.to_np(inp)
+    ref = orc.batchnorm_train(0, n["x"], eps=1e-5, wide=True)
+    gy = y.cpu().numpy().reshape(ref["y_wide"].shape)
+    assert np.max(np.abs(gy - ref["y_wide"])) <= 2e-5
