@@ -166,23 +166,48 @@ typedef enum {
     NRM_PLAN_AUTO = 0,
     NRM_PLAN_GENERIC = 1,   /* one CTA per row, scalar, two reads of the row */
     NRM_PLAN_WARP = 2,      /* one warp per row, row held in registers */
-    NRM_PLAN_CTA = 3        /* one CTA per row, row held in registers */
+    NRM_PLAN_CTA = 3,       /* one CTA per row, row held in registers */
+    NRM_PLAN_TMA = 4        /* persistent CTAs of row groups; each group streams
+                               rows into its own ring of shared-memory stages
+                               with bulk asynchronous copies */
 } nrm_plan;
 
 /*
- * Force a plan (and, where non-zero, the CTA size and the 16-byte packs per
- * thread) for every later row-operator call in this process; plan 0 restores
- * automatic choice.  A forced plan that cannot run a given call makes that
- * call return NRM_ERR_UNSUPPORTED.  Returns NRM_OK or NRM_ERR_UNSUPPORTED for
- * an unknown plan.  Process-wide; not meant to change while calls run.
+ * Force a plan (and, where non-zero, the CTA size -- for NRM_PLAN_TMA the
+ * size of one row group --, the 16-byte packs per thread, and for
+ * NRM_PLAN_TMA the shared-memory stages per group, at most 16, and the row
+ * groups per CTA, at most 15) for every later row-operator call in this
+ * process; plan 0 restores automatic choice.  A forced plan that cannot run
+ * a given call makes that call return NRM_ERR_UNSUPPORTED.  Returns NRM_OK or
+ * NRM_ERR_UNSUPPORTED for an unknown plan.  Process-wide; not meant to change
+ * while calls run.
  */
-int nrm_force_plan(int plan, int threads, int packs);
+int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
 
 /*
- * Plan, CTA size and packs per thread chosen by this thread's most recent
- * successful row-operator call (written to the non-NULL pointers).
+ * Plan, CTA (group) size, packs per thread, stages and groups chosen by this
+ * thread's most recent successful row-operator call (written to the non-NULL
+ * pointers).
  */
-void nrm_last_plan(int *plan, int *threads, int *packs);
+void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups);
+
+/*
+ * Kernels that wait on asynchronous copies (NRM_PLAN_TMA) bound every wait:
+ * after `tries` unsuccessful polls they give up, record a fault bit, drain
+ * their copies in flight (again bounded) and return, leaving the outputs of
+ * that call undefined.  Sets the number of polls (default 2^20; 0 makes every
+ * such wait give up at once, which tests use to exercise the path) and
+ * returns the previous value.  Process-wide.
+ */
+unsigned nrm_set_wait_limit(unsigned tries);
+
+/*
+ * Read the current device's fault word: bit 0 = a kernel gave up a wait,
+ * bit 1 = it also gave up draining its copies.  Synchronizes the device
+ * first.  Clears the word when `clear` is non-zero.  Returns NRM_OK or
+ * NRM_ERR_DEVICE.
+ */
+int nrm_device_fault(unsigned *bits, int clear);
 
 /*
  * Switch pointer checks on (1) or off (0, the default).  When on, every call

@@ -16,8 +16,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libnrm.so")
 
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
-PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA = 0, 1, 2, 3
-PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta"}
+PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA, PLAN_TMA = 0, 1, 2, 3, 4
+PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta", 4: "tma"}
 
 _DT = {torch.float32: NRM_F32, torch.float16: NRM_F16, torch.bfloat16: NRM_BF16}
 
@@ -48,10 +48,14 @@ def _declare(lib):
         getattr(lib, f).restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
-    lib.nrm_force_plan.argtypes = [_INT, _INT, _INT]
+    lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
     lib.nrm_force_plan.restype = _INT
-    lib.nrm_last_plan.argtypes = [ctypes.POINTER(_INT)] * 3
+    lib.nrm_last_plan.argtypes = [ctypes.POINTER(_INT)] * 5
     lib.nrm_last_plan.restype = None
+    lib.nrm_set_wait_limit.argtypes = [ctypes.c_uint]
+    lib.nrm_set_wait_limit.restype = ctypes.c_uint
+    lib.nrm_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint), _INT]
+    lib.nrm_device_fault.restype = _INT
     lib.nrm_set_pointer_checks.argtypes = [_INT]
     lib.nrm_set_pointer_checks.restype = _INT
     return lib
@@ -215,14 +219,27 @@ def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, 
 # ---------------------------------------------------------------------------
 # Plan control (tests and measurements).
 # ---------------------------------------------------------------------------
-def force_plan(plan: int = PLAN_AUTO, threads: int = 0, packs: int = 0):
-    _check(lib().nrm_force_plan(plan, threads, packs), "nrm_force_plan")
+def force_plan(plan: int = PLAN_AUTO, threads: int = 0, packs: int = 0, stages: int = 0,
+               groups: int = 0):
+    _check(lib().nrm_force_plan(plan, threads, packs, stages, groups), "nrm_force_plan")
 
 
 def last_plan():
-    p, t, k = _INT(), _INT(), _INT()
-    lib().nrm_last_plan(ctypes.byref(p), ctypes.byref(t), ctypes.byref(k))
-    return p.value, t.value, k.value
+    """(plan, threads, packs, stages, groups) of this thread's last row-operator call."""
+    v = [_INT() for _ in range(5)]
+    lib().nrm_last_plan(*[ctypes.byref(x) for x in v])
+    return tuple(x.value for x in v)
+
+
+def set_wait_limit(tries: int) -> int:
+    return lib().nrm_set_wait_limit(tries)
+
+
+def device_fault(clear: bool = True) -> int:
+    """Fault bits recorded by kernels on the current device (synchronizes)."""
+    v = ctypes.c_uint()
+    _check(lib().nrm_device_fault(ctypes.byref(v), 1 if clear else 0), "nrm_device_fault")
+    return v.value
 
 
 def set_pointer_checks(enable: bool) -> bool:

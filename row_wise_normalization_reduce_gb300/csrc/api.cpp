@@ -51,9 +51,12 @@ int device_info(DevInfo *out) {
     return NRM_OK;
 }
 
-std::atomic<int> g_force_kind{0}, g_force_threads{0}, g_force_packs{0};
+std::atomic<int> g_force_kind{0}, g_force_threads{0}, g_force_packs{0}, g_force_stages{0},
+    g_force_groups{0};
+std::atomic<unsigned> g_wait_limit{1u << 20};
 std::atomic<int> g_pointer_checks{0};
-thread_local int t_last_kind = 0, t_last_threads = 0, t_last_packs = 0;
+thread_local int t_last_kind = 0, t_last_threads = 0, t_last_packs = 0, t_last_stages = 0,
+                 t_last_groups = 0;
 
 size_t elem_size(int dtype) { return dtype == NRM_F32 ? 4 : 2; }
 bool dtype_ok(int dtype) { return dtype == NRM_F32 || dtype == NRM_F16 || dtype == NRM_BF16; }
@@ -114,7 +117,6 @@ int round_up_pow2(int64_t v) {
 // Vectorized plans need every row pointer 16-byte aligned and N a multiple of
 // the pack width (16 bytes of elements).
 int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *plan) {
-    (void)op;
     const int64_t V = 16 / (int64_t)elem_size(dtype);
     const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16) &&
                         (!a.res || aligned(a.res, 16)) && (!a.res_out || aligned(a.res_out, 16)) &&
@@ -125,20 +127,47 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     int kind = g_force_kind.load(std::memory_order_relaxed);
     int fthreads = g_force_threads.load(std::memory_order_relaxed);
     int fpacks = g_force_packs.load(std::memory_order_relaxed);
+    int fstages = g_force_stages.load(std::memory_order_relaxed);
+    int fgroups = g_force_groups.load(std::memory_order_relaxed);
 
+    // Shared-memory stage of the bulk-copy pipeline: one row of x (and one of
+    // the residual for add+RMS).  Stages are sized to about 96 KB per CTA so
+    // that two or more CTAs fit on an SM.
+    const int64_t stage_bytes = a.N * (int64_t)elem_size(dtype) * (a.res ? 2 : 1);
+    const int64_t kStageBudget = 96 * 1024;
+    // parameters widened to binary32 in shared memory when they fit in 64 KB
+    const int64_t param_bytes = a.N * 4 * (op == OP_LN ? 2 : 1);
+    const bool smem_params = param_bytes <= 64 * 1024;
+    const int64_t fixed = smem_params ? param_bytes : 0;
+    const bool tma_ok = vec_ok && fixed + 2 * stage_bytes <= kSmemMax && P <= 512 * 4;
+
+    // Automatic choice, from measurements on GB300 (cold L2): rows of up to
+    // 1024 packs (8192 bf16 / 4096 fp32 values) run fastest as one CTA per row
+    // with the row in registers; longer rows through the row-group pipeline.
     if (kind == PLAN_AUTO) {
         if (!vec_ok)
             kind = PLAN_GENERIC;
         else if (P <= 32 * 8 && a.rows >= 4 * (int64_t)dev.sms)
             kind = PLAN_WARP;
+        else if (P <= 1024)
+            kind = PLAN_CTA;
+        else if (tma_ok)
+            kind = PLAN_TMA;
         else if (P <= 1024 * 4)
             kind = PLAN_CTA;
         else
             kind = PLAN_GENERIC;
-        fthreads = fpacks = 0;
+        fthreads = fpacks = fstages = fgroups = 0;
+        if (kind == PLAN_TMA) {
+            fthreads = P <= 2048 ? 512 : 0;
+            fpacks = 4;
+            fstages = 2;
+        }
     }
 
-    Plan p{kind, 0, 0, 0};
+    Plan p{};
+    p.kind = kind;
+    p.sms = dev.sms;
     switch (kind) {
     case PLAN_GENERIC: {
         p.threads = fthreads ? fthreads : (a.N >= 4096 ? 512 : 256);
@@ -163,7 +192,7 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     case PLAN_CTA: {
         if (!vec_ok) return NRM_ERR_UNSUPPORTED;
         int packs = fpacks, threads = fthreads;
-        if (!packs) packs = P <= 512 ? 1 : P <= 1024 ? 2 : 4;
+        if (!packs) packs = P <= 256 ? 1 : P <= 1024 ? 2 : 4;  // 256 x 2 for 512 packs
         if (!threads) {
             threads = round_up_pow2((P + packs - 1) / packs);
             if (threads < 128) threads = 128;
@@ -174,6 +203,52 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
         break;
     }
+    case PLAN_TMA: {
+        // Row groups of GT threads x PACKS packs (4 preferred), as many groups
+        // per CTA as fit in 1024 threads and the shared memory with 3 (else 2)
+        // stages each.
+        if (!tma_ok) return NRM_ERR_UNSUPPORTED;
+        int packs = fpacks, threads = fthreads;
+        if (!threads) {
+            threads = round_up_pow2((P + 3) / 4);
+            threads = threads < 128 ? 128 : threads > 512 ? 512 : threads;
+        }
+        if (!packs) packs = (int)((P + threads - 1) / threads) <= 2 && threads == 256 ? 2
+                            : (P + threads - 1) / threads <= 4 ? 4 : 8;
+        if ((int64_t)threads * packs < P) return NRM_ERR_UNSUPPORTED;
+        int stages = fstages, groups = fgroups;
+        auto fits = [&](int gr, int st) {
+            return gr * threads <= 1024 && fixed + (int64_t)gr * st * stage_bytes <= kSmemMax;
+        };
+        if (!groups || !stages) {
+            int best_g = 0, best_s = 0;
+            for (int st : {3, 2}) {
+                if (stages && st != stages) continue;
+                for (int gr : {8, 4, 2, 1}) {
+                    if (groups && gr != groups) continue;
+                    if (fits(gr, st) && gr * threads > best_g * threads) {
+                        best_g = gr;
+                        best_s = st;
+                    }
+                }
+                if (best_g && !stages) break;
+            }
+            if (!best_g && stages && !groups) {
+                for (int gr : {8, 4, 2, 1})
+                    if (fits(gr, stages)) { best_g = gr; best_s = stages; break; }
+            }
+            groups = groups ? groups : best_g;
+            stages = stages ? stages : best_s;
+        }
+        if (groups < 1 || stages < 2 || stages > kMaxStages || !fits(groups, stages))
+            return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.stages = stages;
+        p.groups = groups;
+        p.smem_params = smem_params ? 1 : 0;
+        break;
+    }
     default:
         return NRM_ERR_UNSUPPORTED;
     }
@@ -181,10 +256,12 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     return NRM_OK;
 }
 
-int run_row(Op op, const RowArgs &a, int dtype, cudaStream_t stream) {
+int run_row(Op op, RowArgs a, int dtype, cudaStream_t stream) {
     DevInfo dev;
     int st = device_info(&dev);
     if (st != NRM_OK) return st;
+    a.fault = fault_word();
+    a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     Plan plan;
     st = choose_plan(op, a, dtype, dev, &plan);
     if (st != NRM_OK) return st;
@@ -202,6 +279,8 @@ int run_row(Op op, const RowArgs &a, int dtype, cudaStream_t stream) {
     t_last_kind = plan.kind;
     t_last_threads = plan.threads;
     t_last_packs = plan.packs;
+    t_last_stages = plan.stages;
+    t_last_groups = plan.groups;
     return NRM_OK;
 }
 
@@ -244,7 +323,7 @@ int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *m
             if (overlap(o, i)) return NRM_ERR_ALIAS;
     if (overlap(sy, sm) || overlap(sy, sr) || overlap(sm, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, gamma, beta, y, mean, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps};
+    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps, nullptr, 0};
     return run_row(OP_LN, a, dtype, stream);
 }
 
@@ -264,7 +343,7 @@ int rms_fwd(const void *x, const void *w, void *y, float *rstd, int64_t rows, in
             if (overlap(o, i)) return NRM_ERR_ALIAS;
     if (overlap(sy, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, w, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps};
+    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps, nullptr, 0};
     return run_row(OP_RMS, a, dtype, stream);
 }
 
@@ -289,7 +368,7 @@ int add_rms_fwd(const void *x, const void *residual, const void *w, void *residu
     if (overlap(sy, sres) || overlap(sr, sres)) return NRM_ERR_ALIAS;
     if (overlap(sro, sy) || overlap(sro, sr) || overlap(sy, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, residual, w, residual_out, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps};
+    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0};
     return run_row(OP_ADD_RMS, a, dtype, stream);
 }
 
@@ -360,20 +439,27 @@ const char *nrm_status_string(int status) {
     }
 }
 
-int nrm_force_plan(int plan, int threads, int packs) {
-    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_CTA || threads < 0 || packs < 0)
+int nrm_force_plan(int plan, int threads, int packs, int stages, int groups) {
+    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_TMA || threads < 0 || packs < 0 || stages < 0 ||
+        stages > kMaxStages || groups < 0 || groups > 15)
         return NRM_ERR_UNSUPPORTED;
     g_force_kind.store(plan);
     g_force_threads.store(plan ? threads : 0);
     g_force_packs.store(plan ? packs : 0);
+    g_force_stages.store(plan ? stages : 0);
+    g_force_groups.store(plan ? groups : 0);
     return NRM_OK;
 }
 
-void nrm_last_plan(int *plan, int *threads, int *packs) {
+void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups) {
     if (plan) *plan = t_last_kind;
     if (threads) *threads = t_last_threads;
     if (packs) *packs = t_last_packs;
+    if (stages) *stages = t_last_stages;
+    if (groups) *groups = t_last_groups;
 }
+
+unsigned nrm_set_wait_limit(unsigned tries) { return g_wait_limit.exchange(tries); }
 
 int nrm_set_pointer_checks(int enable) { return g_pointer_checks.exchange(enable ? 1 : 0); }
 

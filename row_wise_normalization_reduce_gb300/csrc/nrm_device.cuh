@@ -80,6 +80,63 @@ template <> struct IO<__nv_bfloat16> {
     __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 
+// Pairwise views of a pack: H = V/2 float2 values, for the packed binary32
+// arithmetic of sm_100+ (__fadd2_rn, __fmul2_rn, __ffma2_rn: two IEEE
+// round-to-nearest operations per instruction, bit-identical to the scalar
+// ones).
+template <typename T> struct IO2;
+
+template <> struct IO2<float> {
+    static constexpr int H = 2;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float2 *f) {
+        f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
+    __device__ __forceinline__ static uint4 pack(const float2 *f) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                          __float_as_uint(f[1].x), __float_as_uint(f[1].y));
+    }
+};
+
+template <> struct IO2<__half> {
+    static constexpr int H = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float2 *f) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+    }
+    __device__ __forceinline__ static uint4 pack(const float2 *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __float22half2_rn(f[i]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <> struct IO2<__nv_bfloat16> {
+    static constexpr int H = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float2 *f) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static uint4 pack(const float2 *f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __float22bfloat162_rn(f[i]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 // Streaming 16-byte load of data read once (no L1 allocation).
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     uint4 r;
@@ -162,30 +219,160 @@ __device__ __forceinline__ float2 warp_sum_all(float2 v) {
     return v;
 }
 
+// Butterfly over groups of NW lanes (NW a power of two): every lane ends
+// with the sum of its group.
+template <int NW>
+__device__ __forceinline__ float group_sum_all(float v) {
+#pragma unroll
+    for (int o = NW / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+template <int NW>
+__device__ __forceinline__ float2 group_sum_all(float2 v) {
+#pragma unroll
+    for (int o = NW / 2; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    return v;
+}
+
 // CTA-wide sum returned to every thread, with one __syncthreads: warps reduce
 // by butterfly, lane 0 of each warp publishes its partial, then every warp
-// reduces the NW partials by butterfly (same data, same order, so every
-// thread gets the same bits).  `slot` must not be rewritten until every thread
-// has passed the next __syncthreads of the CTA (callers alternate two slots).
+// reads the NW partials (lane l takes partial l % NW) and finishes with a
+// log2(NW)-level butterfly (same data, same order, so every thread gets the
+// same bits).  `slot` must not be rewritten until every thread has passed the
+// next __syncthreads of the CTA (callers alternate two slots).
 template <int NW>
 __device__ __forceinline__ float cta_sum_all(float v, float *slot) {
-    static_assert(NW >= 1 && NW <= 32, "1..32 warps");
+    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "1..32 warps, power of two");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = warp_sum_all(v);
     if (NW == 1) return v;
     if (lane == 0) slot[warp] = v;
     __syncthreads();
-    return warp_sum_all(lane < NW ? slot[lane] : 0.f);
+    return group_sum_all<NW>(slot[lane & (NW - 1)]);
 }
 template <int NW>
 __device__ __forceinline__ float2 cta_sum_all(float2 v, float2 *slot) {
-    static_assert(NW >= 1 && NW <= 32, "1..32 warps");
+    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "1..32 warps, power of two");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = warp_sum_all(v);
     if (NW == 1) return v;
     if (lane == 0) slot[warp] = v;
     __syncthreads();
-    return warp_sum_all(lane < NW ? slot[lane] : make_float2(0.f, 0.f));
+    return group_sum_all<NW>(slot[lane & (NW - 1)]);
+}
+
+// Named barrier over `count` threads (a multiple of 32), id 1..15 (id 0 is
+// the barrier of __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Sum over a group of NW warps synchronised by named barrier `bar_id`, returned
+// to every thread of the group (same bits everywhere, as cta_sum_all).
+template <int NW>
+__device__ __forceinline__ float group_cta_sum(float v, float *slot, int bar_id) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & (NW - 1);
+    v = warp_sum_all(v);
+    if (NW == 1) return v;
+    if (lane == 0) slot[warp] = v;
+    named_sync(bar_id, NW * 32);
+    return group_sum_all<NW>(slot[lane & (NW - 1)]);
+}
+template <int NW>
+__device__ __forceinline__ float2 group_cta_sum(float2 v, float2 *slot, int bar_id) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & (NW - 1);
+    v = warp_sum_all(v);
+    if (NW == 1) return v;
+    if (lane == 0) slot[warp] = v;
+    named_sync(bar_id, NW * 32);
+    return group_sum_all<NW>(slot[lane & (NW - 1)]);
+}
+
+// As group_cta_sum, and also OR `flag` over the group in the same barrier
+// (bar.red.or): every thread learns whether any thread of the group raised it.
+template <int NW>
+__device__ __forceinline__ float group_cta_sum_or(float v, float *slot, int bar_id, bool flag,
+                                                  bool &any) {
+    const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & (NW - 1);
+    v = warp_sum_all(v);
+    if (lane == 0) slot[warp] = v;
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "r"(bar_id), "r"(NW * 32)
+        : "memory");
+    any = r != 0;
+    return group_sum_all<NW>(slot[lane & (NW - 1)]);
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (global -> shared) completed on an mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the asynchronous (copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier shared-memory accesses before later
+// asynchronous-proxy writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, trying at most
+// `limit` times; false means the wait gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
 }  // namespace nrm

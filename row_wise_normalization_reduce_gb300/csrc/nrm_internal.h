@@ -10,7 +10,19 @@ namespace nrm {
 
 enum Op { OP_LN = 0, OP_RMS = 1, OP_ADD_RMS = 2 };
 enum DType { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
-enum PlanKind { PLAN_AUTO = 0, PLAN_GENERIC = 1, PLAN_WARP = 2, PLAN_CTA = 3 };
+enum PlanKind { PLAN_AUTO = 0, PLAN_GENERIC = 1, PLAN_WARP = 2, PLAN_CTA = 3, PLAN_TMA = 4 };
+
+// Bits of the device fault word (see fault.cu).
+enum FaultBits : unsigned {
+    FAULT_WAIT = 1u,    // a kernel gave up waiting for a bulk copy
+    FAULT_DRAIN = 2u    // ... and then for its copies still in flight
+};
+
+// Largest number of shared-memory stages of the bulk-copy row pipeline, and
+// the dynamic shared memory a CTA may use (static arrays take the rest of the
+// 227 KB).
+constexpr int kMaxStages = 16;
+constexpr int kSmemMax = 224 * 1024;
 
 // Everything a row kernel needs.  Pointers are device pointers; unused ones
 // are NULL.  p0 = gamma (LayerNorm) or w (RMS ops); p1 = beta.
@@ -26,14 +38,24 @@ struct RowArgs {
     int64_t rows;
     int64_t N;
     float eps;
+    unsigned *fault;      // device fault word of the current device
+    unsigned wait_limit;  // tries per bounded wait (0: give up at once)
 };
 
 struct Plan {
     int kind;      // PlanKind
     int threads;   // CTA size
     int packs;     // 16-byte packs per thread (WARP: per lane)
-    int64_t grid;  // CTAs launched
+    int stages;    // TMA: shared-memory row stages per group
+    int groups;    // TMA: row groups per CTA
+    int smem_params;  // TMA: parameters widened to binary32 in shared memory
+    int sms;       // SMs of the device
+    int64_t grid;  // CTAs launched (TMA: set at launch from occupancy)
 };
+
+// Address of the current device's fault word (set up once per device), or
+// NULL if it cannot be obtained.  fault.cu.
+unsigned *fault_word();
 
 // Launch a row operator with a fully specified plan.  Returns a cudaError_t
 // from the launch (cudaSuccess or the launch error), or

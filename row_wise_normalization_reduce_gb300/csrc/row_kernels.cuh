@@ -8,6 +8,11 @@
 //                       from registers and stored.  x is read from HBM once.
 //   row_warp_kernel     one warp per row (short rows, many rows); reduction
 //                       by shuffles only.
+//   row_pipe_kernel     persistent CTAs of several row groups; each group streams
+//                       whole rows into its own ring of shared-memory stages
+//                       with bulk asynchronous copies completed on mbarriers,
+//                       so rows are always in flight while others are reduced
+//                       (row_pipe.cuh).
 //   row_generic_kernel  any N and any alignment: scalar accesses, one CTA per
 //                       row, the row read twice (statistics, then output).
 //
@@ -19,25 +24,29 @@
 // from sums of x and x^2.
 #pragma once
 
+#include <mutex>
+
 #include "nrm_device.cuh"
 #include "nrm_internal.h"
 
 namespace nrm {
 
-// LayerNorm statistics (register-resident rows).  With K = x[row, 0], the
-// row's first element, every value is first shifted, d = x - K: for 16-bit
-// inputs d is exact in binary32 whenever x and K are within 2^16 of each other
-// in magnitude, so rows with a large mean and a small spread (mean 1000,
-// std 1) lose nothing to cancellation.  Then a corrected two-pass over the
-// values held in registers:
-//   m0 = sum(d) / N                      (first CTA-wide sum)
-//   e  = d - m0;  c = sum(e) / N;  M2 = sum(e^2) - N c^2   (second, fused sum)
-//   mean = K + m0 + c,  var = M2 / N,  y = ((e - c) * rstd) * gamma + beta.
-// The correction c removes the rounding error of the first sum, so the mean
-// is accurate to a few units in the last place of the spread, and e is
-// centered exactly enough that sum(e^2) has no cancellation.  Two float
-// sums per row replace per-thread (count, mean, M2) combines, which need a
-// division at every step and would make a 4096-wide bf16 row issue-bound.
+// LayerNorm statistics (register-resident rows): a corrected two-pass over
+// the values held in registers,
+//   m0 = sum(x) / N                                   (first group-wide sum)
+//   e  = x - m0;  c = sum(e) / N;  M2 = sum(e^2) - N c^2   (second, fused sum)
+//   mean = m0 + c,  var = M2 / N,  y = ((e - c) * rstd) * gamma + beta.
+// m0 may carry the rounding error of a binary32 sum of N values; c, a sum of
+// the small centred values e, removes it, so the mean is accurate to a few
+// roundoffs of the spread.  For rows with a large mean and a small spread
+// (mean 1000, std 1) e = x - m0 is exact (x and m0 within a factor 2), so
+// nothing is lost to cancellation, and sum(e^2) is a sum of small positive
+// terms.  Two float sums per row; no divisions per element or per combine.
+//
+// Arithmetic is done pairwise with the packed binary32 instructions of
+// sm_100+ (two IEEE operations per instruction): the row operators are close
+// to instruction-bound at GB300's bandwidth, so halving the arithmetic
+// instruction count is what lets them stream at HBM speed.
 
 // Row-group reducers: the row is spread over one warp or over one CTA.
 struct WarpRed {
@@ -52,130 +61,198 @@ template <int NW> struct CtaRed {
     __device__ __forceinline__ float2 sum2(float2 v) { return cta_sum_all<NW>(v, s2); }
 };
 
+// Where a row's 16-byte packs come from: global memory (register path) or a
+// shared-memory stage filled by a bulk copy (x, then residual, back to back).
+template <typename T> struct GlobalSrc {
+    const T *x;    // row start in global memory
+    const T *res;
+    __device__ __forceinline__ uint4 x_pack(int idx) const { return ld_stream(x + (size_t)idx * IO<T>::V); }
+    __device__ __forceinline__ uint4 r_pack(int idx) const { return ld_stream(res + (size_t)idx * IO<T>::V); }
+};
+
+template <typename T> struct SmemSrc {
+    const unsigned char *stage;
+    uint32_t row_bytes;
+    __device__ __forceinline__ uint4 x_pack(int idx) const {
+        return reinterpret_cast<const uint4 *>(stage)[idx];
+    }
+    __device__ __forceinline__ uint4 r_pack(int idx) const {
+        return reinterpret_cast<const uint4 *>(stage + row_bytes)[idx];
+    }
+};
+
+// Where the parameters (gamma, beta / w) come from: global memory in their
+// storage type, or shared memory already widened to binary32 (gamma at
+// [0, N), beta at [N, 2N)), filled once per persistent CTA.
+template <typename T> struct GlobalParams {
+    const T *p0, *p1;
+    __device__ __forceinline__ void p0_pack(int idx, float2 *f) const {
+        if (p0) IO2<T>::unpack(ld_param(p0 + (size_t)idx * IO<T>::V), f);
+        else
+#pragma unroll
+            for (int h = 0; h < IO2<T>::H; ++h) f[h] = f2(1.f);
+    }
+    __device__ __forceinline__ void p1_pack(int idx, float2 *f) const {
+        if (p1) IO2<T>::unpack(ld_param(p1 + (size_t)idx * IO<T>::V), f);
+        else
+#pragma unroll
+            for (int h = 0; h < IO2<T>::H; ++h) f[h] = f2(0.f);
+    }
+};
+
+// Shared-memory layout: float4 q[param][quarter][pack] with the 4 (binary32
+// packs) or 8 (16-bit packs) values of pack i split into consecutive float4
+// planes, so the threads of a warp read consecutive 16-byte words (no bank
+// conflicts).  Filled by fill_smem_params.
+template <typename T> struct SmemParams {
+    const float4 *q;
+    int P;  // packs per row
+    static constexpr int Q = IO<T>::V / 4;  // float4 per pack
+    __device__ __forceinline__ void load(int param, int idx, float2 *f) const {
+#pragma unroll
+        for (int h = 0; h < Q; ++h) {
+            const float4 t = q[((size_t)param * Q + h) * P + idx];
+            f[2 * h] = make_float2(t.x, t.y);
+            f[2 * h + 1] = make_float2(t.z, t.w);
+        }
+    }
+    __device__ __forceinline__ void p0_pack(int idx, float2 *f) const { load(0, idx, f); }
+    __device__ __forceinline__ void p1_pack(int idx, float2 *f) const { load(1, idx, f); }
+};
+
+// Widen parameters into the SmemParams layout (absent gamma/w = 1, beta = 0).
+template <typename T, int NPARAM, int THREADS>
+__device__ __forceinline__ void fill_smem_params(const RowArgs &a, float *sp) {
+    constexpr int V = IO<T>::V, Q = V / 4;
+    const int P = (int)(a.N / V);
+    const T *src[2] = {static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+    const float dflt[2] = {1.f, 0.f};
+    for (int i = threadIdx.x; i < (int)a.N; i += THREADS) {
+        const int idx = i / V, j = i % V, h = j / 4, l = j % 4;
+#pragma unroll
+        for (int p = 0; p < NPARAM; ++p)
+            sp[(((size_t)p * Q + h) * P + idx) * 4 + l] = src[p] ? IO<T>::to_f(src[p][i]) : dflt[p];
+    }
+}
+
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+};
+
 // One row, spread over a group whose member `t` owns packs t, t + STRIDE, ...
-template <int OP, typename T, int PACKS, int STRIDE, class Red>
+// `after_sync` runs right after the first group-wide sum, when every member
+// has its values in registers (the bulk-copy pipeline refills the stage there).
+template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class Prm, class Hook>
 __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, const int t,
-                                         Red &red) {
-    using io = IO<T>;
-    constexpr int V = io::V;
-    const int64_t P = a.N / V;  // 16-byte packs per row
+                                         Red &red, const Src &src, const Prm &prm,
+                                         const Hook &after_sync) {
+    using io2 = IO2<T>;
+    constexpr int V = IO<T>::V;
+    constexpr int H = io2::H;
+    const int P = (int)(a.N / V);  // 16-byte packs per row (< 2^31 by construction)
     const float fN = (float)a.N;
-    const int64_t base = row * a.N;
-    const T *__restrict__ X = static_cast<const T *>(a.x);
-    const T *__restrict__ R = static_cast<const T *>(a.res);
-    const T *__restrict__ G = static_cast<const T *>(a.p0);
-    const T *__restrict__ Bt = static_cast<const T *>(a.p1);
-    T *__restrict__ Y = static_cast<T *>(a.y);
-    T *__restrict__ RO = static_cast<T *>(a.res_out);
+    const float invN = 1.0f / fN;
+    T *__restrict__ Y = static_cast<T *>(a.y) + row * a.N;
+    T *__restrict__ RO = static_cast<T *>(a.res_out) + row * a.N;
 
     // ---- S1/S2: issue every load of the row before any arithmetic ----
     uint4 rx[PACKS];
     uint4 rr[PACKS];
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
-        const int64_t idx = t + (int64_t)k * STRIDE;
+        const int idx = t + k * STRIDE;
         if (idx < P) {
-            rx[k] = ld_stream(X + base + idx * V);
-            if (OP == OP_ADD_RMS) rr[k] = ld_stream(R + base + idx * V);
+            rx[k] = src.x_pack(idx);
+            if (OP == OP_ADD_RMS) rr[k] = src.r_pack(idx);
         }
     }
-    const float K = (OP == OP_LN) ? io::to_f(X[base]) : 0.f;
 
-    // v: LayerNorm d = x - K; RMS x; add+RMS the rounded residual-stream value
-    float v[PACKS][V];
+    // v: the row's values (add+RMS: the rounded residual-stream value)
+    float2 v[PACKS][H];
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
-        const int64_t idx = t + (int64_t)k * STRIDE;
+        const int idx = t + k * STRIDE;
         if (idx < P) {
+            io2::unpack(rx[k], v[k]);
             if (OP == OP_ADD_RMS) {
-                float fx[V], fr[V], s[V];
-                io::unpack(rx[k], fx);
-                io::unpack(rr[k], fr);
+                float2 r[H];
+                io2::unpack(rr[k], r);
 #pragma unroll
-                for (int j = 0; j < V; ++j) s[j] = __fadd_rn(fx[j], fr[j]);
-                const uint4 packed = io::pack(s);  // round once to T
-                st_stream(RO + base + idx * V, packed);
-                io::unpack(packed, v[k]);
-            } else {
-                io::unpack(rx[k], v[k]);
-                if (OP == OP_LN)
-#pragma unroll
-                    for (int j = 0; j < V; ++j) v[k][j] -= K;
+                for (int h = 0; h < H; ++h) v[k][h] = __fadd2_rn(v[k][h], r[h]);
+                const uint4 packed = io2::pack(v[k]);  // round once to T
+                st_stream(RO + (size_t)idx * V, packed);
+                io2::unpack(packed, v[k]);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < V; ++j) v[k][j] = 0.f;  // contributes nothing
+            for (int h = 0; h < H; ++h) v[k][h] = f2(0.f);  // contributes nothing
         }
     }
 
     // ---- S3-S6: statistics ----
-    float rstd, m0 = 0.f, c = 0.f;
+    float rstd, c = 0.f;
     if (OP == OP_LN) {
-        float s = 0.f;
+        float2 acc = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) s += v[k][j];
-        m0 = red.sum(s) / fN;
-        float e1 = 0.f, e2 = 0.f;
+            for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, v[k][h]);
+        // m0 by a correctly rounded division: a constant row gives m0 == x
+        // exactly, hence e == 0, c == 0 and y == beta bit for bit.
+        const float m0 = __fdiv_rn(red.sum(acc.x + acc.y), fN);
+        after_sync();
+        const float2 nm = f2(-m0);
+        float2 e1 = f2(0.f), e2 = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
-            const int64_t idx = t + (int64_t)k * STRIDE;
-            if (idx < P)
+            if (t + k * STRIDE < P) {
 #pragma unroll
-                for (int j = 0; j < V; ++j) {
-                    const float e = v[k][j] - m0;
-                    v[k][j] = e;
-                    e1 += e;
-                    e2 = fmaf(e, e, e2);
+                for (int h = 0; h < H; ++h) {
+                    const float2 e = __fadd2_rn(v[k][h], nm);
+                    v[k][h] = e;
+                    e1 = __fadd2_rn(e1, e);
+                    e2 = __ffma2_rn(e, e, e2);
                 }
+            }
         }
-        const float2 E = red.sum2(make_float2(e1, e2));
-        c = E.x / fN;
-        const float var = fmaxf(fmaf(-c, c, E.y / fN), 0.f);
-        rstd = 1.0f / sqrtf(var + a.eps);
+        const float2 E = red.sum2(make_float2(e1.x + e1.y, e2.x + e2.y));
+        c = E.x * invN;
+        const float var = fmaxf(fmaf(-c, c, E.y * invN), 0.f);
+        rstd = rsqrtf(var + a.eps);
         if (t == 0) {
-            if (a.mean) a.mean[row] = K + (m0 + c);
+            if (a.mean) a.mean[row] = m0 + c;
             if (a.rstd) a.rstd[row] = rstd;
         }
     } else {
-        float ss = 0.f;
+        float2 ss = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
 #pragma unroll
-            for (int j = 0; j < V; ++j) ss = fmaf(v[k][j], v[k][j], ss);
-        rstd = 1.0f / sqrtf(red.sum(ss) / fN + a.eps);
+            for (int h = 0; h < H; ++h) ss = __ffma2_rn(v[k][h], v[k][h], ss);
+        rstd = rsqrtf(fmaf(red.sum(ss.x + ss.y), invN, a.eps));
+        after_sync();
         if (t == 0 && a.rstd) a.rstd[row] = rstd;
     }
 
     // ---- S7/S8: parameters, normalize, round once, store ----
+    const float2 r2 = f2(rstd), nc = f2(-c);
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
-        const int64_t idx = t + (int64_t)k * STRIDE;
+        const int idx = t + k * STRIDE;
         if (idx < P) {
-            float out[V];
+            float2 out[H], g[H];
+            prm.p0_pack(idx, g);
             if (OP == OP_LN) {
-                float g[V], b[V];
-                if (G) io::unpack(ld_param(G + idx * V), g);
-                else
+                float2 b[H];
+                prm.p1_pack(idx, b);
 #pragma unroll
-                    for (int j = 0; j < V; ++j) g[j] = 1.f;
-                if (Bt) io::unpack(ld_param(Bt + idx * V), b);
-                else
-#pragma unroll
-                    for (int j = 0; j < V; ++j) b[j] = 0.f;
-#pragma unroll
-                for (int j = 0; j < V; ++j) out[j] = fmaf((v[k][j] - c) * rstd, g[j], b[j]);
+                for (int h = 0; h < H; ++h)
+                    out[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(v[k][h], nc), r2), g[h], b[h]);
             } else {
-                float w[V];
-                if (G) io::unpack(ld_param(G + idx * V), w);
-                else
 #pragma unroll
-                    for (int j = 0; j < V; ++j) w[j] = 1.f;
-#pragma unroll
-                for (int j = 0; j < V; ++j) out[j] = (v[k][j] * rstd) * w[j];
+                for (int h = 0; h < H; ++h) out[h] = __fmul2_rn(__fmul2_rn(v[k][h], r2), g[h]);
             }
-            st_stream(Y + base + idx * V, io::pack(out));
+            st_stream(Y + (size_t)idx * V, io2::pack(out));
         }
     }
 }
@@ -185,21 +262,32 @@ __global__ void __launch_bounds__(THREADS) row_cta_kernel(const RowArgs a) {
     constexpr int NW = THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
+    const T *X = static_cast<const T *>(a.x);
+    const T *R = static_cast<const T *>(a.res);
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
         CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
-        row_body<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red);
+        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+        row_body<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, src, prm, NoHook{});
     }
 }
+
+#include "row_pipe.cuh"
 
 template <int OP, typename T, int PACKS, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) row_warp_kernel(const RowArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     WarpRed red;
+    const T *X = static_cast<const T *>(a.x);
+    const T *R = static_cast<const T *>(a.res);
     for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < a.rows;
-         row += (int64_t)gridDim.x * WARPS)
-        row_body<OP, T, PACKS, 32>(a, row, lane, red);
+         row += (int64_t)gridDim.x * WARPS) {
+        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+        row_body<OP, T, PACKS, 32>(a, row, lane, red, src, prm, NoHook{});
+    }
 }
 
 // Scalar fallback for any N and any (element-aligned) pointers.  Pass 1 keeps
@@ -296,6 +384,46 @@ __global__ void __launch_bounds__(THREADS) row_generic_kernel(const RowArgs a) {
 // ---------------------------------------------------------------------------
 // Launch switch: Plan -> template instance.
 // ---------------------------------------------------------------------------
+
+// Row-group pipeline launch: dynamic shared memory = parameters (binary32,
+// when smem_params) + groups x stages x stage bytes; grid = min(rows, SMs x
+// resident CTAs per SM).  The shared-memory opt-in and the occupancy are
+// computed once per device and size (per kernel instance), under a lock.
+template <int OP, typename T, int GT, int PACKS, int G>
+cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    auto kernel = row_pipe_kernel<OP, T, GT, PACKS, G>;
+    if (p.stages < 2 || p.stages > kMaxStages || !a.fault || p.sms < 1)
+        return cudaErrorInvalidConfiguration;
+    const size_t stage = (size_t)a.N * sizeof(T) * (OP == OP_ADD_RMS ? 2 : 1);
+    const size_t params = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
+    const size_t smem = params + stage * (size_t)p.stages * G;
+    if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::mutex mu;  // one cache per kernel instance
+    static size_t cached_smem[64];
+    static int cached_per_sm[64];
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached_smem[dev] != smem) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, GT * G,
+                                                              smem);
+            if (e != cudaSuccess) return e;
+            cached_smem[dev] = smem;
+        }
+        per_sm = cached_per_sm[dev];
+    }
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t slots = (int64_t)p.sms * per_sm;
+    const int64_t grid = a.rows < slots ? a.rows : slots;
+    kernel<<<(unsigned)grid, GT * G, smem, s>>>(a, p.stages, p.smem_params);
+    return cudaGetLastError();
+}
+
 template <int OP, typename T>
 cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const dim3 grid((unsigned)p.grid);
@@ -325,6 +453,17 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
         NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)
 #undef NRM_CTA_CASE
+        return cudaErrorInvalidConfiguration;
+    } else if (p.kind == PLAN_TMA) {
+#define NRM_PIPE_CASE(GT, PK, GR)                                                  \
+    if (p.threads == GT && p.packs == PK && p.groups == GR)                        \
+        return launch_pipe<OP, T, GT, PK, GR>(a, p, s);
+        NRM_PIPE_CASE(128, 4, 1) NRM_PIPE_CASE(128, 4, 2) NRM_PIPE_CASE(128, 4, 4)
+        NRM_PIPE_CASE(128, 4, 8) NRM_PIPE_CASE(128, 8, 1) NRM_PIPE_CASE(128, 8, 2)
+        NRM_PIPE_CASE(128, 8, 4) NRM_PIPE_CASE(256, 2, 1) NRM_PIPE_CASE(256, 2, 2)
+        NRM_PIPE_CASE(256, 2, 4) NRM_PIPE_CASE(256, 4, 1) NRM_PIPE_CASE(256, 4, 2)
+        NRM_PIPE_CASE(256, 4, 4) NRM_PIPE_CASE(512, 4, 1) NRM_PIPE_CASE(512, 4, 2)
+#undef NRM_PIPE_CASE
         return cudaErrorInvalidConfiguration;
     } else {
         return cudaErrorInvalidConfiguration;

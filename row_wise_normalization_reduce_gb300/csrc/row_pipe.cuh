@@ -1,0 +1,240 @@
+// row_pipe.cuh -- the persistent row-group pipeline (plan NRM_PLAN_TMA).
+//
+// One CTA per SM (or a few) holds G independent row groups of GT threads.
+// Each group streams its rows through its own ring of `stages` shared-memory
+// stages: the group leader claims the next row of the CTA's range from a
+// shared-memory counter and starts one bulk asynchronous copy per input row
+// (cp.async.bulk, completed on the stage's mbarrier), `stages` rows ahead of
+// the row the group is reducing.  So loads are always in flight while rows
+// are reduced, without holding them in registers, and every CTA gets a
+// contiguous, balanced range of rows (its count differs from any other CTA's
+// by at most one) that its groups share dynamically.
+//
+// Per row a group: waits for its stage, copies the raw 16-byte packs into
+// registers (16 registers for 32 bf16 values), releases the stage at the
+// first group barrier (the leader starts the next copy into it), and makes
+// two (LayerNorm) or one (RMS ops) group-wide sums, unpacking the packs again
+// for each pass: unpacking is one integer operation per element, cheaper
+// than the registers to hold the values in binary32.  Parameters are read
+// from shared memory already widened to binary32 (SmemParams) when they fit,
+// else from global memory through L1.
+//
+// Termination and failure are decided together at the first group barrier
+// (bar.red.or): a leader that finds the range exhausted publishes row -1 for
+// the stage and arrives on its barrier without a copy; a thread whose bounded
+// wait gives up raises the same flag.  Either way every thread of the group
+// leaves the loop at the same point, so no named barrier is left waiting.
+// After a give-up the leader waits (bounded) for its copies still in flight
+// before the CTA releases its shared memory.
+//
+// Included by row_kernels.cuh inside namespace nrm, after the row sources,
+// parameter views and reducers it uses.
+#pragma once
+
+template <int OP, typename T>
+__device__ __forceinline__ void pipe_claim(const RowArgs &a, unsigned long long *next_row,
+                                           int64_t r1, long long *slot_row, uint64_t *full,
+                                           unsigned char *ring, int stages, uint32_t stage_bytes,
+                                           uint32_t row_bytes, int64_t li) {
+    const int s = (int)(li % stages);
+    const long long r = (long long)atomicAdd(next_row, 1ULL);
+    if (r < r1) {
+        slot_row[s] = r;
+        unsigned char *dst = ring + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        bulk_g2s(dst, static_cast<const T *>(a.x) + r * a.N, row_bytes, &full[s]);
+        if (OP == OP_ADD_RMS)
+            bulk_g2s(dst + row_bytes, static_cast<const T *>(a.res) + r * a.N, row_bytes,
+                     &full[s]);
+    } else {
+        slot_row[s] = -1;
+        mbar_arrive(&full[s]);  // completes the phase without data
+    }
+}
+
+template <int OP, typename T, int GT, int PACKS, int G>
+__global__ void __launch_bounds__(GT *G, 1)
+    row_pipe_kernel(const RowArgs a, const int stages, const int smem_params) {
+    using io2 = IO2<T>;
+    constexpr int V = IO<T>::V;
+    constexpr int H = io2::H;
+    constexpr int NWG = GT / 32;
+    static_assert(GT % 32 == 0 && (NWG & (NWG - 1)) == 0 && NWG >= 1 && NWG <= 32, "group size");
+    static_assert(G >= 1 && G <= 15 && GT * G <= 1024, "groups per CTA");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float s1[G][2][NWG];
+    __shared__ float2 s2[G][2][NWG];
+    __shared__ __align__(8) uint64_t full[G][kMaxStages];
+    __shared__ long long slot_row[G][kMaxStages];
+    __shared__ unsigned long long next_row;
+
+    const int g = threadIdx.x / GT;
+    const int t = threadIdx.x % GT;
+    const int bar_id = 1 + g;
+
+    // balanced contiguous row range of this CTA
+    const int64_t nb = gridDim.x, b = blockIdx.x;
+    const int64_t q = a.rows / nb, rem = a.rows % nb;
+    const int64_t r0 = b * q + (b < rem ? b : rem);
+    const int64_t r1 = r0 + q + (b < rem ? 1 : 0);
+
+    const int P = (int)(a.N / V);
+    const uint32_t row_bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+    const uint32_t stage_bytes = row_bytes * (OP == OP_ADD_RMS ? 2u : 1u);
+    const int nparams = (OP == OP_LN) ? 2 : 1;
+    const size_t params_bytes = smem_params ? (size_t)nparams * (size_t)a.N * sizeof(float) : 0;
+    unsigned char *ring = smem + params_bytes + (size_t)g * stages * stage_bytes;
+
+    if (threadIdx.x == 0) next_row = (unsigned long long)r0;
+    __syncthreads();
+    int64_t issued = 0;  // leader: local row indices claimed so far
+    if (t == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&full[g][s], 1);
+        fence_mbar_init();
+        for (; issued < stages; ++issued)
+            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stages, stage_bytes,
+                              row_bytes, issued);
+    }
+    if (smem_params) fill_smem_params<T, (OP == OP_LN ? 2 : 1), GT * G>(a, reinterpret_cast<float *>(smem));
+    __syncthreads();
+
+    const float fN = (float)a.N;
+    const float invN = 1.0f / fN;
+    const SmemParams<T> sprm{reinterpret_cast<const float4 *>(smem), P};
+    const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+
+    int64_t li = 0;
+    bool gave_up = false;
+    for (;; ++li) {
+        const int s = (int)(li % stages);
+        const int par = (int)(li & 1);
+        const bool ok = mbar_wait_bounded(&full[g][s], (uint32_t)((li / stages) & 1), a.wait_limit);
+        if (!ok) atomicOr(a.fault, FAULT_WAIT);
+        const int64_t row = slot_row[g][s];
+        const bool valid = ok && row >= 0;
+        const uint4 *st = reinterpret_cast<const uint4 *>(ring + (size_t)s * stage_bytes);
+
+        // raw packs of the row (add+RMS: the rounded residual-stream packs)
+        uint4 raw[PACKS];
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            const int idx = t + k * GT;
+            if (idx < P) {
+                raw[k] = st[idx];
+                if (OP == OP_ADD_RMS) {
+                    const uint4 rr = st[P + idx];
+                    float2 fx[H], fr[H];
+                    io2::unpack(raw[k], fx);
+                    io2::unpack(rr, fr);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) fx[h] = __fadd2_rn(fx[h], fr[h]);
+                    raw[k] = io2::pack(fx);  // round once to T
+                    if (valid)
+                        st_stream(static_cast<T *>(a.res_out) + row * a.N + (size_t)idx * V, raw[k]);
+                }
+            }
+        }
+
+        // pass 1: sum (LayerNorm) or sum of squares (RMS ops)
+        float2 acc = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            if (t + k * GT < P) {
+                float2 f[H];
+                io2::unpack(raw[k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    acc = (OP == OP_LN) ? __fadd2_rn(acc, f[h]) : __ffma2_rn(f[h], f[h], acc);
+            }
+        }
+        bool stop;
+        const float tot = group_cta_sum_or<NWG>(acc.x + acc.y, &s1[g][par][0], bar_id, !valid, stop);
+        if (stop) {
+            // A clean end is a completed phase carrying the sentinel; anything
+            // else means some thread of the group gave up waiting.
+            gave_up = !(ok && row < 0);
+            break;  // the whole group leaves here together
+        }
+        if (t == 0 && issued < li + stages + 1) {
+            // every thread holds this row in registers: refill its stage
+            fence_proxy_async_smem();
+            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stages, stage_bytes,
+                              row_bytes, issued);
+            ++issued;
+        }
+
+        float rstd, m0 = 0.f, c = 0.f;
+        if (OP == OP_LN) {
+            // m0 = tot / N, corrected once so a constant row gives m0 == x
+            m0 = tot * invN;
+            m0 = fmaf(fmaf(-m0, fN, tot), invN, m0);
+            const float2 nm = f2(-m0);
+            float2 e1 = f2(0.f), e2 = f2(0.f);
+#pragma unroll
+            for (int k = 0; k < PACKS; ++k) {
+                if (t + k * GT < P) {
+                    float2 f[H];
+                    io2::unpack(raw[k], f);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        const float2 e = __fadd2_rn(f[h], nm);
+                        e1 = __fadd2_rn(e1, e);
+                        e2 = __ffma2_rn(e, e, e2);
+                    }
+                }
+            }
+            const float2 E = group_cta_sum<NWG>(make_float2(e1.x + e1.y, e2.x + e2.y),
+                                                &s2[g][par][0], bar_id);
+            c = E.x * invN;
+            const float var = fmaxf(fmaf(-c, c, E.y * invN), 0.f);
+            rstd = rsqrtf(var + a.eps);
+            if (t == 0) {
+                if (a.mean) a.mean[row] = m0 + c;
+                if (a.rstd) a.rstd[row] = rstd;
+            }
+        } else {
+            rstd = rsqrtf(fmaf(tot, invN, a.eps));
+            if (t == 0 && a.rstd) a.rstd[row] = rstd;
+        }
+
+        // pass 3: normalize, scale (and shift), round once, store
+        T *Y = static_cast<T *>(a.y) + row * a.N;
+        const float2 r2 = f2(rstd), nm = f2(-m0), nc = f2(-c);
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            const int idx = t + k * GT;
+            if (idx < P) {
+                float2 f[H], g2[H], out[H];
+                io2::unpack(raw[k], f);
+                if (smem_params) sprm.p0_pack(idx, g2);
+                else gprm.p0_pack(idx, g2);
+                if (OP == OP_LN) {
+                    float2 b2[H];
+                    if (smem_params) sprm.p1_pack(idx, b2);
+                    else gprm.p1_pack(idx, b2);
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+                        out[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nm), nc), r2),
+                                            g2[h], b2[h]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < H; ++h) out[h] = __fmul2_rn(__fmul2_rn(f[h], r2), g2[h]);
+                }
+                st_stream(Y + (size_t)idx * V, io2::pack(out));
+            }
+        }
+    }
+
+    // After a give-up: wait (bounded) for this group's copies still in flight,
+    // the latest claimed index of each stage from li on, before exiting.
+    if (t == 0 && gave_up) {
+        for (int s = 0; s < stages; ++s) {
+            int64_t j = -1;
+            for (int64_t k = issued - 1; k >= li && k >= issued - stages; --k)
+                if (k % stages == s) { j = k; break; }
+            if (j >= 0 && slot_row[g][s] >= 0 &&
+                !mbar_wait_bounded(&full[g][s], (uint32_t)((j / stages) & 1), 1u << 22))
+                atomicOr(a.fault, FAULT_DRAIN);
+        }
+    }
+}

@@ -120,10 +120,15 @@ def test_bn_validation(lib):
 
 
 def test_force_plan_api(lib):
-    assert lib.nrm_force_plan(99, 0, 0) == UNSUP
-    assert lib.nrm_force_plan(-1, 0, 0) == UNSUP
-    assert lib.nrm_force_plan(3, 256, 2) == OK
-    assert lib.nrm_force_plan(0, 0, 0) == OK
+    assert lib.nrm_force_plan(99, 0, 0, 0, 0) == UNSUP
+    assert lib.nrm_force_plan(-1, 0, 0, 0, 0) == UNSUP
+    assert lib.nrm_force_plan(4, 256, 2, 17, 0) == UNSUP
+    assert lib.nrm_force_plan(4, 256, 2, 2, 16) == UNSUP
+    assert lib.nrm_force_plan(3, 256, 2, 0, 0) == OK
+    assert lib.nrm_force_plan(4, 256, 2, 4, 2) == OK
+    assert lib.nrm_force_plan(0, 0, 0, 0, 0) == OK
+    old = lib.nrm_set_wait_limit(5)
+    assert lib.nrm_set_wait_limit(old) == 5
     assert lib.nrm_set_pointer_checks(0) in (0, 1)
 
 

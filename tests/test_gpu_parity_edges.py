@@ -63,12 +63,16 @@ PLANS = [(nrm.PLAN_GENERIC, 128, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_GENER
          (nrm.PLAN_WARP, 128, 8), (nrm.PLAN_CTA, 128, 2), (nrm.PLAN_CTA, 256, 1),
          (nrm.PLAN_CTA, 256, 2), (nrm.PLAN_CTA, 512, 1), (nrm.PLAN_CTA, 1024, 1),
          (nrm.PLAN_CTA, 256, 4), (nrm.PLAN_CTA, 512, 4), (nrm.PLAN_CTA, 1024, 4),
-         (nrm.PLAN_CTA, 1024, 2), (nrm.PLAN_CTA, 512, 2)]
+         (nrm.PLAN_CTA, 1024, 2), (nrm.PLAN_CTA, 512, 2),
+         (nrm.PLAN_TMA, 128, 4, 2, 1), (nrm.PLAN_TMA, 128, 4, 3, 8), (nrm.PLAN_TMA, 256, 2, 0, 0),
+         (nrm.PLAN_TMA, 256, 4, 5, 2), (nrm.PLAN_TMA, 512, 4, 2, 2), (nrm.PLAN_TMA, 128, 8, 16, 1)]
 
 
 @pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
 @pytest.mark.parametrize("dt", DTYPES)
-@pytest.mark.parametrize("plan", PLANS, ids=lambda p: f"{nrm.PLAN_NAMES[p[0]]}{p[1]}x{p[2]}")
+@pytest.mark.parametrize("plan", PLANS,
+                         ids=lambda p: f"{nrm.PLAN_NAMES[p[0]]}{p[1]}x{p[2]}" + (
+                             f"s{p[3]}g{p[4]}" if len(p) > 3 else ""))
 def test_forced_plans(orc, op, dt, plan):
     # N = 1000 elements: a ragged number of packs for every dtype that fits
     # every plan above (fp32: 250 packs, 16-bit: 125 packs)
@@ -80,6 +84,44 @@ def test_forced_plans(orc, op, dt, plan):
     _check(orc, op, inp)
     got = nrm.last_plan()
     assert got[0] == plan[0]
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt,threads,packs,groups", [("bf16", 128, 4, 4), ("f32", 256, 4, 2),
+                                                     ("f16", 256, 2, 1), ("bf16", 128, 4, 8)])
+@pytest.mark.parametrize("stages", [2, 3, 5])
+def test_tma_pipeline_many_rows_per_cta(orc, op, dt, threads, packs, groups, stages):
+    # 3001 rows over at most a few hundred row groups: every group streams many
+    # rows through its ring, so stages are refilled, barrier phases alternate
+    # and groups claim rows from their CTA's range until it runs out.
+    inp = W.generic_rows(op, dt, 3001, 4096, seed=stages, scale=1.3, shift=-0.4)
+    try:
+        nrm.force_plan(nrm.PLAN_TMA, threads, packs, stages, groups)
+        _check(orc, op, inp)
+    except nrm.NrmError as e:
+        # only a shared-memory budget overflow may refuse this combination
+        assert e.status == 6
+        pytest.skip("stages x groups exceed the shared memory of one CTA")
+    assert nrm.last_plan() == (nrm.PLAN_TMA, threads, packs, stages, groups)
+
+
+def test_tma_wait_give_up_path(orc):
+    # With a wait limit of 0 every bulk-copy wait gives up at once: the kernel
+    # must flag the fault, drain its copies and return (outputs undefined), and
+    # the next call with the normal limit must be correct again.
+    inp = W.generic_rows("add_rms", "bf16", 900, 4096, seed=77)
+    d = {k: v.cuda() for k, v in inp.items()}
+    nrm.force_plan(nrm.PLAN_TMA, 128, 4, 3, 4)
+    assert nrm.device_fault(clear=True) == 0
+    old = nrm.set_wait_limit(0)
+    try:
+        nrm.add_rms_fwd(d["x"], d["residual"], d["w"], 1e-6)
+        bits = nrm.device_fault(clear=True)
+    finally:
+        nrm.set_wait_limit(old)
+    assert bits == 1, bits            # gave up waiting, drained cleanly
+    _check(orc, "add_rms", inp, eps=1e-6)
+    assert nrm.device_fault(clear=True) == 0
 
 
 def test_forced_plan_that_cannot_run():
