@@ -72,8 +72,10 @@ typedef enum {
     NRM_ERR_WORKSPACE = 7,     /* BatchNorm workspace NULL, too small or misaligned */
     NRM_ERR_DEVICE = 8,        /* no current CUDA device or attribute query failed */
     NRM_ERR_LAUNCH = 9,        /* cudaGetLastError reported a launch failure */
-    NRM_ERR_POINTER = 10       /* pointer checks on, and a pointer is not device
+    NRM_ERR_POINTER = 10,      /* pointer checks on, and a pointer is not device
                                   memory of the current device */
+    NRM_ERR_TOO_LARGE = 11     /* bn_fwd_train_noalloc: batch * C above its fixed
+                                  capacity (65536) */
 } nrm_status;
 
 /*
@@ -154,6 +156,28 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y,
                  float *running_var, int64_t batch, int64_t C, int64_t HW,
                  float eps, float momentum, int dtype, void *workspace,
                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * bn_fwd_train without a workspace argument: it allocates nothing.  No page
+ * describes this entry point; it exists for callers that cannot allocate
+ * device memory at call time (a runtime that reserves its whole device memory
+ * budget at start-up and allows no later allocation, or a component that only
+ * receives device pointers from another part of the program).  Same
+ * arguments, results and errors as bn_fwd_train, minus the workspace.
+ *   The partial statistics live in a fixed array inside the library, sized
+ *   for batch * C <= 65536 (512 KB, held on every device that loads the
+ *   library until the process exits); larger shapes return
+ *   NRM_ERR_TOO_LARGE before anything is launched.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture on the device.
+ *   All calls on one device share the array: calls that may overlap on the
+ *   GPU (unordered streams) race and must not be issued.
+ */
+int bn_fwd_train_noalloc(const void *x, const void *gamma, const void *beta, void *y,
+                         float *save_mean, float *save_rstd, float *running_mean,
+                         float *running_var, int64_t batch, int64_t C, int64_t HW,
+                         float eps, float momentum, int dtype, cudaStream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char *nrm_status_string(int status);

@@ -46,6 +46,9 @@ def _declare(lib):
                                  _P, ctypes.c_size_t, _P]
     for f in ("ln_fwd", "rms_fwd", "add_rms_fwd", "bn_fwd_train"):
         getattr(lib, f).restype = _INT
+    lib.bn_fwd_train_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F,
+                                         _F, _INT, _P]
+    lib.bn_fwd_train_noalloc.restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
     lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
@@ -214,6 +217,24 @@ def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, 
                                 stream if stream is not None else _stream(x.device))
     _check(st, "bn_fwd_train")
     return y, save_mean, save_rstd
+
+
+def bn_fwd_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_var=None,
+                         eps=1e-5, momentum=0.1, *, out, save_mean, save_rstd, stream=None):
+    """bn_fwd_train for callers that cannot allocate device memory at call time:
+    every output is passed in, and the library keeps the partial statistics in
+    a fixed array of its own (batch * C <= 65536).  Returns (y, save_mean,
+    save_rstd)."""
+    _cuda(x, "x")
+    batch, c = x.shape[0], x.shape[1]
+    hw = x.numel() // (batch * c) if batch * c else 0
+    with torch.cuda.device(x.device):
+        st = lib().bn_fwd_train_noalloc(
+            _ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(save_mean), _ptr(save_rstd),
+            _ptr(running_mean), _ptr(running_var), batch, c, hw, eps, momentum, _dtype_code(x),
+            stream if stream is not None else _stream(x.device))
+    _check(st, "bn_fwd_train_noalloc")
+    return out, save_mean, save_rstd
 
 
 # ---------------------------------------------------------------------------

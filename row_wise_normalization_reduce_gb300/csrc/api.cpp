@@ -435,6 +435,7 @@ const char *nrm_status_string(int status) {
     case NRM_ERR_DEVICE: return "no usable current CUDA device";
     case NRM_ERR_LAUNCH: return "kernel launch failed";
     case NRM_ERR_POINTER: return "a pointer is not device memory of the current device";
+    case NRM_ERR_TOO_LARGE: return "batch * C exceeds the fixed capacity (65536) of bn_fwd_train_noalloc";
     default: return "unknown status";
     }
 }

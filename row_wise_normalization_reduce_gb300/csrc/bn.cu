@@ -16,6 +16,11 @@
 // All statistics of channel c are taken on d = x - K_c with K_c the channel's
 // first element x[0, c, 0]: the shift keeps channels with a large mean and a
 // small spread free of cancellation.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "nrm.h"
 #include "nrm_device.cuh"
 #include "nrm_internal.h"
 
@@ -149,3 +154,92 @@ cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace nrm
+
+// ---------------------------------------------------------------------------
+// bn_fwd_train_noalloc: the same two kernels, with the per-plane partial
+// statistics kept in a fixed array of this library instead of a workspace the
+// caller allocates.  It is for callers that cannot allocate device memory
+// when they call -- for example a runtime that reserves its whole device
+// memory budget at start-up and forbids later allocations, or a component
+// that is handed device pointers by another part of the program and has no
+// allocator of its own.
+//
+// The array is a file-scope __device__ variable: every GPU that loads this
+// library holds it (kBnStaticPlanes float2 = 512 KB) until the process exits.
+// Its name in host code is only a host-side stand-in, so the device address
+// is taken with cudaGetSymbolAddress, once per device, with that device
+// current, on the first call made on that device.  All calls on a device
+// share the array: calls that overlap on the GPU (different streams without
+// ordering) race on it.  Every partial a call reads it first writes in the
+// same call, so nothing needs clearing between calls.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kBnStaticPlanes = 65536;  // largest batch * C accepted
+__device__ __align__(256) float2 g_bn_static_partials[kBnStaticPlanes];
+
+constexpr int kMaxDevices = 64;
+float2 *g_bn_static_ptr[kMaxDevices];
+std::once_flag g_bn_static_once[kMaxDevices];
+
+bool spans_overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace
+
+extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void *beta, void *y,
+                                    float *save_mean, float *save_rstd, float *running_mean,
+                                    float *running_var, int64_t batch, int64_t C, int64_t HW,
+                                    float eps, float momentum, int dtype, cudaStream_t stream) {
+    using namespace nrm;
+    if (dtype != NRM_F32 && dtype != NRM_F16 && dtype != NRM_BF16) return NRM_ERR_DTYPE;
+    if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / 4) return NRM_ERR_SHAPE;
+    if (batch * HW < 2) return NRM_ERR_SHAPE;
+    if (batch * C > kBnStaticPlanes) return NRM_ERR_TOO_LARGE;
+    if (!std::isfinite(eps) || eps < 0.f || !(momentum >= 0.f && momentum <= 1.f))
+        return NRM_ERR_VALUE;
+    if (!x || !y) return NRM_ERR_NULL;
+    if (dtype != NRM_F32) return NRM_ERR_UNSUPPORTED;
+    const void *all[] = {x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var};
+    for (const void *p : all)
+        if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return NRM_ERR_VALUE;
+    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * 4, cb = (size_t)C * 4;
+    const void *ins[] = {x, gamma, beta};
+    const size_t in_n[] = {tb, cb, cb};
+    const void *outs[] = {y, save_mean, save_rstd, running_mean, running_var};
+    const size_t out_n[] = {tb, cb, cb, cb, cb};
+    for (int o = 0; o < 5; ++o) {
+        for (int i = 0; i < 3; ++i)
+            if (spans_overlap(outs[o], out_n[o], ins[i], in_n[i])) return NRM_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 5; ++o2)
+            if (spans_overlap(outs[o], out_n[o], outs[o2], out_n[o2])) return NRM_ERR_ALIAS;
+    }
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NRM_ERR_DEVICE;
+    }
+    std::call_once(g_bn_static_once[dev], [dev]() {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bn_static_partials) == cudaSuccess)
+            g_bn_static_ptr[dev] = static_cast<float2 *>(p);
+        else
+            cudaGetLastError();
+    });
+    if (!g_bn_static_ptr[dev]) return NRM_ERR_DEVICE;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1) {
+        cudaGetLastError();
+        return NRM_ERR_DEVICE;
+    }
+    BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
+             static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
+             running_mean, running_var, batch, C, HW, eps, momentum, g_bn_static_ptr[dev]};
+    return launch_bn_train_f32(a, sms, stream) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
+}
