@@ -434,6 +434,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--plan", default="auto",
+                    help="row-operator plan: auto, generic:T, warp:T:P, cta:T:P or "
+                         "tma:T:P:STAGES:GROUPS (for measurements and profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -457,6 +460,10 @@ def main():
     torch.cuda.set_device(device)
     import row_wise_normalization_reduce_gb300 as nrm
     nrm.lib()
+    if args.plan != "auto":
+        kind, *nums = args.plan.split(":")
+        code = {v: k for k, v in nrm.PLAN_NAMES.items()}[kind]
+        nrm.force_plan(code, *[int(v) for v in nums])
     stream = torch.cuda.Stream(device)
     l2 = l2_size(local)
 
