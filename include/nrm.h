@@ -191,9 +191,13 @@ typedef enum {
     NRM_PLAN_GENERIC = 1,   /* one CTA per row, scalar, two reads of the row */
     NRM_PLAN_WARP = 2,      /* one warp per row, row held in registers */
     NRM_PLAN_CTA = 3,       /* one CTA per row, row held in registers */
-    NRM_PLAN_TMA = 4        /* persistent CTAs of row groups; each group streams
+    NRM_PLAN_TMA = 4,       /* persistent CTAs of row groups; each group streams
                                rows into its own ring of shared-memory stages
                                with bulk asynchronous copies */
+    NRM_PLAN_PERSIST = 5,   /* persistent CTAs; the next row is loaded into
+                               registers while the current one is reduced */
+    NRM_PLAN_WRAW = 6       /* warp per row, the whole row's packs in registers,
+                               shuffle-only reductions */
 } nrm_plan;
 
 /*
@@ -202,9 +206,11 @@ typedef enum {
  * NRM_PLAN_TMA the shared-memory stages per group, at most 16, and the row
  * groups per CTA, at most 15) for every later row-operator call in this
  * process; plan 0 restores automatic choice.  A forced plan that cannot run
- * a given call makes that call return NRM_ERR_UNSUPPORTED.  Returns NRM_OK or
- * NRM_ERR_UNSUPPORTED for an unknown plan.  Process-wide; not meant to change
- * while calls run.
+ * a given call makes that call return NRM_ERR_UNSUPPORTED.  NRM_PLAN_GENERIC
+ * also makes bn_fwd_train use its two-kernel plan (partials in the workspace,
+ * then normalize) instead of one cluster of CTAs per channel.  Returns NRM_OK
+ * or NRM_ERR_UNSUPPORTED for an unknown plan.  Process-wide; not meant to
+ * change while calls run.
  */
 int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
 

@@ -16,8 +16,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libnrm.so")
 
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
-PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA, PLAN_TMA = 0, 1, 2, 3, 4
-PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta", 4: "tma"}
+PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA, PLAN_TMA, PLAN_PERSIST, PLAN_WRAW = range(7)
+PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta", 4: "tma", 5: "persist", 6: "wraw"}
 
 _DT = {torch.float32: NRM_F32, torch.float16: NRM_F16, torch.bfloat16: NRM_BF16}
 

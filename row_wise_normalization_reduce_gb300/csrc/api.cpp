@@ -143,26 +143,28 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
 
     // Automatic choice, from measurements on GB300 (cold L2): rows of up to
     // 1024 packs (8192 bf16 / 4096 fp32 values) run fastest as one CTA per row
-    // with the row in registers; longer rows through the row-group pipeline.
+    // with the row in registers (256 threads x 2 packs at 4096 bf16); rows of
+    // up to 2048 packs on persistent CTAs that prefetch the next row (1024 x 2
+    // at 16384 bf16); longer rows through the bulk-copy row-group pipeline.
     if (kind == PLAN_AUTO) {
+        fthreads = fpacks = fstages = fgroups = 0;
         if (!vec_ok)
             kind = PLAN_GENERIC;
         else if (P <= 32 * 8 && a.rows >= 4 * (int64_t)dev.sms)
             kind = PLAN_WARP;
         else if (P <= 1024)
             kind = PLAN_CTA;
-        else if (tma_ok)
+        else if (P <= 2048) {
+            kind = PLAN_PERSIST;
+            fpacks = 2;
+        } else if (tma_ok) {
             kind = PLAN_TMA;
-        else if (P <= 1024 * 4)
+            fpacks = 4;
+            fstages = 2;
+        } else if (P <= 1024 * 4)
             kind = PLAN_CTA;
         else
             kind = PLAN_GENERIC;
-        fthreads = fpacks = fstages = fgroups = 0;
-        if (kind == PLAN_TMA) {
-            fthreads = P <= 2048 ? 512 : 0;
-            fpacks = 4;
-            fstages = 2;
-        }
     }
 
     Plan p{};
@@ -203,6 +205,34 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
         break;
     }
+    case PLAN_WRAW: {
+        // one warp per row: 32 lanes x packs >= P; 8 warps per CTA by default
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        int packs = fpacks, threads = fthreads ? fthreads : 256;
+        if (!packs) {
+            const int64_t need = (P + 31) / 32;
+            packs = need <= 4 ? 4 : need <= 8 ? 8 : need <= 16 ? 16 : 32;
+        }
+        if ((int64_t)packs * 32 < P) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.smem_params = smem_params ? 1 : 0;
+        break;
+    }
+    case PLAN_PERSIST: {
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        int packs = fpacks, threads = fthreads;
+        if (!packs) packs = P <= 256 ? 1 : P <= 1024 ? 2 : 4;
+        if (!threads) {
+            threads = round_up_pow2((P + packs - 1) / packs);
+            if (threads < 128) threads = 128;
+        }
+        if (threads > 1024 || (int64_t)threads * packs < P) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.smem_params = smem_params ? 1 : 0;
+        break;
+    }
     case PLAN_TMA: {
         // Row groups of GT threads x PACKS packs (4 preferred), as many groups
         // per CTA as fit in 1024 threads and the shared memory with 3 (else 2)
@@ -218,7 +248,8 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         if ((int64_t)threads * packs < P) return NRM_ERR_UNSUPPORTED;
         int stages = fstages, groups = fgroups;
         auto fits = [&](int gr, int st) {
-            return gr * threads <= 1024 && fixed + (int64_t)gr * st * stage_bytes <= kSmemMax;
+            const int64_t prm = (smem_params && gr >= 4) ? param_bytes : 0;
+            return gr * threads <= 1024 && prm + (int64_t)gr * st * stage_bytes <= kSmemMax;
         };
         if (!groups || !stages) {
             int best_g = 0, best_s = 0;
@@ -246,7 +277,10 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.packs = packs;
         p.stages = stages;
         p.groups = groups;
-        p.smem_params = smem_params ? 1 : 0;
+        // binary32 parameters in shared memory pay off when several groups of
+        // a CTA share them; small CTAs read them through L1 (shared by every
+        // CTA of the SM) and keep their shared memory for stages.
+        p.smem_params = (smem_params && groups >= 4) ? 1 : 0;
         break;
     }
     default:
@@ -262,6 +296,8 @@ int run_row(Op op, RowArgs a, int dtype, cudaStream_t stream) {
     if (st != NRM_OK) return st;
     a.fault = fault_word();
     a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+    a.fN = (float)a.N;
+    a.invN = 1.0f / a.fN;
     Plan plan;
     st = choose_plan(op, a, dtype, dev, &plan);
     if (st != NRM_OK) return st;
@@ -323,7 +359,7 @@ int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *m
             if (overlap(o, i)) return NRM_ERR_ALIAS;
     if (overlap(sy, sm) || overlap(sy, sr) || overlap(sm, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, gamma, beta, y, mean, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps, nullptr, 0};
+    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
     return run_row(OP_LN, a, dtype, stream);
 }
 
@@ -343,7 +379,7 @@ int rms_fwd(const void *x, const void *w, void *y, float *rstd, int64_t rows, in
             if (overlap(o, i)) return NRM_ERR_ALIAS;
     if (overlap(sy, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, w, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps, nullptr, 0};
+    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
     return run_row(OP_RMS, a, dtype, stream);
 }
 
@@ -368,7 +404,7 @@ int add_rms_fwd(const void *x, const void *residual, const void *w, void *residu
     if (overlap(sy, sres) || overlap(sr, sres)) return NRM_ERR_ALIAS;
     if (overlap(sro, sy) || overlap(sro, sr) || overlap(sy, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, residual, w, residual_out, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0};
+    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
     return run_row(OP_ADD_RMS, a, dtype, stream);
 }
 
@@ -417,7 +453,9 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
     if ((st = device_info(&dev)) != NRM_OK) return st;
     BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
              static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
-             running_mean, running_var, batch, C, HW, eps, momentum, workspace};
+             running_mean, running_var, batch, C, HW, eps, momentum, workspace, fault_word(),
+             g_wait_limit.load(std::memory_order_relaxed),
+             g_force_kind.load(std::memory_order_relaxed) == PLAN_GENERIC ? 1 : 0};
     const cudaError_t e = launch_bn_train_f32(a, dev.sms, stream);
     return e == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }
@@ -441,7 +479,7 @@ const char *nrm_status_string(int status) {
 }
 
 int nrm_force_plan(int plan, int threads, int packs, int stages, int groups) {
-    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_TMA || threads < 0 || packs < 0 || stages < 0 ||
+    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_WRAW || threads < 0 || packs < 0 || stages < 0 ||
         stages > kMaxStages || groups < 0 || groups > 15)
         return NRM_ERR_UNSUPPORTED;
     g_force_kind.store(plan);

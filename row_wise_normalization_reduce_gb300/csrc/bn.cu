@@ -16,6 +16,8 @@
 // All statistics of channel c are taken on d = x - K_c with K_c the channel's
 // first element x[0, c, 0]: the shift keeps channels with a large mean and a
 // small spread free of cancellation.
+#include <cooperative_groups.h>
+
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -140,9 +142,210 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// One thread-block cluster per channel (the single-launch plan).
+//
+// The cs CTAs of cluster c split the batch: CTA rank r owns planes
+// n in [r*ppc, min((r+1)*ppc, batch)) of channel c and copies them into its
+// shared memory with one bulk asynchronous copy per plane (x is read from HBM
+// once).  Each CTA computes the statistics of its planes with a shifted,
+// corrected two-pass over shared memory (shift K = x[0, c, 0], so channels
+// with a large mean lose nothing to cancellation), publishes (count, mean,
+// M2) in its shared memory, and after a cluster barrier every CTA folds the
+// cs partials over distributed shared memory in rank order (so all agree bit
+// for bit), normalizes its planes from shared memory and writes y.  Rank 0
+// writes save_mean/save_rstd and the running statistics.  A second cluster
+// barrier keeps every CTA's partial readable until all have folded.  The
+// bulk-copy wait is bounded; on a give-up the CTA raises a fault bit, still
+// takes part in both cluster barriers, and drains its copies before exiting.
+// The second barrier is split: each CTA arrives once it has read the peers'
+// partials and waits only before it exits, so the barrier overlaps the
+// stores of y.
+// ---------------------------------------------------------------------------
+constexpr int BNC_THREADS = 512;
+
+__global__ void __launch_bounds__(BNC_THREADS) bn_cluster_kernel(const BnArgs a, const int ppc) {
+    namespace cg = cooperative_groups;
+    constexpr int NW = BNC_THREADS / 32;
+    extern __shared__ __align__(16) float4 sx4[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float s1[NW];
+    __shared__ float2 s2[NW];
+    __shared__ float part[3];  // count, mean, M2 of this CTA's planes (shifted)
+    __shared__ float stat[3];  // combined shifted mean, rstd, biased variance
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cs = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x;
+    const int64_t C = a.C, HW = a.HW;
+    const int64_t c = blockIdx.x / cs;
+    const int64_t n0 = (int64_t)rank * ppc;
+    const int64_t left = a.batch - n0;
+    const int np = (int)(left <= 0 ? 0 : left < ppc ? left : ppc);
+    const int q4 = (int)(HW / 4);  // float4 per plane
+    const uint32_t plane_bytes = (uint32_t)(HW * 4);
+    const float K = a.x[c * HW];   // x[0, c, 0]
+
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (np > 0) {
+            mbar_arrive_expect_tx(&bar, plane_bytes * (uint32_t)np);
+            for (int j = 0; j < np; ++j)
+                bulk_g2s(sx4 + (size_t)j * q4, a.x + ((n0 + j) * C + c) * HW, plane_bytes, &bar);
+        }
+    }
+    // one thread waits on the copies; the CTA barrier then releases the rest
+    __shared__ int s_ok;
+    if (tid == 0) {
+        const bool got = np == 0 || mbar_wait_bounded(&bar, 0, a.wait_limit);
+        if (!got) atomicOr(a.fault, FAULT_WAIT);
+        s_ok = got;
+    }
+    __syncthreads();
+    const bool ok = s_ok != 0;
+
+    // pass 1: sum of d = x - K over this CTA's planes
+    const float2 nk = f2(-K);
+    float2 acc = f2(0.f);
+    for (int j = 0; j < np; ++j)
+        for (int q = tid; q < q4; q += BNC_THREADS) {
+            const float4 v = sx4[(size_t)j * q4 + q];
+            acc = __fadd2_rn(acc, __fadd2_rn(make_float2(v.x, v.y), nk));
+            acc = __fadd2_rn(acc, __fadd2_rn(make_float2(v.z, v.w), nk));
+        }
+    const float cnt = (float)np * (float)HW;
+    const float tot = cta_sum_all<NW>(acc.x + acc.y, s1);
+    const float m0 = np ? tot / cnt : 0.f;
+    // pass 2: e = d - m0, corrected
+    float2 e1 = f2(0.f), e2 = f2(0.f);
+    for (int j = 0; j < np; ++j)
+        for (int q = tid; q < q4; q += BNC_THREADS) {
+            const float4 v = sx4[(size_t)j * q4 + q];
+            const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), f2(-m0));
+            const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), f2(-m0));
+            e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
+            e2 = __ffma2_rn(ea, ea, e2);
+            e2 = __ffma2_rn(eb, eb, e2);
+        }
+    const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2);
+    if (tid == 0) {
+        const float cc = np ? E.x / cnt : 0.f;
+        part[0] = cnt;
+        part[1] = m0 + cc;
+        part[2] = fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f);
+    }
+    cluster.sync();  // every partial of the cluster is written
+
+    // fold the cs partials in rank order: lanes 0..cs-1 of warp 0 read them
+    // from the peers' shared memory in parallel, lane 0 combines
+    if (tid < 32) {
+        float pn = 0.f, pm = 0.f, p2 = 0.f;
+        if (tid < cs) {
+            const float *pr = cluster.map_shared_rank(part, tid);
+            pn = pr[0];
+            pm = pr[1];
+            p2 = pr[2];
+        }
+        Stats st{0.f, 0.f, 0.f};
+        for (int r = 0; r < cs; ++r)
+            st = combine(st, Stats{__shfl_sync(0xffffffffu, pn, r), __shfl_sync(0xffffffffu, pm, r),
+                                   __shfl_sync(0xffffffffu, p2, r)});
+        if (tid == 0) {
+            const float ctot = (float)(a.batch * HW);
+            const float var = st.m2 / ctot;
+            stat[0] = st.mean;
+            stat[1] = 1.0f / sqrtf(var + a.eps);
+            stat[2] = var;
+        }
+    }
+    // Nobody reads a peer's partial after this point; arrive now and wait
+    // only before exiting, so the barrier overlaps the store phase.
+    cluster_arrive();
+    __syncthreads();
+    const float md = stat[0], rstd = stat[1];
+    if (rank == 0 && tid == 0) {
+        const float ctot = (float)(a.batch * HW);
+        if (a.save_mean) a.save_mean[c] = K + md;
+        if (a.save_rstd) a.save_rstd[c] = rstd;
+        const float m = a.momentum;
+        if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
+        if (a.running_var) {
+            const float unbiased = stat[2] * (ctot / (float)(a.batch * HW - 1));
+            a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
+        }
+    }
+
+    // normalize from shared memory: y = ((x - K) - md) * rstd * gamma + beta
+    const float g = a.gamma ? a.gamma[c] : 1.f;
+    const float b = a.beta ? a.beta[c] : 0.f;
+    const float2 sh = f2(-K), nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(b);
+    for (int j = 0; j < np; ++j) {
+        float4 *yp = reinterpret_cast<float4 *>(a.y + ((n0 + j) * C + c) * HW);
+        for (int q = tid; q < q4; q += BNC_THREADS) {
+            const float4 v = sx4[(size_t)j * q4 + q];
+            const float2 lo = __ffma2_rn(
+                __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), sh), nmd), r2), g2, b2);
+            const float2 hi = __ffma2_rn(
+                __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), sh), nmd), r2), g2, b2);
+            __stcs(yp + q, make_float4(lo.x, lo.y, hi.x, hi.y));
+        }
+    }
+    cluster_wait();  // peers are done reading this CTA's partial
+    if (tid == 0 && !ok && !mbar_wait_bounded(&bar, 0, 1u << 22)) atomicOr(a.fault, FAULT_DRAIN);
+}
+
 }  // namespace
 
+// Single launch when the channel's planes fit the shared memory of a cluster
+// of up to 8 CTAs and the rows are 16-byte aligned; else the two-kernel plan.
 cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s) {
+    const bool aligned = (a.HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
+    if (aligned && a.fault && !a.two_kernel && a.C <= 0x7fffffff / 8) {
+        int cs = 8;
+        while (cs > 1 && cs > a.batch) cs >>= 1;
+        const int64_t ppc = (a.batch + cs - 1) / cs;
+        const size_t smem = (size_t)ppc * (size_t)a.HW * 4;
+        if (smem <= (size_t)100 * 1024) {
+            static std::mutex mu;
+            static int attr_done[64];
+            int dev = 0;
+            cudaGetDevice(&dev);
+            {
+                std::lock_guard<std::mutex> lock(mu);
+                if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+                    if (cudaFuncSetAttribute(bn_cluster_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             100 * 1024) == cudaSuccess)
+                        attr_done[dev] = 1;
+                    else
+                        cudaGetLastError();
+                }
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(a.C * cs));
+            cfg.blockDim = dim3(BNC_THREADS);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) == cudaSuccess &&
+                clusters > 0) {
+                const cudaError_t e = cudaLaunchKernelEx(&cfg, bn_cluster_kernel, a, (int)ppc);
+                if (e == cudaSuccess) return cudaGetLastError();
+                return e;
+            }
+            cudaGetLastError();
+        }
+    }
     const int64_t planes = a.batch * a.C;
     const int64_t cap = (int64_t)num_sms * 64;
     const unsigned grid = (unsigned)(planes < cap ? planes : cap);
@@ -240,6 +443,7 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
     }
     BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
              static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
-             running_mean, running_var, batch, C, HW, eps, momentum, g_bn_static_ptr[dev]};
+             running_mean, running_var, batch, C, HW, eps, momentum, g_bn_static_ptr[dev],
+             fault_word(), 1u << 20, 0};
     return launch_bn_train_f32(a, sms, stream) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

@@ -355,24 +355,40 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// One try of the phase with the given parity.  The hint lets the hardware
+// suspend the thread for up to kWaitHintNs (it resumes as soon as the phase
+// completes), so a waiting warp does not spin on the issue slots.
+constexpr uint32_t kWaitHintNs = 1000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kWaitHintNs)
         : "memory");
     return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete, trying at most
-// `limit` times; false means the wait gave up.
+// `limit` times (each try suspends for at most kWaitHintNs); false means the
+// wait gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// Cluster barrier in two halves: arrive (release: this thread's earlier
+// memory accesses, including reads of peers' shared memory, are done) and
+// wait (acquire).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace nrm

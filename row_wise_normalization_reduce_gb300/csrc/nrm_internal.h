@@ -10,7 +10,15 @@ namespace nrm {
 
 enum Op { OP_LN = 0, OP_RMS = 1, OP_ADD_RMS = 2 };
 enum DType { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
-enum PlanKind { PLAN_AUTO = 0, PLAN_GENERIC = 1, PLAN_WARP = 2, PLAN_CTA = 3, PLAN_TMA = 4 };
+enum PlanKind {
+    PLAN_AUTO = 0,
+    PLAN_GENERIC = 1,
+    PLAN_WARP = 2,
+    PLAN_CTA = 3,
+    PLAN_TMA = 4,
+    PLAN_PERSIST = 5,
+    PLAN_WRAW = 6
+};
 
 // Bits of the device fault word (see fault.cu).
 enum FaultBits : unsigned {
@@ -40,6 +48,8 @@ struct RowArgs {
     float eps;
     unsigned *fault;      // device fault word of the current device
     unsigned wait_limit;  // tries per bounded wait (0: give up at once)
+    float fN;             // (float)N, and its correctly rounded reciprocal,
+    float invN;           // computed once on the host
 };
 
 struct Plan {
@@ -76,7 +86,10 @@ struct BnArgs {
     float *running_var;
     int64_t batch, C, HW;
     float eps, momentum;
-    void *ws;
+    void *ws;             // two-kernel plan: batch * C float2 partials
+    unsigned *fault;      // device fault word (cluster plan), or NULL
+    unsigned wait_limit;  // tries per bounded wait
+    int two_kernel;       // 1: skip the cluster plan
 };
 cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s);
 

@@ -13,6 +13,12 @@
 //                       with bulk asynchronous copies completed on mbarriers,
 //                       so rows are always in flight while others are reduced
 //                       (row_pipe.cuh).
+//   row_persist_kernel  persistent CTAs; the next row's packs are loaded into
+//                       registers while the current row is reduced, and the
+//                       parameters are widened to binary32 in shared memory
+//                       once per CTA.
+//   row_wraw_kernel     warp per row with the raw packs of the whole row in
+//                       registers; shuffle-only reductions; long rows.
 //   row_generic_kernel  any N and any alignment: scalar accesses, one CTA per
 //                       row, the row read twice (statistics, then output).
 //
@@ -139,33 +145,24 @@ struct NoHook {
     __device__ __forceinline__ void operator()() const {}
 };
 
-// One row, spread over a group whose member `t` owns packs t, t + STRIDE, ...
-// `after_sync` runs right after the first group-wide sum, when every member
-// has its values in registers (the bulk-copy pipeline refills the stage there).
-template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class Prm, class Hook>
-__device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, const int t,
-                                         Red &red, const Src &src, const Prm &prm,
-                                         const Hook &after_sync) {
+// Everything after the loads of one row: the row is spread over a group whose
+// member `t` owns packs t, t + STRIDE, ...; rx (and rr, the residual packs of
+// add+RMS) hold its raw 16-byte packs.  `after_sync` runs right after the
+// first group-wide sum, when every member has its values in registers (the
+// bulk-copy pipeline refills the stage there).
+template <int OP, typename T, int PACKS, int STRIDE, class Red, class Prm, class Hook>
+__device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row, const int t,
+                                            Red &red, const uint4 (&rx)[PACKS],
+                                            const uint4 (&rr)[PACKS], const Prm &prm,
+                                            const Hook &after_sync) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
     const int P = (int)(a.N / V);  // 16-byte packs per row (< 2^31 by construction)
-    const float fN = (float)a.N;
-    const float invN = 1.0f / fN;
+    const float fN = a.fN;
+    const float invN = a.invN;
     T *__restrict__ Y = static_cast<T *>(a.y) + row * a.N;
     T *__restrict__ RO = static_cast<T *>(a.res_out) + row * a.N;
-
-    // ---- S1/S2: issue every load of the row before any arithmetic ----
-    uint4 rx[PACKS];
-    uint4 rr[PACKS];
-#pragma unroll
-    for (int k = 0; k < PACKS; ++k) {
-        const int idx = t + k * STRIDE;
-        if (idx < P) {
-            rx[k] = src.x_pack(idx);
-            if (OP == OP_ADD_RMS) rr[k] = src.r_pack(idx);
-        }
-    }
 
     // v: the row's values (add+RMS: the rounded residual-stream value)
     float2 v[PACKS][H];
@@ -197,10 +194,12 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
         for (int k = 0; k < PACKS; ++k)
 #pragma unroll
             for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, v[k][h]);
-        // m0 by a correctly rounded division: a constant row gives m0 == x
-        // exactly, hence e == 0, c == 0 and y == beta bit for bit.
-        const float m0 = __fdiv_rn(red.sum(acc.x + acc.y), fN);
+        const float tot = red.sum(acc.x + acc.y);
         after_sync();
+        // m0 = tot / N, corrected once: a constant row (tot = N x exactly)
+        // gives m0 == x, hence e == 0, c == 0 and y == beta bit for bit.
+        float m0 = tot * invN;
+        m0 = fmaf(fmaf(-m0, fN, tot), invN, m0);
         const float2 nm = f2(-m0);
         float2 e1 = f2(0.f), e2 = f2(0.f);
 #pragma unroll
@@ -257,8 +256,44 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
     }
 }
 
+// Issue every load of one row (S1/S2) before any arithmetic.
+template <int OP, int PACKS, int STRIDE, class Src>
+__device__ __forceinline__ void row_load(const Src &src, const int t, const int P,
+                                         uint4 (&rx)[PACKS], uint4 (&rr)[PACKS]) {
+#pragma unroll
+    for (int k = 0; k < PACKS; ++k) {
+        const int idx = t + k * STRIDE;
+        if (idx < P) {
+            rx[k] = src.x_pack(idx);
+            if (OP == OP_ADD_RMS) rr[k] = src.r_pack(idx);
+        }
+    }
+}
+
+// One row: load, then compute.
+template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class Prm, class Hook>
+__device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, const int t,
+                                         Red &red, const Src &src, const Prm &prm,
+                                         const Hook &after_sync) {
+    uint4 rx[PACKS], rr[PACKS];
+    row_load<OP, PACKS, STRIDE>(src, t, (int)(a.N / IO<T>::V), rx, rr);
+    row_compute<OP, T, PACKS, STRIDE>(a, row, t, red, rx, rr, prm, after_sync);
+}
+
+// Resident threads per SM the CTA and persistent kernels with at most 2
+// packs per thread are compiled for (caps registers at 65536 /
+// NRM_CTA_MIN_THREADS): measured on GB300, 1280 (five 256-thread CTAs per SM,
+// at most 51 registers) keeps the most row loads in flight; 1024 and 1536
+// were slower.  Wider per-thread rows get no cap (they would spill).
+#ifndef NRM_CTA_MIN_THREADS
+#define NRM_CTA_MIN_THREADS 1280
+#endif
+#define NRM_MIN_BLOCKS(THREADS, PACKS)                                                   \
+    (((PACKS) <= 2 && NRM_CTA_MIN_THREADS / (THREADS) > 0) ? NRM_CTA_MIN_THREADS / (THREADS) : 1)
+
 template <int OP, typename T, int THREADS, int PACKS>
-__global__ void __launch_bounds__(THREADS) row_cta_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
+    row_cta_kernel(const RowArgs a) {
     constexpr int NW = THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
@@ -270,6 +305,178 @@ __global__ void __launch_bounds__(THREADS) row_cta_kernel(const RowArgs a) {
         const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
         const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
         row_body<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, src, prm, NoHook{});
+    }
+}
+
+// Persistent register pipeline: CTA b handles rows b, b + G, ... (G =
+// gridDim.x, as many CTAs as are resident).  Row r + G's packs are loaded
+// into registers before row r is reduced, so every CTA always has a row in
+// flight; parameters are widened to binary32 in shared memory once per CTA
+// (SmemParams layout) when smem_params is set.
+template <int OP, typename T, int THREADS, int PACKS>
+__global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
+    row_persist_kernel(const RowArgs a, const int smem_params) {
+    constexpr int NW = THREADS / 32;
+    extern __shared__ __align__(16) float4 sparams[];
+    __shared__ float s1[2][NW];
+    __shared__ float2 s2[2][NW];
+    const int P = (int)(a.N / IO<T>::V);
+    const T *X = static_cast<const T *>(a.x);
+    const T *R = static_cast<const T *>(a.res);
+    if (smem_params)
+        fill_smem_params<T, (OP == OP_LN ? 2 : 1), THREADS>(a, reinterpret_cast<float *>(sparams));
+    __syncthreads();
+    const SmemParams<T> sprm{sparams, P};
+    const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+    const int64_t G = gridDim.x;
+
+    uint4 rx[PACKS], rr[PACKS];
+    int64_t row = blockIdx.x;
+    if (row < a.rows) {
+        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        row_load<OP, PACKS, THREADS>(src, threadIdx.x, P, rx, rr);
+    }
+    int parity = 0;
+    for (; row < a.rows; row += G, parity ^= 1) {
+        uint4 nx[PACKS], nr[PACKS];
+        const int64_t next = row + G;
+        if (next < a.rows) {
+            const GlobalSrc<T> src{X + next * a.N, R + next * a.N};
+            row_load<OP, PACKS, THREADS>(src, threadIdx.x, P, nx, nr);
+        }
+        CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
+        if (smem_params)
+            row_compute<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, rx, rr, sprm, NoHook{});
+        else
+            row_compute<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, rx, rr, gprm, NoHook{});
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            rx[k] = nx[k];
+            if (OP == OP_ADD_RMS) rr[k] = nr[k];
+        }
+    }
+}
+
+// Warp per row, raw packs in registers: each warp owns whole rows (row r of
+// the grid-stride loop), issues all PACKS 16-byte loads of its row at once
+// (a whole 4096-wide bf16 row, 8 KB, in flight per warp), reduces with
+// shuffles only -- no CTA barrier -- and unpacks the packs again for each
+// pass instead of holding binary32 copies.  The CTA's warps share the
+// parameters widened to binary32 in shared memory (when smem_params).
+// Sized so that an SM keeps well over 100 KB of row loads in flight, which
+// GB300's loaded memory latency needs to stream at HBM speed.
+template <int OP, typename T, int PACKS, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, const int smem_params) {
+    using io2 = IO2<T>;
+    constexpr int V = IO<T>::V;
+    constexpr int H = io2::H;
+    extern __shared__ __align__(16) float4 sparams[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int P = (int)(a.N / V);
+    const float fN = a.fN, invN = a.invN;
+    if (smem_params)
+        fill_smem_params<T, (OP == OP_LN ? 2 : 1), WARPS * 32>(a, reinterpret_cast<float *>(sparams));
+    __syncthreads();
+    const SmemParams<T> sprm{sparams, P};
+    const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+    const T *X = static_cast<const T *>(a.x);
+    const T *R = static_cast<const T *>(a.res);
+
+    for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < a.rows;
+         row += (int64_t)gridDim.x * WARPS) {
+        const T *xr = X + row * a.N;
+        uint4 raw[PACKS];
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k)
+            if (lane + 32 * k < P) raw[k] = ld_stream(xr + (size_t)(lane + 32 * k) * V);
+        if (OP == OP_ADD_RMS) {
+            const T *rr = R + row * a.N;
+            T *RO = static_cast<T *>(a.res_out) + row * a.N;
+#pragma unroll
+            for (int k = 0; k < PACKS; ++k) {
+                const int idx = lane + 32 * k;
+                if (idx < P) {
+                    float2 fx[H], fr[H];
+                    io2::unpack(raw[k], fx);
+                    io2::unpack(ld_stream(rr + (size_t)idx * V), fr);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) fx[h] = __fadd2_rn(fx[h], fr[h]);
+                    raw[k] = io2::pack(fx);  // round once to T
+                    st_stream(RO + (size_t)idx * V, raw[k]);
+                }
+            }
+        }
+        // pass 1
+        float2 acc = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            if (lane + 32 * k < P) {
+                float2 f[H];
+                io2::unpack(raw[k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    acc = (OP == OP_LN) ? __fadd2_rn(acc, f[h]) : __ffma2_rn(f[h], f[h], acc);
+            }
+        }
+        const float tot = warp_sum_all(acc.x + acc.y);
+        float rstd, m0 = 0.f, c = 0.f;
+        if (OP == OP_LN) {
+            m0 = tot * invN;
+            m0 = fmaf(fmaf(-m0, fN, tot), invN, m0);  // exact for constant rows
+            const float2 nm = f2(-m0);
+            float2 e1 = f2(0.f), e2 = f2(0.f);
+#pragma unroll
+            for (int k = 0; k < PACKS; ++k) {
+                if (lane + 32 * k < P) {
+                    float2 f[H];
+                    io2::unpack(raw[k], f);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        const float2 e = __fadd2_rn(f[h], nm);
+                        e1 = __fadd2_rn(e1, e);
+                        e2 = __ffma2_rn(e, e, e2);
+                    }
+                }
+            }
+            const float2 E = warp_sum_all(make_float2(e1.x + e1.y, e2.x + e2.y));
+            c = E.x * invN;
+            const float var = fmaxf(fmaf(-c, c, E.y * invN), 0.f);
+            rstd = rsqrtf(var + a.eps);
+            if (lane == 0) {
+                if (a.mean) a.mean[row] = m0 + c;
+                if (a.rstd) a.rstd[row] = rstd;
+            }
+        } else {
+            rstd = rsqrtf(fmaf(tot, invN, a.eps));
+            if (lane == 0 && a.rstd) a.rstd[row] = rstd;
+        }
+        // pass 3: normalize, scale (and shift), round once, store
+        T *Y = static_cast<T *>(a.y) + row * a.N;
+        const float2 r2 = f2(rstd), nm = f2(-m0), nc = f2(-c);
+#pragma unroll
+        for (int k = 0; k < PACKS; ++k) {
+            const int idx = lane + 32 * k;
+            if (idx < P) {
+                float2 f[H], g2[H], out[H];
+                io2::unpack(raw[k], f);
+                if (smem_params) sprm.p0_pack(idx, g2);
+                else gprm.p0_pack(idx, g2);
+                if (OP == OP_LN) {
+                    float2 b2[H];
+                    if (smem_params) sprm.p1_pack(idx, b2);
+                    else gprm.p1_pack(idx, b2);
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+                        out[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nm), nc), r2),
+                                            g2[h], b2[h]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < H; ++h) out[h] = __fmul2_rn(__fmul2_rn(f[h], r2), g2[h]);
+                }
+                st_stream(Y + (size_t)idx * V, io2::pack(out));
+            }
+        }
     }
 }
 
@@ -424,6 +631,79 @@ cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Persistent register-pipeline launch: dynamic shared memory = parameters in
+// binary32 (when smem_params), grid = min(rows, SMs x resident CTAs per SM).
+template <int OP, typename T, int THREADS, int PACKS>
+cudaError_t launch_persist(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    auto kernel = row_persist_kernel<OP, T, THREADS, PACKS>;
+    if (p.sms < 1) return cudaErrorInvalidConfiguration;
+    const size_t smem = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
+    if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::mutex mu;  // one cache per kernel instance
+    static size_t cached_smem[64] = {};
+    static int cached_per_sm[64] = {};
+    static bool cached[64] = {};
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!cached[dev] || cached_smem[dev] != smem) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, THREADS,
+                                                              smem);
+            if (e != cudaSuccess) return e;
+            cached_smem[dev] = smem;
+            cached[dev] = true;
+        }
+        per_sm = cached_per_sm[dev];
+    }
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t slots = (int64_t)p.sms * per_sm;
+    const int64_t grid = a.rows < slots ? a.rows : slots;
+    kernel<<<(unsigned)grid, THREADS, smem, s>>>(a, p.smem_params);
+    return cudaGetLastError();
+}
+
+// Warp-per-row launch: dynamic shared memory = parameters in binary32 (when
+// smem_params), grid = min(ceil(rows / WARPS), SMs x resident CTAs per SM).
+template <int OP, typename T, int PACKS, int WARPS>
+cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    auto kernel = row_wraw_kernel<OP, T, PACKS, WARPS>;
+    if (p.sms < 1) return cudaErrorInvalidConfiguration;
+    const size_t smem = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
+    if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::mutex mu;  // one cache per kernel instance
+    static size_t cached_smem[64] = {};
+    static int cached_per_sm[64] = {};
+    static bool cached[64] = {};
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!cached[dev] || cached_smem[dev] != smem) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel,
+                                                              WARPS * 32, smem);
+            if (e != cudaSuccess) return e;
+            cached_smem[dev] = smem;
+            cached[dev] = true;
+        }
+        per_sm = cached_per_sm[dev];
+    }
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t need = (a.rows + WARPS - 1) / WARPS;
+    const int64_t slots = (int64_t)p.sms * per_sm;
+    const int64_t grid = need < slots ? need : slots;
+    kernel<<<(unsigned)grid, WARPS * 32, smem, s>>>(a, p.smem_params);
+    return cudaGetLastError();
+}
+
 template <int OP, typename T>
 cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const dim3 grid((unsigned)p.grid);
@@ -453,6 +733,21 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
         NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)
 #undef NRM_CTA_CASE
+        return cudaErrorInvalidConfiguration;
+    } else if (p.kind == PLAN_WRAW) {
+#define NRM_WRAW_CASE(PK, WP)                                                      \
+    if (p.packs == PK && p.threads == WP * 32) return launch_wraw<OP, T, PK, WP>(a, p, s);
+        NRM_WRAW_CASE(4, 8) NRM_WRAW_CASE(8, 8) NRM_WRAW_CASE(16, 8) NRM_WRAW_CASE(16, 16)
+        NRM_WRAW_CASE(8, 16) NRM_WRAW_CASE(32, 8)
+#undef NRM_WRAW_CASE
+        return cudaErrorInvalidConfiguration;
+    } else if (p.kind == PLAN_PERSIST) {
+#define NRM_PERSIST_CASE(TH, PK)                                                   \
+    if (p.threads == TH && p.packs == PK) return launch_persist<OP, T, TH, PK>(a, p, s);
+        NRM_PERSIST_CASE(128, 4) NRM_PERSIST_CASE(256, 1) NRM_PERSIST_CASE(256, 2)
+        NRM_PERSIST_CASE(256, 4) NRM_PERSIST_CASE(512, 1) NRM_PERSIST_CASE(512, 2)
+        NRM_PERSIST_CASE(1024, 2)
+#undef NRM_PERSIST_CASE
         return cudaErrorInvalidConfiguration;
     } else if (p.kind == PLAN_TMA) {
 #define NRM_PIPE_CASE(GT, PK, GR)                                                  \

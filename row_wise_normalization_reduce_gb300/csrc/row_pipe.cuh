@@ -52,8 +52,10 @@ __device__ __forceinline__ void pipe_claim(const RowArgs &a, unsigned long long 
     }
 }
 
+// Launch bounds ask for at least 1024 resident threads per SM (at most 64
+// registers per thread), so several CTAs share an SM and their rows overlap.
 template <int OP, typename T, int GT, int PACKS, int G>
-__global__ void __launch_bounds__(GT *G, 1)
+__global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G)) : 1)
     row_pipe_kernel(const RowArgs a, const int stages, const int smem_params) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
@@ -98,8 +100,8 @@ __global__ void __launch_bounds__(GT *G, 1)
     if (smem_params) fill_smem_params<T, (OP == OP_LN ? 2 : 1), GT * G>(a, reinterpret_cast<float *>(smem));
     __syncthreads();
 
-    const float fN = (float)a.N;
-    const float invN = 1.0f / fN;
+    const float fN = a.fN;
+    const float invN = a.invN;
     const SmemParams<T> sprm{reinterpret_cast<const float4 *>(smem), P};
     const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
 

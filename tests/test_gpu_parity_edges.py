@@ -65,7 +65,9 @@ PLANS = [(nrm.PLAN_GENERIC, 128, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_GENER
          (nrm.PLAN_CTA, 256, 4), (nrm.PLAN_CTA, 512, 4), (nrm.PLAN_CTA, 1024, 4),
          (nrm.PLAN_CTA, 1024, 2), (nrm.PLAN_CTA, 512, 2),
          (nrm.PLAN_TMA, 128, 4, 2, 1), (nrm.PLAN_TMA, 128, 4, 3, 8), (nrm.PLAN_TMA, 256, 2, 0, 0),
-         (nrm.PLAN_TMA, 256, 4, 5, 2), (nrm.PLAN_TMA, 512, 4, 2, 2), (nrm.PLAN_TMA, 128, 8, 16, 1)]
+         (nrm.PLAN_TMA, 256, 4, 5, 2), (nrm.PLAN_TMA, 512, 4, 2, 2), (nrm.PLAN_TMA, 128, 8, 16, 1),
+         (nrm.PLAN_PERSIST, 256, 1), (nrm.PLAN_PERSIST, 128, 4), (nrm.PLAN_PERSIST, 1024, 2),
+         (nrm.PLAN_WRAW, 256, 8), (nrm.PLAN_WRAW, 512, 16), (nrm.PLAN_WRAW, 256, 32)]
 
 
 @pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
@@ -103,6 +105,26 @@ def test_tma_pipeline_many_rows_per_cta(orc, op, dt, threads, packs, groups, sta
         assert e.status == 6
         pytest.skip("stages x groups exceed the shared memory of one CTA")
     assert nrm.last_plan() == (nrm.PLAN_TMA, threads, packs, stages, groups)
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt,threads,packs", [("bf16", 256, 2), ("f32", 512, 2), ("f16", 128, 4)])
+def test_persist_many_rows_per_cta(orc, op, dt, threads, packs):
+    # 3001 rows over the resident CTAs: each CTA prefetches row r + G while it
+    # reduces row r, several times over, and ends on a ragged last round.
+    inp = W.generic_rows(op, dt, 3001, 4096, seed=31, scale=0.7, shift=2.0)
+    nrm.force_plan(nrm.PLAN_PERSIST, threads, packs)
+    _check(orc, op, inp)
+    assert nrm.last_plan()[:3] == (nrm.PLAN_PERSIST, threads, packs)
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt,n", [("bf16", 4096), ("f32", 2048), ("f16", 4096), ("bf16", 3000)])
+def test_wraw_many_rows(orc, op, dt, n):
+    inp = W.generic_rows(op, dt, 1501, n, seed=41, scale=1.1, shift=-0.3)
+    nrm.force_plan(nrm.PLAN_WRAW, 256, 16)
+    _check(orc, op, inp)
+    assert nrm.last_plan()[:3] == (nrm.PLAN_WRAW, 256, 16)
 
 
 def test_tma_wait_give_up_path(orc):
@@ -226,21 +248,40 @@ def test_guard_bands_untouched(op):
 
 
 # ---- BatchNorm ------------------------------------------------------------
+BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_GENERIC]  # cluster per channel / two kernels
+
+
+@pytest.mark.parametrize("plan", BN_PLANS, ids=["cluster", "two_kernel"])
 @pytest.mark.parametrize("shape", [(1, 1, 7, 7), (1, 3, 5, 5), (2, 4, 3, 3), (8, 16, 28, 28),
-                                   (4, 8, 1, 1), (3, 5, 13, 11), (64, 3, 8, 8)])
-def test_bn_shapes(orc, shape):
+                                   (4, 8, 1, 1), (3, 5, 13, 11), (64, 3, 8, 8), (5, 7, 20, 20),
+                                   (13, 2, 12, 12), (32, 4, 56, 56)])
+def test_bn_shapes(orc, shape, plan):
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape)
+    nrm.force_plan(plan)
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
     ref = RN.run_oracle(orc, "bn", inp, 1e-5, 0.1)
     RN.compare("bn", inp, gpu, ref)
 
 
-def test_bn_large_mean_channel(orc):
+@pytest.mark.parametrize("plan", BN_PLANS, ids=["cluster", "two_kernel"])
+def test_bn_large_mean_channel(orc, plan):
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(4, 3, 16, 16))
     inp["x"][:, 1] += 1000.0
+    nrm.force_plan(plan)
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
     ref = RN.run_oracle(orc, "bn", inp, 1e-5, 0.1)
     RN.compare("bn", inp, gpu, ref)
+
+
+def test_bn_plans_agree_and_repeat():
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 8, 28, 28))
+    outs = []
+    for plan in (nrm.PLAN_AUTO, nrm.PLAN_AUTO, nrm.PLAN_GENERIC):
+        nrm.force_plan(plan)
+        outs.append(RN.run_gpu("bn", inp, 1e-5, 0.1))
+    for k in outs[0]:
+        assert (outs[0][k] == outs[1][k]).all(), k  # bitwise repeatable
+        assert np.max(np.abs(outs[0][k].astype(np.float64) - outs[2][k])) <= 2e-5, k
 
 
 def test_bn_without_optionals(orc):
