@@ -206,11 +206,13 @@ typedef enum {
  * NRM_PLAN_TMA the shared-memory stages per group, at most 16, and the row
  * groups per CTA, at most 15) for every later row-operator call in this
  * process; plan 0 restores automatic choice.  A forced plan that cannot run
- * a given call makes that call return NRM_ERR_UNSUPPORTED.  NRM_PLAN_GENERIC
- * also makes bn_fwd_train use its two-kernel plan (partials in the workspace,
- * then normalize) instead of one cluster of CTAs per channel.  Returns NRM_OK
- * or NRM_ERR_UNSUPPORTED for an unknown plan.  Process-wide; not meant to
- * change while calls run.
+ * a given call makes that call return NRM_ERR_UNSUPPORTED.  bn_fwd_train
+ * follows the forced plan too: NRM_PLAN_CTA selects its streaming two-kernel
+ * plan (per-plane statistics into the workspace, then a dependent launch that
+ * normalizes), NRM_PLAN_TMA one cluster of CTAs per channel (shared memory and
+ * distributed shared memory, no workspace), NRM_PLAN_GENERIC the scalar
+ * two-kernel plan for any layout.  Returns NRM_OK or NRM_ERR_UNSUPPORTED for
+ * an unknown plan.  Process-wide; not meant to change while calls run.
  */
 int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
 

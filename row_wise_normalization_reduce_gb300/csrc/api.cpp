@@ -105,6 +105,17 @@ int check_pointers(std::initializer_list<const void *> ps) {
 
 bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.f; }
 
+// BatchNorm plan from the forced row plan (a test and measurement hook):
+// GENERIC -> scalar two kernels, TMA -> cluster per channel, CTA -> streaming.
+int bn_plan_from_forced() {
+    switch (g_force_kind.load(std::memory_order_relaxed)) {
+    case PLAN_GENERIC: return BN_PLAN_SCALAR;
+    case PLAN_TMA: return BN_PLAN_CLUSTER;
+    case PLAN_CTA: return BN_PLAN_STREAM;
+    default: return BN_PLAN_AUTO;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Plan choice for the row operators.
 // ---------------------------------------------------------------------------
@@ -454,8 +465,7 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
     BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
              static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
              running_mean, running_var, batch, C, HW, eps, momentum, workspace, fault_word(),
-             g_wait_limit.load(std::memory_order_relaxed),
-             g_force_kind.load(std::memory_order_relaxed) == PLAN_GENERIC ? 1 : 0};
+             g_wait_limit.load(std::memory_order_relaxed), bn_plan_from_forced()};
     const cudaError_t e = launch_bn_train_f32(a, dev.sms, stream);
     return e == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

@@ -143,210 +143,450 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// One thread-block cluster per channel (the single-launch plan).
+// Streaming two-kernel plan (the default for 16-byte aligned planes).
 //
-// The cs CTAs of cluster c split the batch: CTA rank r owns planes
-// n in [r*ppc, min((r+1)*ppc, batch)) of channel c and copies them into its
-// shared memory with one bulk asynchronous copy per plane (x is read from HBM
-// once).  Each CTA computes the statistics of its planes with a shifted,
+// bn_stats_kernel: one CTA per (n, c) plane holds the plane in registers
+// (PACKS float4 per thread) and computes its exact partial statistics on
+// d = x - K (K = x[0, c, 0]) with a corrected two-pass: (mean_d, M2) into the
+// workspace.  It then allows the dependent launch to start.
+// bn_norm_kernel (launched with programmatic stream serialization): each CTA
+// loads its plane of x into registers first -- x is an input, and for a batch
+// that fits in L2 these reads hit L2 -- then waits for the statistics kernel
+// (griddepcontrol.wait), folds the channel's batch partials in a fixed order
+// (every CTA of a channel gets the same bits), normalizes and writes y.  The
+// CTA of plane n = 0 writes save_mean/save_rstd and the running statistics.
+// ---------------------------------------------------------------------------
+constexpr int BNS_THREADS = 256;
+constexpr int BNS_PACKS = 4;  // float4 per thread: planes of up to 4096 values
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
+    constexpr int NW = BNS_THREADS / 32;
+    __shared__ float s1[2][NW];
+    __shared__ float2 s2[2][NW];
+    const int tid = threadIdx.x;
+    const int64_t planes = a.batch * a.C, HW = a.HW;
+    const int q4 = (int)(HW / 4);
+    const float cnt = (float)HW;
+    float2 *ws = static_cast<float2 *>(a.ws);
+    int par = 0;
+    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
+        const int64_t n = p / a.C, c = p - n * a.C;
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + p * HW);
+        // first read of x: default L2 policy, so the normalize kernel's second
+        // read finds it in L2 (a streaming, evict-first read would lose it)
+        float4 v[BNS_PACKS];
+#pragma unroll
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < q4) v[k] = __ldg(xp + tid + k * BNS_THREADS);
+        const float K = a.x[c * HW];
+        const float2 nk = f2(-K);
+        float2 acc = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < q4)
+                acc = __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk),
+                                                 __fadd2_rn(make_float2(v[k].z, v[k].w), nk)));
+        const float tot = cta_sum_all<NW>(acc.x + acc.y, s1[par]);
+        const float m0 = tot / cnt;
+        const float2 nkm = f2(-m0);
+        float2 e1 = f2(0.f), e2 = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < q4) {
+                const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk), nkm);
+                const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v[k].z, v[k].w), nk), nkm);
+                e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
+                e2 = __ffma2_rn(ea, ea, e2);
+                e2 = __ffma2_rn(eb, eb, e2);
+            }
+        const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2[par]);
+        if (tid == 0) {
+            const float cc = E.x / cnt;
+            ws[c * a.batch + n] = make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
+        }
+    }
+    pdl_launch_dependents();
+}
+
+__global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
+    __shared__ float stat[2][3];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t planes = a.batch * a.C, HW = a.HW;
+    const int q4 = (int)(HW / 4);
+    const float ctot = (float)(a.batch * HW);
+    const float2 *ws = static_cast<const float2 *>(a.ws);
+    bool waited = false;
+    int par = 0;
+    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
+        const int64_t n = p / a.C, c = p - n * a.C;
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + p * HW);
+        float4 v[BNS_PACKS];
+#pragma unroll
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < q4) v[k] = __ldcs(xp + tid + k * BNS_THREADS);
+        const float K = a.x[c * HW];
+        if (!waited) {
+            pdl_wait();  // the statistics kernel has finished and its writes are visible
+            waited = true;
+        }
+        if (warp == 0) {
+            Stats st{0.f, 0.f, 0.f};
+            for (int64_t j = lane; j < a.batch; j += 32) {
+                const float2 q = ws[c * a.batch + j];
+                st = combine(st, Stats{(float)HW, q.x, q.y});
+            }
+            st = warp_stats_down(st);
+            if (lane == 0) {
+                const float var = st.m2 / ctot;
+                stat[par][0] = st.mean;
+                stat[par][1] = 1.0f / sqrtf(var + a.eps);
+                stat[par][2] = var;
+            }
+        }
+        __syncthreads();
+        const float md = stat[par][0], rstd = stat[par][1];
+        if (n == 0 && tid == 0) {
+            if (a.save_mean) a.save_mean[c] = K + md;
+            if (a.save_rstd) a.save_rstd[c] = rstd;
+            const float m = a.momentum;
+            if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
+            if (a.running_var) {
+                const float unbiased = stat[par][2] * (ctot / (float)(a.batch * HW - 1));
+                a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
+            }
+        }
+        const float g = a.gamma ? a.gamma[c] : 1.f;
+        const float bb = a.beta ? a.beta[c] : 0.f;
+        const float2 nk = f2(-K), nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
+        float4 *yp = reinterpret_cast<float4 *>(a.y + p * HW);
+#pragma unroll
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < q4) {
+                const float2 lo = __ffma2_rn(
+                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk), nmd), r2), g2, b2);
+                const float2 hi = __ffma2_rn(
+                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v[k].z, v[k].w), nk), nmd), r2), g2, b2);
+                __stcs(yp + tid + k * BNS_THREADS, make_float4(lo.x, lo.y, hi.x, hi.y));
+            }
+    }
+    if (!waited) pdl_wait();
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters over channels (a single-launch plan).
+//
+// Cluster k (cs CTAs) handles channels k, k + K, k + 2K, ... (K clusters).
+// The cs CTAs split the batch: CTA rank r owns planes n in [r*ppc,
+// min((r+1)*ppc, batch)) of the channel.  Each CTA has two shared-memory
+// buffers: while channel i is reduced and written from one buffer, the planes
+// of channel i+1 stream into the other (one bulk asynchronous copy per
+// plane), so x is read from HBM once and loads overlap the stores.
+//
+// Per channel a CTA computes the statistics of its planes with a shifted,
 // corrected two-pass over shared memory (shift K = x[0, c, 0], so channels
 // with a large mean lose nothing to cancellation), publishes (count, mean,
-// M2) in its shared memory, and after a cluster barrier every CTA folds the
-// cs partials over distributed shared memory in rank order (so all agree bit
-// for bit), normalizes its planes from shared memory and writes y.  Rank 0
-// writes save_mean/save_rstd and the running statistics.  A second cluster
-// barrier keeps every CTA's partial readable until all have folded.  The
-// bulk-copy wait is bounded; on a give-up the CTA raises a fault bit, still
-// takes part in both cluster barriers, and drains its copies before exiting.
-// The second barrier is split: each CTA arrives once it has read the peers'
-// partials and waits only before it exits, so the barrier overlaps the
-// stores of y.
+// M2), and after a cluster barrier every CTA folds the cs partials over
+// distributed shared memory in rank order (all agree bit for bit), then
+// normalizes its planes and writes y.  Rank 0 writes save_mean/save_rstd and
+// the running statistics.  The barrier that protects the partials is split:
+// each CTA arrives right after its fold and waits only before it writes the
+// next channel's partial (or exits), so it overlaps the stores of y.  The
+// bulk-copy waits are bounded; on a give-up the CTA raises a fault bit, keeps
+// taking part in every barrier, and drains its copies before exiting.
 // ---------------------------------------------------------------------------
 constexpr int BNC_THREADS = 512;
 
-__global__ void __launch_bounds__(BNC_THREADS) bn_cluster_kernel(const BnArgs a, const int ppc) {
+__device__ __forceinline__ void bn_issue_planes(const BnArgs &a, float4 *buf, uint64_t *bar,
+                                                int64_t c, int64_t n0, int np, int q4,
+                                                uint32_t plane_bytes) {
+    mbar_arrive_expect_tx(bar, plane_bytes * (uint32_t)np);
+    for (int j = 0; j < np; ++j)
+        bulk_g2s(buf + (size_t)j * q4, a.x + ((n0 + j) * a.C + c) * a.HW, plane_bytes, bar);
+}
+
+// Four 512-thread CTAs per SM (at most 32 registers): with fewer, the 8-CTA
+// clusters of a 64-channel batch no longer all fit at once.
+__global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs a, const int ppc) {
     namespace cg = cooperative_groups;
     constexpr int NW = BNC_THREADS / 32;
-    extern __shared__ __align__(16) float4 sx4[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ float s1[NW];
-    __shared__ float2 s2[NW];
-    __shared__ float part[3];  // count, mean, M2 of this CTA's planes (shifted)
-    __shared__ float stat[3];  // combined shifted mean, rstd, biased variance
+    extern __shared__ __align__(16) float4 sx4[];  // two buffers of ppc planes
+    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ float s1[2][NW];
+    __shared__ float2 s2[2][NW];
+    __shared__ float part[2][3];  // count, mean, M2 of this CTA's planes (shifted)
+    __shared__ float stat[2][3];  // combined shifted mean, rstd, biased variance
+    __shared__ int s_ok[2];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x;
     const int64_t C = a.C, HW = a.HW;
-    const int64_t c = blockIdx.x / cs;
+    const int64_t K_clusters = gridDim.x / cs;
+    const int64_t first_c = blockIdx.x / cs;
     const int64_t n0 = (int64_t)rank * ppc;
     const int64_t left = a.batch - n0;
     const int np = (int)(left <= 0 ? 0 : left < ppc ? left : ppc);
     const int q4 = (int)(HW / 4);  // float4 per plane
     const uint32_t plane_bytes = (uint32_t)(HW * 4);
-    const float K = a.x[c * HW];   // x[0, c, 0]
-
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-        if (np > 0) {
-            mbar_arrive_expect_tx(&bar, plane_bytes * (uint32_t)np);
-            for (int j = 0; j < np; ++j)
-                bulk_g2s(sx4 + (size_t)j * q4, a.x + ((n0 + j) * C + c) * HW, plane_bytes, &bar);
-        }
-    }
-    // one thread waits on the copies; the CTA barrier then releases the rest
-    __shared__ int s_ok;
-    if (tid == 0) {
-        const bool got = np == 0 || mbar_wait_bounded(&bar, 0, a.wait_limit);
-        if (!got) atomicOr(a.fault, FAULT_WAIT);
-        s_ok = got;
-    }
-    __syncthreads();
-    const bool ok = s_ok != 0;
-
-    // pass 1: sum of d = x - K over this CTA's planes
-    const float2 nk = f2(-K);
-    float2 acc = f2(0.f);
-    for (int j = 0; j < np; ++j)
-        for (int q = tid; q < q4; q += BNC_THREADS) {
-            const float4 v = sx4[(size_t)j * q4 + q];
-            acc = __fadd2_rn(acc, __fadd2_rn(make_float2(v.x, v.y), nk));
-            acc = __fadd2_rn(acc, __fadd2_rn(make_float2(v.z, v.w), nk));
-        }
+    const size_t buf_f4 = (size_t)ppc * q4;
     const float cnt = (float)np * (float)HW;
-    const float tot = cta_sum_all<NW>(acc.x + acc.y, s1);
-    const float m0 = np ? tot / cnt : 0.f;
-    // pass 2: e = d - m0, corrected
-    float2 e1 = f2(0.f), e2 = f2(0.f);
-    for (int j = 0; j < np; ++j)
-        for (int q = tid; q < q4; q += BNC_THREADS) {
-            const float4 v = sx4[(size_t)j * q4 + q];
-            const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), f2(-m0));
-            const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), f2(-m0));
-            e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
-            e2 = __ffma2_rn(ea, ea, e2);
-            e2 = __ffma2_rn(eb, eb, e2);
-        }
-    const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2);
+    const float ctot = (float)(a.batch * HW);
+
+    // thread 0's bookkeeping: iteration whose planes were last issued into /
+    // last received from each buffer (for the drain after a give-up)
+    int last_issued0 = -1, last_issued1 = -1, last_done0 = -1, last_done1 = -1;
     if (tid == 0) {
-        const float cc = np ? E.x / cnt : 0.f;
-        part[0] = cnt;
-        part[1] = m0 + cc;
-        part[2] = fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f);
-    }
-    cluster.sync();  // every partial of the cluster is written
-
-    // fold the cs partials in rank order: lanes 0..cs-1 of warp 0 read them
-    // from the peers' shared memory in parallel, lane 0 combines
-    if (tid < 32) {
-        float pn = 0.f, pm = 0.f, p2 = 0.f;
-        if (tid < cs) {
-            const float *pr = cluster.map_shared_rank(part, tid);
-            pn = pr[0];
-            pm = pr[1];
-            p2 = pr[2];
-        }
-        Stats st{0.f, 0.f, 0.f};
-        for (int r = 0; r < cs; ++r)
-            st = combine(st, Stats{__shfl_sync(0xffffffffu, pn, r), __shfl_sync(0xffffffffu, pm, r),
-                                   __shfl_sync(0xffffffffu, p2, r)});
-        if (tid == 0) {
-            const float ctot = (float)(a.batch * HW);
-            const float var = st.m2 / ctot;
-            stat[0] = st.mean;
-            stat[1] = 1.0f / sqrtf(var + a.eps);
-            stat[2] = var;
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        for (int b = 0; b < 2; ++b) {
+            const int64_t c = first_c + b * K_clusters;
+            if (np > 0 && c < C) {
+                bn_issue_planes(a, sx4 + b * buf_f4, &bar[b], c, n0, np, q4, plane_bytes);
+                if (b == 0) last_issued0 = 0;
+                else last_issued1 = 1;
+            }
         }
     }
-    // Nobody reads a peer's partial after this point; arrive now and wait
-    // only before exiting, so the barrier overlaps the store phase.
-    cluster_arrive();
     __syncthreads();
-    const float md = stat[0], rstd = stat[1];
-    if (rank == 0 && tid == 0) {
-        const float ctot = (float)(a.batch * HW);
-        if (a.save_mean) a.save_mean[c] = K + md;
-        if (a.save_rstd) a.save_rstd[c] = rstd;
-        const float m = a.momentum;
-        if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
-        if (a.running_var) {
-            const float unbiased = stat[2] * (ctot / (float)(a.batch * HW - 1));
-            a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
-        }
-    }
 
-    // normalize from shared memory: y = ((x - K) - md) * rstd * gamma + beta
-    const float g = a.gamma ? a.gamma[c] : 1.f;
-    const float b = a.beta ? a.beta[c] : 0.f;
-    const float2 sh = f2(-K), nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(b);
-    for (int j = 0; j < np; ++j) {
-        float4 *yp = reinterpret_cast<float4 *>(a.y + ((n0 + j) * C + c) * HW);
-        for (int q = tid; q < q4; q += BNC_THREADS) {
-            const float4 v = sx4[(size_t)j * q4 + q];
-            const float2 lo = __ffma2_rn(
-                __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), sh), nmd), r2), g2, b2);
-            const float2 hi = __ffma2_rn(
-                __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), sh), nmd), r2), g2, b2);
-            __stcs(yp + q, make_float4(lo.x, lo.y, hi.x, hi.y));
+    bool gave_up = false;  // identical in every thread (read from s_ok)
+    int i = 0;
+    for (int64_t c = first_c; c < C; c += K_clusters, ++i) {
+        const int b = i & 1;
+        const float4 *buf = sx4 + b * buf_f4;
+        // second half of the previous channel's barrier: every peer has folded
+        // that channel's partials before any partial is written again
+        if (i > 0) cluster_wait();
+        // one thread waits on the copies; the CTA barrier releases the rest
+        if (tid == 0) {
+            // after a give-up nothing more is issued: do not wait again
+            const bool got = np == 0 ||
+                             (!gave_up && mbar_wait_bounded(&bar[b], (uint32_t)((i >> 1) & 1), a.wait_limit));
+            if (!got && np > 0 && !gave_up) atomicOr(a.fault, FAULT_WAIT);
+            if (got && np > 0) {
+                if (b == 0) last_done0 = i;
+                else last_done1 = i;
+            }
+            s_ok[b] = got;
+        }
+        __syncthreads();
+        gave_up = gave_up || !s_ok[b];
+        const float K = a.x[c * HW];  // x[0, c, 0]
+
+        // pass 1: sum of d = x - K over this CTA's planes
+        const float2 nk = f2(-K);
+        float2 acc = f2(0.f);
+        for (int j = 0; j < np; ++j)
+            for (int q = tid; q < q4; q += BNC_THREADS) {
+                const float4 v = buf[(size_t)j * q4 + q];
+                acc = __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk),
+                                                 __fadd2_rn(make_float2(v.z, v.w), nk)));
+            }
+        const float tot = cta_sum_all<NW>(acc.x + acc.y, s1[b]);
+        const float m0 = np ? tot / cnt : 0.f;
+        // pass 2: e = d - m0, corrected
+        const float2 nkm = f2(-m0);
+        float2 e1 = f2(0.f), e2 = f2(0.f);
+        for (int j = 0; j < np; ++j)
+            for (int q = tid; q < q4; q += BNC_THREADS) {
+                const float4 v = buf[(size_t)j * q4 + q];
+                const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), nkm);
+                const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), nkm);
+                e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
+                e2 = __ffma2_rn(ea, ea, e2);
+                e2 = __ffma2_rn(eb, eb, e2);
+            }
+        const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2[b]);
+        if (tid == 0) {
+            const float cc = np ? E.x / cnt : 0.f;
+            part[b][0] = cnt;
+            part[b][1] = m0 + cc;
+            part[b][2] = fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f);
+        }
+        cluster.sync();  // every partial of this channel is written
+
+        // fold the cs partials in rank order: lanes 0..cs-1 of warp 0 read them
+        // from the peers' shared memory in parallel, lane 0 combines
+        if (tid < 32) {
+            float pn = 0.f, pm = 0.f, p2 = 0.f;
+            if (tid < cs) {
+                const float *pr = cluster.map_shared_rank(&part[b][0], tid);
+                pn = pr[0];
+                pm = pr[1];
+                p2 = pr[2];
+            }
+            Stats st{0.f, 0.f, 0.f};
+            for (int r = 0; r < cs; ++r)
+                st = combine(st, Stats{__shfl_sync(0xffffffffu, pn, r),
+                                       __shfl_sync(0xffffffffu, pm, r),
+                                       __shfl_sync(0xffffffffu, p2, r)});
+            if (tid == 0) {
+                const float var = st.m2 / ctot;
+                stat[b][0] = st.mean;
+                stat[b][1] = 1.0f / sqrtf(var + a.eps);
+                stat[b][2] = var;
+            }
+        }
+        // nobody reads a peer's partial of this channel after this point:
+        // arrive now, wait before the next channel (or exit), so the barrier
+        // overlaps the stores of y instead of waiting for them
+        cluster_arrive();
+        __syncthreads();
+        const float md = stat[b][0], rstd = stat[b][1];
+        if (rank == 0 && tid == 0) {
+            if (a.save_mean) a.save_mean[c] = K + md;
+            if (a.save_rstd) a.save_rstd[c] = rstd;
+            const float m = a.momentum;
+            if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
+            if (a.running_var) {
+                const float unbiased = stat[b][2] * (ctot / (float)(a.batch * HW - 1));
+                a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
+            }
+        }
+
+        // normalize from shared memory: y = ((x - K) - md) * rstd * gamma + beta
+        const float g = a.gamma ? a.gamma[c] : 1.f;
+        const float bb = a.beta ? a.beta[c] : 0.f;
+        const float2 nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
+        for (int j = 0; j < np; ++j) {
+            float4 *yp = reinterpret_cast<float4 *>(a.y + ((n0 + j) * C + c) * HW);
+            for (int q = tid; q < q4; q += BNC_THREADS) {
+                const float4 v = buf[(size_t)j * q4 + q];
+                const float2 lo = __ffma2_rn(
+                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), nmd), r2), g2, b2);
+                const float2 hi = __ffma2_rn(
+                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), nmd), r2), g2, b2);
+                __stcs(yp + q, make_float4(lo.x, lo.y, hi.x, hi.y));
+            }
+        }
+        __syncthreads();  // every thread is done with this buffer
+        const int64_t next = c + 2 * K_clusters;
+        if (tid == 0 && np > 0 && next < C && !gave_up) {
+            fence_proxy_async_smem();
+            bn_issue_planes(a, sx4 + b * buf_f4, &bar[b], next, n0, np, q4, plane_bytes);
+            if (b == 0) last_issued0 = i + 2;
+            else last_issued1 = i + 2;
         }
     }
-    cluster_wait();  // peers are done reading this CTA's partial
-    if (tid == 0 && !ok && !mbar_wait_bounded(&bar, 0, 1u << 22)) atomicOr(a.fault, FAULT_DRAIN);
+    if (i > 0) cluster_wait();  // peers are done reading this CTA's last partials
+    if (tid == 0 && gave_up) {
+        // wait (bounded) for copies issued but never received
+        if (last_issued0 > last_done0 &&
+            !mbar_wait_bounded(&bar[0], (uint32_t)((last_issued0 >> 1) & 1), 1u << 22))
+            atomicOr(a.fault, FAULT_DRAIN);
+        if (last_issued1 > last_done1 &&
+            !mbar_wait_bounded(&bar[1], (uint32_t)((last_issued1 >> 1) & 1), 1u << 22))
+            atomicOr(a.fault, FAULT_DRAIN);
+    }
 }
 
 }  // namespace
 
-// Single launch when the channel's planes fit the shared memory of a cluster
-// of up to 8 CTAs and the rows are 16-byte aligned; else the two-kernel plan.
+// Plan choice (measured on GB300 at [32, 64, 56, 56]: cluster 15.9 us,
+// streaming 17.2 us, scalar 24.3 us).  One cluster of up to 8 CTAs per
+// channel when the channel's planes fit the clusters' shared memory and every
+// channel's cluster can be resident at once (one buffer); when there are
+// more channels than resident clusters, each cluster pipelines its channels
+// through two buffers.  Otherwise the streaming two kernels when the planes
+// are 16-byte aligned and fit one CTA's registers; else the scalar plan.
+namespace {
+
+cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
+    *launched = false;
+    int cs = 8;
+    while (cs > 1 && cs > a.batch) cs >>= 1;
+    const int64_t ppc = (a.batch + cs - 1) / cs;
+    const size_t buf = (size_t)ppc * (size_t)a.HW * 4;
+    if (2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
+    static std::mutex mu;
+    static int attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+            if (cudaFuncSetAttribute(bn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     200 * 1024) == cudaSuccess)
+                attr_done[dev] = 1;
+            else
+                cudaGetLastError();
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(BNC_THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(a.C * cs));
+    // one buffer if every channel gets its own resident cluster
+    cfg.dynamicSmemBytes = buf;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return cudaSuccess;
+    }
+    int64_t k = a.C;
+    if (clusters < a.C) {
+        cfg.dynamicSmemBytes = 2 * buf;
+        if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return cudaSuccess;
+        }
+        k = clusters;
+    }
+    if (k < 1) return cudaSuccess;
+    cfg.gridDim = dim3((unsigned)(k * cs));
+    *launched = true;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bn_cluster_kernel, a, (int)ppc);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
+    const int64_t planes = a.batch * a.C;
+    const int64_t cap = (int64_t)num_sms * 64;
+    const unsigned grid = (unsigned)(planes < cap ? planes : cap);
+    bn_stats_kernel<<<grid, BNS_THREADS, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(BNS_THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bn_norm_kernel, a);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+}  // namespace
+
 cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s) {
     const bool aligned = (a.HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
                          ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
-    if (aligned && a.fault && !a.two_kernel && a.C <= 0x7fffffff / 8) {
-        int cs = 8;
-        while (cs > 1 && cs > a.batch) cs >>= 1;
-        const int64_t ppc = (a.batch + cs - 1) / cs;
-        const size_t smem = (size_t)ppc * (size_t)a.HW * 4;
-        if (smem <= (size_t)100 * 1024) {
-            static std::mutex mu;
-            static int attr_done[64];
-            int dev = 0;
-            cudaGetDevice(&dev);
-            {
-                std::lock_guard<std::mutex> lock(mu);
-                if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-                    if (cudaFuncSetAttribute(bn_cluster_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             100 * 1024) == cudaSuccess)
-                        attr_done[dev] = 1;
-                    else
-                        cudaGetLastError();
-                }
-            }
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(a.C * cs));
-            cfg.blockDim = dim3(BNC_THREADS);
-            cfg.dynamicSmemBytes = smem;
-            cfg.stream = s;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = cs;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) == cudaSuccess &&
-                clusters > 0) {
-                const cudaError_t e = cudaLaunchKernelEx(&cfg, bn_cluster_kernel, a, (int)ppc);
-                if (e == cudaSuccess) return cudaGetLastError();
-                return e;
-            }
-            cudaGetLastError();
-        }
-    }
     const int64_t planes = a.batch * a.C;
+    const bool stream_ok = aligned && a.HW / 4 <= (int64_t)BNS_THREADS * BNS_PACKS;
+    if (aligned && a.fault && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_CLUSTER)) {
+        bool launched = false;
+        const cudaError_t e = launch_bn_cluster(a, s, &launched);
+        if (launched) return e;
+    }
+    if (stream_ok && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_STREAM))
+        return launch_bn_stream(a, num_sms, s);
     const int64_t cap = (int64_t)num_sms * 64;
     const unsigned grid = (unsigned)(planes < cap ? planes : cap);
     bn_partial_kernel<<<grid, BN_THREADS, 0, s>>>(a);
@@ -359,9 +599,10 @@ cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s) {
 }  // namespace nrm
 
 // ---------------------------------------------------------------------------
-// bn_fwd_train_noalloc: the same two kernels, with the per-plane partial
-// statistics kept in a fixed array of this library instead of a workspace the
-// caller allocates.  It is for callers that cannot allocate device memory
+// bn_fwd_train_noalloc: the same plans as bn_fwd_train; the plans that keep
+// per-plane partial statistics in global memory (the streaming and scalar
+// two-kernel plans) keep them in a fixed array of this library instead of a
+// workspace the caller allocates.  It is for callers that cannot allocate device memory
 // when they call -- for example a runtime that reserves its whole device
 // memory budget at start-up and forbids later allocations, or a component
 // that is handed device pointers by another part of the program and has no
@@ -444,6 +685,6 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
     BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
              static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
              running_mean, running_var, batch, C, HW, eps, momentum, g_bn_static_ptr[dev],
-             fault_word(), 1u << 20, 0};
+             fault_word(), 1u << 20, BN_PLAN_AUTO};
     return launch_bn_train_f32(a, sms, stream) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

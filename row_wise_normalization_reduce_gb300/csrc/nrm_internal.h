@@ -89,8 +89,13 @@ struct BnArgs {
     void *ws;             // two-kernel plan: batch * C float2 partials
     unsigned *fault;      // device fault word (cluster plan), or NULL
     unsigned wait_limit;  // tries per bounded wait
-    int two_kernel;       // 1: skip the cluster plan
+    int bn_plan;          // BnPlan
 };
+
+// BatchNorm plans: automatic, streaming two kernels (registers + dependent
+// launch), one cluster of CTAs per channel (shared memory + DSMEM), and the
+// scalar two-kernel plan (any layout).
+enum BnPlan { BN_PLAN_AUTO = 0, BN_PLAN_STREAM = 1, BN_PLAN_CLUSTER = 2, BN_PLAN_SCALAR = 3 };
 cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace nrm

@@ -248,10 +248,12 @@ def test_guard_bands_untouched(op):
 
 
 # ---- BatchNorm ------------------------------------------------------------
-BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_GENERIC]  # cluster per channel / two kernels
+# automatic / streaming two kernels / cluster per channel / scalar two kernels
+BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC]
+BN_IDS = ["auto", "stream", "cluster", "scalar"]
 
 
-@pytest.mark.parametrize("plan", BN_PLANS, ids=["cluster", "two_kernel"])
+@pytest.mark.parametrize("plan", BN_PLANS, ids=BN_IDS)
 @pytest.mark.parametrize("shape", [(1, 1, 7, 7), (1, 3, 5, 5), (2, 4, 3, 3), (8, 16, 28, 28),
                                    (4, 8, 1, 1), (3, 5, 13, 11), (64, 3, 8, 8), (5, 7, 20, 20),
                                    (13, 2, 12, 12), (32, 4, 56, 56)])
@@ -263,7 +265,7 @@ def test_bn_shapes(orc, shape, plan):
     RN.compare("bn", inp, gpu, ref)
 
 
-@pytest.mark.parametrize("plan", BN_PLANS, ids=["cluster", "two_kernel"])
+@pytest.mark.parametrize("plan", BN_PLANS, ids=BN_IDS)
 def test_bn_large_mean_channel(orc, plan):
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(4, 3, 16, 16))
     inp["x"][:, 1] += 1000.0
@@ -276,12 +278,15 @@ def test_bn_large_mean_channel(orc, plan):
 def test_bn_plans_agree_and_repeat():
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 8, 28, 28))
     outs = []
-    for plan in (nrm.PLAN_AUTO, nrm.PLAN_AUTO, nrm.PLAN_GENERIC):
+    plans = (nrm.PLAN_CTA, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_TMA, nrm.PLAN_GENERIC)
+    for plan in plans:
         nrm.force_plan(plan)
         outs.append(RN.run_gpu("bn", inp, 1e-5, 0.1))
     for k in outs[0]:
         assert (outs[0][k] == outs[1][k]).all(), k  # bitwise repeatable
-        assert np.max(np.abs(outs[0][k].astype(np.float64) - outs[2][k])) <= 2e-5, k
+        assert (outs[2][k] == outs[3][k]).all(), k
+        for o in (outs[2], outs[4]):
+            assert np.max(np.abs(outs[0][k].astype(np.float64) - o[k])) <= 2e-5, k
 
 
 def test_bn_without_optionals(orc):
@@ -293,3 +298,23 @@ def test_bn_without_optionals(orc):
     ref = orc.batchnorm_train(0, n["x"], eps=1e-5, wide=True)
     gy = y.cpu().numpy().reshape(ref["y_wide"].shape)
     assert np.max(np.abs(gy - ref["y_wide"])) <= 2e-5
+
+
+def test_bn_cluster_wait_give_up_path(orc):
+    # wait limit 0: every bulk-copy wait of the cluster plan gives up at once;
+    # the kernel must raise the fault bit, keep every CTA in its cluster
+    # barriers, drain its copies and return; the next call must be correct.
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 12, 28, 28))
+    nrm.force_plan(nrm.PLAN_TMA)
+    x = inp["x"].cuda()
+    assert nrm.device_fault(clear=True) == 0
+    old = nrm.set_wait_limit(0)
+    try:
+        nrm.bn_fwd_train(x, None, None, None, None, 1e-5, 0.1)
+        bits = nrm.device_fault(clear=True)
+    finally:
+        nrm.set_wait_limit(old)
+    assert bits == 1, bits
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
+    assert nrm.device_fault(clear=True) == 0
