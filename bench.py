@@ -368,6 +368,23 @@ def oracle_time(w: W.Workload, rows_sample: int, reps: int, threads: int):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (one process per GPU; replicas, weak scaling)
+# ---------------------------------------------------------------------------
+def max_over_ranks(seconds: float, dist=None, device="cpu") -> float:
+    """The slowest rank's timed region (every rank gets the same value)."""
+    if dist is None:
+        return seconds
+    t = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, steps: int, bytes_per_step: int, seconds: float) -> float:
+    """Whole-job throughput: the bytes every rank moved over the slowest rank's time."""
+    return world * steps * bytes_per_step / seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
 def emit(line: dict):
     print(json.dumps(line), flush=True)
 
@@ -472,13 +489,10 @@ def main():
     sampler.start()
     sec, t0, t1 = time_graphs(step, args.steps, args.warmup, stream, dist=dist)
     sampler.stop()
-    if dist is not None:
-        t = torch.tensor([sec], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = max_over_ranks(sec, dist, device)
     per_step = sec / args.steps
     nbytes = algorithmic_bytes(w)
-    value = world * args.steps * nbytes / sec / 1e9
+    value = job_gbs(world, args.steps, nbytes, sec)
     peak, peak_src = measured_peak()
     kernel_gbs = nbytes / (per_step / step.launches_per_step) / 1e9 if step.launches_per_step == 1 \
         else nbytes / per_step / 1e9

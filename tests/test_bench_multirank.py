@@ -1,0 +1,52 @@
+"""bench.py's multi-process logic on CPU ranks (gloo, world size 2): the timed
+region is the slowest rank's, the value counts every rank's bytes, and the
+reference arm prints from rank 0 only."""
+import os
+import subprocess
+import sys
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        sec = [0.010, 0.025][rank]
+        m = bench.max_over_ranks(sec, dist, "cpu")
+        out[rank] = (m, bench.job_gbs(world, 100, 1_000_000, m))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_gloo():
+    port = 29500 + (os.getpid() % 1000)
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 0.025
+    assert abs(res[0][1] - 2 * 100 * 1_000_000 / 0.025 / 1e9) < 1e-9
+
+
+def test_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(0.5) == 0.5
+    assert bench.job_gbs(1, 10, 2_000_000_000, 2.0) == 10.0
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
