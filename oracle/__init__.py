@@ -57,7 +57,13 @@ def _declare(lib):
                                     ctypes.c_float]
     lib.orc_batchnorm_train.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _I64, _I64, _I64, ctypes.c_float, ctypes.c_float]
-    for name in ("orc_layernorm", "orc_rmsnorm", "orc_add_rmsnorm", "orc_batchnorm_train"):
+    lib.orc_batchnorm_infer.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                                        _I64, ctypes.c_float]
+    lib.orc_batchnorm_backward.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           _I64, _I64, _I64]
+    lib.orc_softmax.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _I64, _I64]
+    for name in ("orc_layernorm", "orc_rmsnorm", "orc_add_rmsnorm", "orc_batchnorm_train",
+                 "orc_batchnorm_infer", "orc_batchnorm_backward", "orc_softmax"):
         getattr(lib, name).restype = ctypes.c_int
     lib.orc_f16_bits_to_double.argtypes = [ctypes.c_uint16]
     lib.orc_f16_bits_to_double.restype = ctypes.c_double
@@ -169,6 +175,56 @@ class Oracle:
         _rc(rc)
         return {"y": y, "y_wide": yw, "save_mean": smean, "save_rstd": srstd,
                 "running_mean": rm, "running_var": rv}
+
+    def batchnorm_infer(self, dt, x, running_mean, running_var, gamma=None, beta=None,
+                        eps=1e-5, wide=False):
+        """x is [batch, C, HW...]; running statistics are binary32 [C]."""
+        x = np.ascontiguousarray(x)
+        batch, c = x.shape[0], x.shape[1]
+        hw = int(np.prod(x.shape[2:])) if x.ndim > 2 else 1
+        x = _check(dt, x.reshape(batch, c, hw))
+        rm = np.ascontiguousarray(running_mean, np.float32)
+        rv = np.ascontiguousarray(running_var, np.float32)
+        assert rm.shape == (c,) and rv.shape == (c,)
+        y = np.empty_like(x)
+        yw = np.empty(x.shape, np.float64) if wide else None
+        rc = self._l.orc_batchnorm_infer(dt, _ptr(x), _ptr(_check(dt, gamma, c)),
+                                         _ptr(_check(dt, beta, c)), _ptr(y), _ptr(yw),
+                                         _ptr(rm), _ptr(rv), batch, c, hw, eps)
+        _rc(rc)
+        return {"y": y, "y_wide": yw}
+
+    def batchnorm_backward(self, dt, dy, x, mean, rstd, gamma=None, wide=False):
+        """dy, x are [batch, C, HW...]; mean/rstd are the saved per-channel
+        statistics (any float array of shape [C], widened to double)."""
+        x = np.ascontiguousarray(x)
+        batch, c = x.shape[0], x.shape[1]
+        hw = int(np.prod(x.shape[2:])) if x.ndim > 2 else 1
+        x = _check(dt, x.reshape(batch, c, hw))
+        dy = _check(dt, np.ascontiguousarray(dy).reshape(batch, c, hw))
+        mean = np.ascontiguousarray(mean, np.float64)
+        rstd = np.ascontiguousarray(rstd, np.float64)
+        assert mean.shape == (c,) and rstd.shape == (c,)
+        dx = np.empty_like(x)
+        dxw = np.empty(x.shape, np.float64) if wide else None
+        dg = np.empty(c, np.float64)
+        db = np.empty(c, np.float64)
+        rc = self._l.orc_batchnorm_backward(dt, _ptr(dy), _ptr(x), _ptr(_check(dt, gamma, c)),
+                                            _ptr(mean), _ptr(rstd), _ptr(dx), _ptr(dxw),
+                                            _ptr(dg), _ptr(db), batch, c, hw)
+        _rc(rc)
+        return {"dx": dx, "dx_wide": dxw, "dgamma": dg, "dbeta": db}
+
+    def softmax(self, dt, x, wide=False):
+        x = _check(dt, x)
+        rows, n = x.shape
+        y = np.empty_like(x)
+        yw = np.empty(x.shape, np.float64) if wide else None
+        m = np.empty(rows, np.float64)
+        d = np.empty(rows, np.float64)
+        rc = self._l.orc_softmax(dt, _ptr(x), _ptr(y), _ptr(yw), _ptr(m), _ptr(d), rows, n)
+        _rc(rc)
+        return {"y": y, "y_wide": yw, "row_max": m, "row_sum": d}
 
 
 def _check(dt, a, n=None):

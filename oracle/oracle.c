@@ -1,7 +1,8 @@
 /*
  * oracle.c -- plain, slow, obviously correct CPU reference for the row-wise
  * reduce-then-normalize path (LayerNorm, RMSNorm, residual-add + RMSNorm,
- * BatchNorm2d training forward).
+ * BatchNorm2d training forward, inference forward and training backward,
+ * row softmax).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this file.  Only the test suite, the smoke check and the CPU-baseline
@@ -363,6 +364,129 @@ int orc_batchnorm_train(int dt, const void *x, const void *gamma, const void *be
         if (running_var)
             running_var[c] = (1.0 - m) * running_var[c]
                              + m * var * (double)cnt / (double)(cnt - 1);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* BatchNorm2d inference forward (BatchNorm CUDA implementation walkthrough, */
+/* jianying88.com/news/30214, section 2.4: inference normalizes with the     */
+/* running statistics kept during training instead of the batch's):        */
+/*   y = (x - running_mean_c) / sqrt(running_var_c + eps) * gamma_c + beta_c */
+/* NCHW: x[n][c][k] at (n*C + c)*HW + k.  running_* are binary32 inputs.    */
+/* ------------------------------------------------------------------------ */
+int orc_batchnorm_infer(int dt, const void *x, const void *gamma, const void *beta,
+                        void *y, double *y_wide, const float *running_mean,
+                        const float *running_var, int64_t batch, int64_t C, int64_t HW,
+                        float eps)
+{
+    if (!orc_dtype_ok(dt) || !x || !running_mean || !running_var || batch < 0 || C < 1
+        || HW < 1)
+        return ORC_BAD_ARGS;
+    for (int64_t c = 0; c < C; ++c) {
+        const double mean = (double)running_mean[c];
+        const double rstd = 1.0 / sqrt((double)running_var[c] + (double)eps);
+        const double g = gamma ? orc_get(dt, gamma, c) : 1.0;
+        const double b = beta ? orc_get(dt, beta, c) : 0.0;
+        for (int64_t n = 0; n < batch; ++n)
+            for (int64_t k = 0; k < HW; ++k) {
+                const int64_t i = (n * C + c) * HW + k;
+                const double out = (orc_get(dt, x, i) - mean) * rstd * g + b;
+                if (y)
+                    orc_put(dt, y, i, out);
+                if (y_wide)
+                    y_wide[i] = out;
+            }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* BatchNorm2d training backward (BatchNorm CUDA implementation walkthrough, */
+/* section 3.1).  With xhat = (x - mean_c) * rstd_c over the channel's       */
+/* count = batch*HW elements:                                               */
+/*   dbeta_c  = sum dy                                                       */
+/*   dgamma_c = sum dy * xhat                                                */
+/*   dx       = gamma_c * rstd_c * (dy - dbeta_c/count - xhat * dgamma_c/count) */
+/* mean_c and rstd_c are the statistics the training forward saved; they    */
+/* are inputs here (xhat is recomputed from x, not stored).  The section's  */
+/* first statement of dx leaves out the factor gamma_c; its restatement in  */
+/* terms of the two sums has it, and only that form is the derivative of    */
+/* y = xhat * gamma + beta, so that form is the one followed.               */
+/* dgamma/dbeta may be NULL (not written); gamma NULL means 1.              */
+/* ------------------------------------------------------------------------ */
+int orc_batchnorm_backward(int dt, const void *dy, const void *x, const void *gamma,
+                           const double *mean, const double *rstd, void *dx,
+                           double *dx_wide, double *dgamma, double *dbeta,
+                           int64_t batch, int64_t C, int64_t HW)
+{
+    if (!orc_dtype_ok(dt) || !dy || !x || !mean || !rstd || batch < 1 || C < 1 || HW < 1)
+        return ORC_BAD_ARGS;
+    const double cnt = (double)(batch * HW);
+    for (int64_t c = 0; c < C; ++c) {
+        orc_sum s1 = {0.0, 0.0}, s2 = {0.0, 0.0};
+        for (int64_t n = 0; n < batch; ++n)
+            for (int64_t k = 0; k < HW; ++k) {
+                const int64_t i = (n * C + c) * HW + k;
+                const double g_out = orc_get(dt, dy, i);
+                const double xhat = (orc_get(dt, x, i) - mean[c]) * rstd[c];
+                orc_sum_add(&s1, g_out);
+                orc_sum_add(&s2, g_out * xhat);
+            }
+        const double db = orc_sum_get(&s1), dg = orc_sum_get(&s2);
+        const double g = gamma ? orc_get(dt, gamma, c) : 1.0;
+        for (int64_t n = 0; n < batch; ++n)
+            for (int64_t k = 0; k < HW; ++k) {
+                const int64_t i = (n * C + c) * HW + k;
+                const double xhat = (orc_get(dt, x, i) - mean[c]) * rstd[c];
+                const double out =
+                    g * rstd[c] * (orc_get(dt, dy, i) - db / cnt - xhat * dg / cnt);
+                if (dx)
+                    orc_put(dt, dx, i, out);
+                if (dx_wide)
+                    dx_wide[i] = out;
+            }
+        if (dgamma)
+            dgamma[c] = dg;
+        if (dbeta)
+            dbeta[c] = db;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row softmax (LLM-ops page, smarter.xin, section 1, "Softmax"):           */
+/*   m = max_j x_j,  d = sum_j exp(x_j - m),  y_i = exp(x_i - m) / d        */
+/* The online single-pass form on that page reaches the same m and d; this  */
+/* is the plain definition.  row_max/row_sum (m and d) may be NULL.         */
+/* ------------------------------------------------------------------------ */
+int orc_softmax(int dt, const void *x, void *y, double *y_wide, double *row_max,
+                double *row_sum, int64_t rows, int64_t N)
+{
+    if (!orc_dtype_ok(dt) || !x || rows < 0 || N < 1)
+        return ORC_BAD_ARGS;
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = orc_get(dt, x, r * N + j);
+            if (v > m)
+                m = v;
+        }
+        orc_sum s = {0.0, 0.0};
+        for (int64_t j = 0; j < N; ++j)
+            orc_sum_add(&s, exp(orc_get(dt, x, r * N + j) - m));
+        const double d = orc_sum_get(&s);
+        for (int64_t j = 0; j < N; ++j) {
+            const double out = exp(orc_get(dt, x, r * N + j) - m) / d;
+            if (y)
+                orc_put(dt, y, r * N + j, out);
+            if (y_wide)
+                y_wide[r * N + j] = out;
+        }
+        if (row_max)
+            row_max[r] = m;
+        if (row_sum)
+            row_sum[r] = d;
     }
     return ORC_OK;
 }

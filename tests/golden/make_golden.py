@@ -79,6 +79,33 @@ def cases():
                 "save_rstd": r["save_rstd"].tolist(),
                 "running_mean": r["running_mean"].tolist(),
                 "running_var": r["running_var"].tolist()})
+    for dt in (0, 2):
+        x = storage(dt, pattern(batch * c, hw, 5, 17, 3, 4.0).reshape(batch, c, hw))
+        g = storage(dt, [1.0, 0.75, 1.5])
+        b = storage(dt, [0.5, 0.0, -0.25])
+        rm = np.array([0.25, -1.0, 2.0], np.float32)
+        rv = np.array([1.5, 0.5, 4.0], np.float32)
+        r = orc.batchnorm_infer(dt, x, rm, rv, g, b, eps=np.float32(1e-5))
+        out.append({"op": "bn_infer", "dtype": dt, "batch": batch, "c": c, "hw": hw,
+                    "eps": 1e-5, "x": hexs(x), "gamma": hexs(g), "beta": hexs(b),
+                    "running_mean": rm.tolist(), "running_var": rv.tolist(), "y": hexs(r["y"])})
+    for dt in (0, 1):
+        x = storage(dt, pattern(batch * c, hw, 7, 13, 2, 2.0).reshape(batch, c, hw) + 1.0)
+        dy = storage(dt, pattern(batch * c, hw, 11, 19, 4, 8.0).reshape(batch, c, hw))
+        g = storage(dt, [1.0, 0.5, 1.25])
+        mean = [1.0, 0.75, 1.25]
+        rstd = [0.5, 0.625, 0.375]
+        r = orc.batchnorm_backward(dt, dy, x, mean, rstd, g)
+        out.append({"op": "bn_bwd", "dtype": dt, "batch": batch, "c": c, "hw": hw,
+                    "x": hexs(x), "dy": hexs(dy), "gamma": hexs(g), "mean": mean,
+                    "rstd": rstd, "dx": hexs(r["dx"]), "dgamma": r["dgamma"].tolist(),
+                    "dbeta": r["dbeta"].tolist()})
+    for dt, rows, n in ((0, 3, 19), (2, 2, 24), (1, 2, 9)):
+        x = storage(dt, pattern(rows, n, 23, 41, 6, 4.0))
+        r = orc.softmax(dt, x)
+        out.append({"op": "softmax", "dtype": dt, "rows": rows, "n": n, "x": hexs(x),
+                    "y": hexs(r["y"]), "row_max": r["row_max"].tolist(),
+                    "row_sum": r["row_sum"].tolist()})
     return out
 
 

@@ -425,4 +425,261 @@ def pin_bn_single_plane_is_ln(orc):
     assert np.max(np.abs(bn["y_wide"].ravel() - ln["y_wide"].ravel())) <= 1e-13
 
 
+# --------------------------------------------------------------------------
+# BatchNorm inference forward (running statistics)
+# --------------------------------------------------------------------------
+def pin_bn_infer_exact_tiny(orc):
+    rng = np.random.default_rng(51)
+    batch, C, HW = 2, 3, 5
+    x = rng.integers(-40, 41, size=(batch, C, HW)) / 8.0
+    g = 1.0 + rng.integers(-8, 9, C) / 8.0
+    b = rng.integers(-8, 9, C) / 16.0
+    rm = rng.integers(-16, 17, C) / 8.0
+    rv = 0.25 + rng.integers(0, 32, C) / 8.0
+    eps = np.float32(1e-5)
+    for dt in (F32, F16, BF16):
+        r = orc.batchnorm_infer(dt, _enc(dt, x), rm.astype(np.float32), rv.astype(np.float32),
+                                _enc(dt, g), _enc(dt, b), eps=eps, wide=True)
+        for c in range(C):
+            den = (_dec(rv[c]) + _dec(eps)).sqrt()
+            for n in range(batch):
+                for k in range(HW):
+                    want = (_dec(x[n, c, k]) - _dec(rm[c])) / den * _dec(g[c]) + _dec(b[c])
+                    _close(r["y_wide"][n, c, k], want, 1e-14, 1e-14)
+
+
+def pin_bn_infer_identity_statistics(orc):
+    # running mean 0, running variance 1, eps 0: y = x * gamma + beta exactly
+    rng = np.random.default_rng(52)
+    batch, C, HW = 3, 4, 6
+    x = rng.integers(-64, 65, size=(batch, C, HW)) / 16.0
+    g = 1.0 + rng.integers(-8, 9, C) / 8.0
+    b = rng.integers(-8, 9, C) / 8.0
+    r = orc.batchnorm_infer(F32, _enc(F32, x), np.zeros(C, np.float32), np.ones(C, np.float32),
+                            _enc(F32, g), _enc(F32, b), eps=np.float32(0.0), wide=True)
+    assert np.array_equal(r["y_wide"], x * g[None, :, None] + b[None, :, None])
+
+
+def pin_bn_infer_with_batch_statistics_is_train(orc):
+    # channels that are arithmetic sequences have a mean and biased variance
+    # exact in binary32; feeding them as running statistics reproduces the
+    # training forward's normalization
+    batch, HW = 2, 8
+    cnt = batch * HW
+    a = np.array([0.5, -3.0, 10.0])
+    d = np.array([0.25, 1.0, 0.5])
+    C = a.size
+    x = np.empty((batch, C, HW))
+    for c in range(C):
+        x[:, c, :] = (a[c] + d[c] * np.arange(cnt)).reshape(batch, HW)
+    mean = a + d * (cnt - 1) / 2.0
+    var = d * d * (cnt * cnt - 1) / 12.0
+    assert np.array_equal(mean.astype(np.float32), mean)
+    assert np.array_equal(var.astype(np.float32), var)
+    eps = np.float32(1e-3)
+    inf = orc.batchnorm_infer(F32, _enc(F32, x), mean.astype(np.float32), var.astype(np.float32),
+                              eps=eps, wide=True)
+    tr = orc.batchnorm_train(F32, _enc(F32, x), eps=eps, wide=True)
+    assert np.max(np.abs(inf["y_wide"] - tr["y_wide"])) <= 1e-13
+
+
+# --------------------------------------------------------------------------
+# BatchNorm training backward
+# --------------------------------------------------------------------------
+def _bn_loss(orc, x, g, b, dy, eps):
+    """L = sum(dy * y) with y the training forward of x (double outputs)."""
+    r = orc.batchnorm_train(F32, x, g, b, eps=eps, wide=True)
+    return float(np.sum(dy * r["y_wide"]))
+
+
+def pin_bn_bwd_matches_finite_differences(orc):
+    # Gradient check (the BatchNorm page's section 6.3 recommends one): the
+    # backward of L = sum(dy * y) against central differences of the training
+    # forward, which recomputes the batch statistics at every perturbed x.
+    # x, gamma and the steps are multiples of 2^-12, so x +- h is exact.
+    rng = np.random.default_rng(61)
+    batch, C, HW = 2, 2, 3
+    x = (rng.integers(-256, 257, size=(batch, C, HW)) / 64.0).astype(np.float32)
+    g = (1.0 + rng.integers(-8, 9, C) / 8.0).astype(np.float32)
+    b = (rng.integers(-8, 9, C) / 16.0).astype(np.float32)
+    dy = rng.standard_normal((batch, C, HW))
+    eps = np.float32(1e-2)
+    fw = orc.batchnorm_train(F32, x, g, b, eps=eps)
+    bw = orc.batchnorm_backward(F32, _enc(F32, np.zeros((batch, C, HW))), x,
+                                fw["save_mean"], fw["save_rstd"], g, wide=True)
+    h = 2.0 ** -12
+    # dy enters the backward as data: use the real dy in double via linearity
+    # (the backward is linear in dy: run it once per unit vector of dy)
+    grad = np.zeros((batch, C, HW))
+    for idx in np.ndindex(batch, C, HW):
+        unit = np.zeros((batch, C, HW), np.float32)
+        unit[idx] = 1.0
+        grad += dy[idx] * orc.batchnorm_backward(F32, unit, x, fw["save_mean"], fw["save_rstd"],
+                                                 g, wide=True)["dx_wide"]
+    for idx in np.ndindex(batch, C, HW):
+        xp = x.copy(); xp[idx] += np.float32(h)
+        xm = x.copy(); xm[idx] -= np.float32(h)
+        num = (_bn_loss(orc, xp, g, b, dy, eps) - _bn_loss(orc, xm, g, b, dy, eps)) / (2 * h)
+        _close(grad[idx], num, 1e-5, 1e-7)
+    # dgamma, dbeta: central differences in gamma and beta
+    dyf = dy.astype(np.float32)
+    full = orc.batchnorm_backward(F32, dyf, x, fw["save_mean"], fw["save_rstd"], g)
+    for c in range(C):
+        for which, key in ((0, "dgamma"), (1, "dbeta")):
+            gp, gm, bp, bm = g.copy(), g.copy(), b.copy(), b.copy()
+            if which == 0:
+                gp[c] += np.float32(h); gm[c] -= np.float32(h)
+            else:
+                bp[c] += np.float32(h); bm[c] -= np.float32(h)
+            num = (_bn_loss(orc, x, gp, bp, dyf.astype(np.float64), eps)
+                   - _bn_loss(orc, x, gm, bm, dyf.astype(np.float64), eps)) / (2 * h)
+            _close(full[key][c], num, 1e-6, 1e-7)
+    assert np.all(bw["dx_wide"] == 0.0)
+
+
+def pin_bn_bwd_exact_tiny(orc):
+    # sums and dx in 60-digit decimals from the formulas of the BatchNorm
+    # page's section 3.1, on binary-fraction data
+    rng = np.random.default_rng(62)
+    batch, C, HW = 2, 2, 4
+    x = rng.integers(-40, 41, size=(batch, C, HW)) / 8.0
+    dy = rng.integers(-16, 17, size=(batch, C, HW)) / 8.0
+    g = 1.0 + rng.integers(-8, 9, C) / 8.0
+    mean = rng.integers(-8, 9, C) / 4.0
+    rstd = 0.5 + rng.integers(0, 8, C) / 4.0
+    r = orc.batchnorm_backward(F32, _enc(F32, dy), _enc(F32, x), mean, rstd, _enc(F32, g),
+                               wide=True)
+    cnt = batch * HW
+    for c in range(C):
+        xh = [(_dec(x[n, c, k]) - _dec(mean[c])) * _dec(rstd[c])
+              for n in range(batch) for k in range(HW)]
+        dd = [_dec(dy[n, c, k]) for n in range(batch) for k in range(HW)]
+        s1 = sum(dd)
+        s2 = sum(a * b for a, b in zip(dd, xh))
+        _close(r["dbeta"][c], s1, 1e-15, 1e-15)
+        _close(r["dgamma"][c], s2, 1e-15, 1e-15)
+        j = 0
+        for n in range(batch):
+            for k in range(HW):
+                want = _dec(g[c]) * _dec(rstd[c]) * (dd[j] - s1 / cnt - xh[j] * s2 / cnt)
+                _close(r["dx_wide"][n, c, k], want, 1e-14, 1e-14)
+                j += 1
+
+
+def pin_bn_bwd_invariants(orc):
+    # with the batch's own statistics: sum over a channel of dx is 0, a
+    # constant dy gives dx = 0 and dbeta = k * count, and with eps = 0
+    # dx is orthogonal to xhat as well
+    rng = np.random.default_rng(63)
+    batch, C, HW = 3, 4, 10
+    x = (rng.standard_normal((batch, C, HW)) * 2 + 1).astype(np.float32)
+    g = (1.0 + 0.1 * rng.standard_normal(C)).astype(np.float32)
+    dy = rng.standard_normal((batch, C, HW)).astype(np.float32)
+    eps = np.float32(0.0)
+    fw = orc.batchnorm_train(F32, x, eps=eps)
+    r = orc.batchnorm_backward(F32, dy, x, fw["save_mean"], fw["save_rstd"], g, wide=True)
+    xh = (x.astype(np.float64) - fw["save_mean"][None, :, None]) * fw["save_rstd"][None, :, None]
+    scale = np.abs(r["dx_wide"]).sum(axis=(0, 2))
+    assert np.all(np.abs(r["dx_wide"].sum(axis=(0, 2))) <= 1e-13 * scale)
+    assert np.all(np.abs((r["dx_wide"] * xh).sum(axis=(0, 2))) <= 1e-13 * scale * 4)
+    k = np.float32(0.75)
+    rc = orc.batchnorm_backward(F32, np.full_like(dy, k), x, fw["save_mean"], fw["save_rstd"],
+                                g, wide=True)
+    assert np.max(np.abs(rc["dx_wide"])) <= 1e-14
+    assert np.allclose(rc["dbeta"], float(k) * batch * HW, rtol=1e-15, atol=0)
+    assert np.max(np.abs(rc["dgamma"])) <= 1e-12
+
+
+# --------------------------------------------------------------------------
+# Row softmax
+# --------------------------------------------------------------------------
+def pin_softmax_constant_rows(orc):
+    for dt in (F32, F16, BF16):
+        for n in (1, 7, 64, 1000):
+            for c in (0.0, -3.5, 1000.0):
+                r = orc.softmax(dt, _enc(dt, np.full((2, n), c)), wide=True)
+                assert np.all(r["y_wide"] == 1.0 / n)
+                assert np.all(r["row_max"] == c) and np.all(r["row_sum"] == n)
+
+
+def pin_softmax_exact_tiny(orc):
+    # 60-digit evaluation of exp(x_i - max) / sum_j exp(x_j - max)
+    rng = np.random.default_rng(71)
+    x = rng.integers(-64, 65, size=(3, 9)) / 8.0
+    r = orc.softmax(F32, _enc(F32, x), wide=True)
+    for i in range(x.shape[0]):
+        m = max(_dec(v) for v in x[i])
+        e = [(_dec(v) - m).exp() for v in x[i]]
+        d = sum(e)
+        _close(r["row_max"][i], m, 0.0, 0.0)
+        _close(r["row_sum"][i], d, 1e-15)
+        for j in range(x.shape[1]):
+            _close(r["y_wide"][i, j], e[j] / d, 1e-14, 1e-300)
+
+
+def pin_softmax_two_values_logistic(orc):
+    # a row (a, b) gives y_0 = 1 / (1 + exp(b - a))
+    for a, b in ((0.0, 1.0), (2.5, -1.5), (30.0, 30.5), (-7.0, 9.0)):
+        r = orc.softmax(F32, _enc(F32, np.array([[a, b]])), wide=True)
+        want = Decimal(1) / (Decimal(1) + (_dec(b) - _dec(a)).exp())
+        _close(r["y_wide"][0, 0], want, 1e-15)
+        _close(r["y_wide"][0, 1], Decimal(1) - want, 1e-14)
+
+
+def pin_softmax_shift_and_overflow(orc):
+    # softmax(x + c) = softmax(x); large inputs stay finite (the max is
+    # subtracted before exp); outputs sum to 1
+    rng = np.random.default_rng(72)
+    base = rng.integers(-512, 513, size=(4, 200)) / 32.0
+    ref = orc.softmax(F32, _enc(F32, base), wide=True)["y_wide"]
+    for c in (1000.0, -600.0, 5000.0):
+        got = orc.softmax(F32, _enc(F32, base + c), wide=True)["y_wide"]
+        assert np.all(np.isfinite(got))
+        assert np.max(np.abs(got - ref)) <= 1e-15
+    assert np.max(np.abs(ref.sum(axis=1) - 1.0)) <= 1e-14
+
+
+def pin_softmax_online_recurrence_matches(orc):
+    # The single-pass update of the LLM-ops page (section 1, "online softmax"):
+    # m_new = max(m_old, x_k), d_new = d_old * exp(m_old - m_new) + exp(x_k - m_new),
+    # run in Python doubles, reaches the oracle's max and denominator; and the
+    # page's pairwise merge of two (max, sum) halves reaches the same pair.
+    rng = np.random.default_rng(73)
+    x = (rng.standard_normal((5, 333)) * 4).astype(np.float32)
+    r = orc.softmax(F32, x)
+    for i in range(x.shape[0]):
+        m, d = float("-inf"), 0.0
+        for v in x[i].astype(np.float64):
+            mn = max(m, v)
+            d = d * np.exp(m - mn) + np.exp(v - mn)
+            m = mn
+        _close(r["row_max"][i], m, 0.0, 0.0)
+        _close(r["row_sum"][i], d, 1e-13)
+        h = x.shape[1] // 2
+        lo, hi = x[i, :h].astype(np.float64), x[i, h:].astype(np.float64)
+        ma, mb = lo.max(), hi.max()
+        da, db = np.exp(lo - ma).sum(), np.exp(hi - mb).sum()
+        mm = max(ma, mb)
+        _close(r["row_sum"][i], da * np.exp(ma - mm) + db * np.exp(mb - mm), 1e-13)
+
+
+def pin_softmax_ratios_and_rounding(orc):
+    # y_i / y_j = exp(x_i - x_j); 16-bit outputs are the nearest value of y
+    rng = np.random.default_rng(74)
+    x = rng.integers(-96, 97, size=(3, 50)) / 16.0
+    r = orc.softmax(F32, _enc(F32, x), wide=True)
+    y = r["y_wide"]
+    for i in range(3):
+        j, k = int(np.argmax(x[i])), int(np.argmin(x[i]))
+        _close(y[i, k] / y[i, j], np.exp(x[i, k] - x[i, j]), 1e-13)
+    for dt in (F16, BF16):
+        rr = orc.softmax(dt, _enc(dt, x), wide=True)
+        if dt == F16:
+            ref = B.f64_to_bits_numpy_f16(rr["y_wide"])
+        else:
+            ref = np.array([_bf16_rn_exact(v) for v in rr["y_wide"].ravel()],
+                           np.uint16).reshape(rr["y_wide"].shape)
+        assert np.array_equal(rr["y"], ref)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -30,6 +30,30 @@ def test_golden_regression(orc):
             for k in ("save_mean", "save_rstd", "running_mean", "running_var"):
                 assert np.array_equal(r[k], np.array(c[k]))
             continue
+        if c["op"] == "bn_infer":
+            shape = (c["batch"], c["c"], c["hw"])
+            r = orc.batchnorm_infer(dt, _arr(dt, c["x"], shape), np.array(c["running_mean"]),
+                                    np.array(c["running_var"]),
+                                    _arr(dt, c["gamma"], (c["c"],)),
+                                    _arr(dt, c["beta"], (c["c"],)), eps=np.float32(c["eps"]))
+            assert np.array_equal(r["y"], _arr(dt, c["y"], shape))
+            continue
+        if c["op"] == "bn_bwd":
+            shape = (c["batch"], c["c"], c["hw"])
+            r = orc.batchnorm_backward(dt, _arr(dt, c["dy"], shape), _arr(dt, c["x"], shape),
+                                       np.array(c["mean"]), np.array(c["rstd"]),
+                                       _arr(dt, c["gamma"], (c["c"],)))
+            assert np.array_equal(r["dx"], _arr(dt, c["dx"], shape))
+            assert np.array_equal(r["dgamma"], np.array(c["dgamma"]))
+            assert np.array_equal(r["dbeta"], np.array(c["dbeta"]))
+            continue
+        if c["op"] == "softmax":
+            shape = (c["rows"], c["n"])
+            r = orc.softmax(dt, _arr(dt, c["x"], shape))
+            assert np.array_equal(r["y"], _arr(dt, c["y"], shape))
+            assert np.array_equal(r["row_max"], np.array(c["row_max"]))
+            assert np.array_equal(r["row_sum"], np.array(c["row_sum"]))
+            continue
         shape = (c["rows"], c["n"])
         x = _arr(dt, c["x"], shape)
         if c["op"] == "ln":

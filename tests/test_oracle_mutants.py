@@ -51,6 +51,30 @@ MUTANTS = [
     ("bn_momentum_swapped",
      "running_mean[c] = (1.0 - m) * running_mean[c] + m * mean;",
      "running_mean[c] = m * running_mean[c] + (1.0 - m) * mean;", 0),
+    ("bn_infer_eps_dropped",
+     "const double rstd = 1.0 / sqrt((double)running_var[c] + (double)eps);",
+     "const double rstd = 1.0 / sqrt((double)running_var[c]);", 0),
+    ("bn_infer_drop_beta", "const double out = (orc_get(dt, x, i) - mean) * rstd * g + b;",
+     "const double out = (orc_get(dt, x, i) - mean) * rstd * g;", 1),
+    ("bn_infer_channel_index", "const double mean = (double)running_mean[c];",
+     "const double mean = (double)running_mean[0];", 0),
+    ("bn_bwd_drop_gamma",
+     "g * rstd[c] * (orc_get(dt, dy, i) - db / cnt - xhat * dg / cnt);",
+     "rstd[c] * (orc_get(dt, dy, i) - db / cnt - xhat * dg / cnt);", 0),
+    ("bn_bwd_xhat_term_sign", "- xhat * dg / cnt);", "+ xhat * dg / cnt);", 0),
+    ("bn_bwd_dbeta_not_averaged", "(orc_get(dt, dy, i) - db / cnt", "(orc_get(dt, dy, i) - db", 0),
+    ("bn_bwd_dgamma_uses_x", "orc_sum_add(&s2, g_out * xhat);",
+     "orc_sum_add(&s2, g_out * orc_get(dt, x, i));", 0),
+    ("bn_bwd_xhat_unscaled", "const double xhat = (orc_get(dt, x, i) - mean[c]) * rstd[c];",
+     "const double xhat = (orc_get(dt, x, i) - mean[c]);", 0),
+    ("bn_bwd_biased_count", "const double cnt = (double)(batch * HW);",
+     "const double cnt = (double)(batch * HW - 1);", 0),
+    ("softmax_no_max", "double m = -INFINITY;", "double m = 0.0; if (0)", 0),
+    ("softmax_sum_skips_last", "orc_sum_add(&s, exp(orc_get(dt, x, r * N + j) - m));",
+     "if (j + 1 < N) orc_sum_add(&s, exp(orc_get(dt, x, r * N + j) - m));", 0),
+    ("softmax_eps_in_denominator", "const double out = exp(orc_get(dt, x, r * N + j) - m) / d;",
+     "const double out = exp(orc_get(dt, x, r * N + j) - m) / (d + 1e-12);", 0),
+    ("softmax_uses_min", "if (v > m)", "if (v < m || m == -INFINITY)", 0),
     ("rn_ties_away", "if (r > 0.5 || (r == 0.5 && fmod(n, 2.0) == 1.0))",
      "if (r >= 0.5)", 0),
     ("rn_flush_subnormals", "        E = emin;                  /* subnormal range",
