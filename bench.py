@@ -220,6 +220,7 @@ class Step:
         self.run(self.sets[0])
         torch.cuda.synchronize()
         kind = nrm.last_plan()[0]
+        self.plan = nrm.PLAN_NAMES.get(kind)
         self.launches_per_step = 1
         if w.op in ("bn", "bn_bwd") and kind in (nrm.PLAN_CTA, nrm.PLAN_GENERIC):
             self.launches_per_step = 2
@@ -457,7 +458,7 @@ def secondary(args, device, stream, l2):
         out.append({"workload": w.name, "us_per_call": per * 1e6, "gbs": b / per / 1e9,
                     "frac_of_measured_peak": b / per / 1e9 / peak,
                     "frac_of_8tbs": b / per / 1e9 / 8000.0, "bytes": b,
-                    "launches_per_call": st.launches_per_step})
+                    "launches_per_call": st.launches_per_step, "plan": st.plan})
         del st
         torch.cuda.empty_cache()
     return out
@@ -554,7 +555,7 @@ def main():
                          "algorithmic_bytes_per_launch": nbytes, "traffic": traffic},
             "gpu_launches": args.steps * step.launches_per_step,
             "clocks": sampler.summary(t0, t1),
-            "plan": nrm.PLAN_NAMES.get(nrm.last_plan()[0]),
+            "plan": step.plan,
         })
         if e2e is not None:
             line["e2e"] = e2e

@@ -125,8 +125,10 @@ int add_rms_fwd(const void *x, const void *residual, const void *w,
 
 /*
  * Bytes of device workspace bn_fwd_train needs for this shape (0 on invalid
- * arguments).  The workspace holds per-(n, c) partial statistics; its content
- * on entry does not matter and it is scratch on exit.
+ * arguments): 8 bytes per chunk of at most 1024 16-byte packs of each (n, c)
+ * plane, i.e. batch * C * ceil(ceil(HW / (16 / element size)) / 1024) * 8.
+ * The workspace holds partial statistics; its content on entry does not
+ * matter and it is scratch on exit.
  */
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype);
 
@@ -201,7 +203,8 @@ int bn_fwd_infer(const void *x, const void *gamma, const void *beta, void *y,
                  cudaStream_t stream);
 
 /* Bytes of device workspace bn_bwd needs for this shape (0 on invalid
- * arguments): per-(n, c) partial sums; content on entry does not matter. */
+ * arguments): partial sums, sized as for bn_fwd_train_workspace_size;
+ * content on entry does not matter. */
 size_t bn_bwd_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype);
 
 /*
@@ -254,7 +257,9 @@ typedef enum {
  * Force a plan (and, where non-zero, the CTA size -- for NRM_PLAN_TMA the
  * size of one row group --, the 16-byte packs per thread, and for
  * NRM_PLAN_TMA the shared-memory stages per group, at most 16, and the row
- * groups per CTA, at most 15) for every later row-operator call in this
+ * groups per CTA, at most 15; for NRM_PLAN_CTA and NRM_PLAN_PERSIST `stages`
+ * sets the L2 prefetch of rows ahead: 0 = automatic (one wave of resident
+ * CTAs ahead), 1 = off, s >= 2 = s - 1 waves ahead) for every later row-operator call in this
  * process; plan 0 restores automatic choice.  A forced plan that cannot run
  * a given call makes that call return NRM_ERR_UNSUPPORTED.  bn_fwd_train
  * follows the forced plan too: NRM_PLAN_CTA selects its streaming two-kernel
@@ -305,6 +310,16 @@ int nrm_device_fault(unsigned *bits, int clear);
  * previous setting.
  */
 int nrm_set_pointer_checks(int enable);
+
+/*
+ * The streaming BatchNorm plans (bn_fwd_train's NRM_PLAN_CTA plan, bn_bwd)
+ * read each input twice: once for the channel statistics, once to normalize.
+ * They process the channels in groups whose inputs take at most `bytes`
+ * (default 48 MiB, a third of GB300's L2), so the second read of a group
+ * comes from L2.  Sets the budget (0 restores the default) and returns the
+ * previous one.  Process-wide; a measurement hook.
+ */
+size_t nrm_set_bn_group_bytes(size_t bytes);
 
 #ifdef __cplusplus
 }

@@ -68,6 +68,8 @@ def _declare(lib):
     lib.nrm_device_fault.restype = _INT
     lib.nrm_set_pointer_checks.argtypes = [_INT]
     lib.nrm_set_pointer_checks.restype = _INT
+    lib.nrm_set_bn_group_bytes.argtypes = [ctypes.c_size_t]
+    lib.nrm_set_bn_group_bytes.restype = ctypes.c_size_t
     return lib
 
 
@@ -334,6 +336,11 @@ def device_fault(clear: bool = True) -> int:
     v = ctypes.c_uint()
     _check(lib().nrm_device_fault(ctypes.byref(v), 1 if clear else 0), "nrm_device_fault")
     return v.value
+
+
+def set_bn_group_bytes(nbytes: int) -> int:
+    """Input bytes per channel group of the streaming BatchNorm plans (0: default)."""
+    return lib().nrm_set_bn_group_bytes(nbytes)
 
 
 def set_pointer_checks(enable: bool) -> bool:

@@ -55,6 +55,7 @@ std::atomic<int> g_force_kind{0}, g_force_threads{0}, g_force_packs{0}, g_force_
     g_force_groups{0};
 std::atomic<unsigned> g_wait_limit{1u << 20};
 std::atomic<int> g_pointer_checks{0};
+std::atomic<size_t> g_bn_group_bytes{(size_t)48 << 20};
 thread_local int t_last_kind = 0, t_last_threads = 0, t_last_packs = 0, t_last_stages = 0,
                  t_last_groups = 0;
 
@@ -222,6 +223,9 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.threads = threads;
         p.packs = packs;
         p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
+        // L2 prefetch distance in waves (forced `stages`: 1 = off, s >= 2 = s - 1)
+        p.prefetch = fstages == 0 ? 1 : fstages - 1;
+        p.stages = fstages;
         break;
     }
     case PLAN_WRAW: {
@@ -250,6 +254,9 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.threads = threads;
         p.packs = packs;
         p.smem_params = smem_params ? 1 : 0;
+        // L2 prefetch distance in waves (forced `stages`: 1 = off, s >= 2 = s - 1)
+        p.prefetch = fstages == 0 ? 1 : fstages - 1;
+        p.stages = fstages;
         break;
     }
     case PLAN_TMA: {
@@ -359,6 +366,10 @@ int check_elem_alignment(std::initializer_list<const void *> ps, size_t es) {
 
 }  // namespace
 
+namespace nrm {
+size_t bn_group_bytes() { return g_bn_group_bytes.load(std::memory_order_relaxed); }
+}  // namespace nrm
+
 extern "C" {
 
 int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
@@ -429,8 +440,13 @@ int add_rms_fwd(const void *x, const void *residual, const void *w, void *residu
 
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
     if (!dtype_ok(dtype) || batch < 1 || C < 1 || HW < 1) return 0;
-    if ((uint64_t)batch > (uint64_t)INT64_MAX / 8 / (uint64_t)C) return 0;
-    return (size_t)batch * (size_t)C * 8;
+    // one float2 per chunk of at most 1024 packs of a plane (streaming
+    // plans); the scalar plan needs one per plane, never more
+    const int64_t V = 16 / (int64_t)elem_size(dtype);
+    const int64_t packs = (HW + V - 1) / V;
+    const int64_t nch = (packs + kBnChunkPacks - 1) / kBnChunkPacks;
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / 8 / (uint64_t)C / (uint64_t)nch) return 0;
+    return (size_t)batch * (size_t)C * (size_t)nch * 8;
 }
 
 int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
@@ -586,5 +602,9 @@ void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups
 unsigned nrm_set_wait_limit(unsigned tries) { return g_wait_limit.exchange(tries); }
 
 int nrm_set_pointer_checks(int enable) { return g_pointer_checks.exchange(enable ? 1 : 0); }
+
+size_t nrm_set_bn_group_bytes(size_t bytes) {
+    return g_bn_group_bytes.exchange(bytes ? bytes : (size_t)48 << 20);
+}
 
 }  // extern "C"

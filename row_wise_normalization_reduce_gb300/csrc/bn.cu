@@ -166,52 +166,56 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Streaming two-kernel plan (16-byte aligned planes that fit one CTA's
-// registers).
+// Streaming two-kernel plan (16-byte aligned planes of any size).
 //
-// bn_stats_kernel: one CTA per (n, c) plane holds the plane in registers
-// (BNS_PACKS 16-byte packs per thread) and computes its exact partial
-// statistics on d = x - K (K = x[0, c, 0]) with a corrected two-pass:
-// (mean_d, M2) into the workspace.  It then allows the dependent launch to
-// start.
+// The work is cut into units, chunks of at most 1024 packs of one plane
+// (bn_common.cuh), and the channels into groups whose x fits comfortably in
+// L2.  Per group:
+// bn_stats_kernel: one CTA per unit holds the chunk in registers and computes
+// its exact partial statistics on d = x - K (K = x[0, c, 0]) with a corrected
+// two-pass: (mean_d, M2) into the workspace.  It then allows the dependent
+// launch to start.
 // bn_norm_kernel (launched with programmatic stream serialization): each CTA
-// loads its plane of x into registers first -- x is an input, and for a batch
-// that fits in L2 these reads hit L2 -- then waits for the statistics kernel
-// (griddepcontrol.wait), folds the channel's batch partials in a fixed order
+// loads its chunk of x into registers first -- x is an input, and the group
+// was just read, so these reads hit L2 -- then waits for the statistics
+// kernel (griddepcontrol.wait), folds the channel's partials in a fixed order
 // (every CTA of a channel gets the same bits), normalizes and writes y.  The
-// CTA of plane n = 0 writes save_mean/save_rstd and the running statistics.
+// CTA of unit (n = 0, chunk 0) writes save_mean/save_rstd and the running
+// statistics.  It lets the next group's statistics kernel start as soon as
+// its own loads are issued, so that kernel fills the SMs this one frees; that
+// kernel waits at its end for this one to finish (griddepcontrol.wait), so
+// each call's last kernel completes after all of the call's kernels.  No
+// kernel of the chain waits on a grid that is not fully resident: a
+// dependent grid starts only once every CTA of its primary has started.
 // ---------------------------------------------------------------------------
-constexpr int BNS_THREADS = 256;
-constexpr int BNS_PACKS = 4;  // packs per thread: planes of up to 1024 packs
-
 template <typename T>
-__global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
+__global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, const BnChunks u) {
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     constexpr int NW = BNS_THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
     const int tid = threadIdx.x;
-    const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q = (int)(HW / IO<T>::V);
-    const float cnt = (float)HW;
+    const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
     float2 *ws = static_cast<float2 *>(a.ws);
     int par = 0;
-    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
-        const int64_t n = p / a.C, c = p - n * a.C;
-        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
+    for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
+        const BnUnit w = bn_unit(u, idx);
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) +
+                                                          (w.n * a.C + w.c) * HW) + w.off;
         // first read of x: default L2 policy, so the normalize kernel's second
         // read finds it in L2 (a streaming, evict-first read would lose it)
         uint4 v[BNS_PACKS];
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q) v[k] = __ldg(xp + tid + k * BNS_THREADS);
-        const float K = bn_elem<T>(a.x, c * HW);
+            if (tid + k * BNS_THREADS < w.len) v[k] = __ldg(xp + tid + k * BNS_THREADS);
+        const float K = bn_elem<T>(a.x, w.c * HW);
+        const float cnt = (float)(w.len * IO<T>::V);
         const float2 nk = f2(-K);
         float2 acc = f2(0.f);
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q) {
+            if (tid + k * BNS_THREADS < w.len) {
                 float2 f[H];
                 io2::unpack(v[k], f);
 #pragma unroll
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
         float2 e1 = f2(0.f), e2 = f2(0.f);
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q) {
+            if (tid + k * BNS_THREADS < w.len) {
                 float2 f[H];
                 io2::unpack(v[k], f);
 #pragma unroll
@@ -236,41 +240,51 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a) {
         const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2[par]);
         if (tid == 0) {
             const float cc = E.x / cnt;
-            ws[c * a.batch + n] = make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
+            ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] =
+                make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
         }
     }
     pdl_launch_dependents();
+    // A later group's statistics kernel overlaps the previous group's
+    // normalize kernel; it finishes only after that kernel has, so the end of
+    // the last kernel of a call implies the end of all of them.
+    pdl_wait();
 }
 
 template <typename T>
-__global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
+__global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a, const BnChunks u) {
     using io2 = IO2<T>;
     constexpr int H = io2::H;
+    constexpr int V = IO<T>::V;
     __shared__ float stat[2][3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q = (int)(HW / IO<T>::V);
+    const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
+    const int64_t per_channel = a.batch * u.nch;  // partials per channel
     const float ctot = (float)(a.batch * HW);
     const float2 *ws = static_cast<const float2 *>(a.ws);
     bool waited = false;
     int par = 0;
-    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
-        const int64_t n = p / a.C, c = p - n * a.C;
-        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
+    for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
+        const BnUnit w = bn_unit(u, idx);
+        const int64_t base = (w.n * a.C + w.c) * HW;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + base) + w.off;
         uint4 v[BNS_PACKS];
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q) v[k] = __ldcs(xp + tid + k * BNS_THREADS);
-        const float K = bn_elem<T>(a.x, c * HW);
+            if (tid + k * BNS_THREADS < w.len) v[k] = __ldcs(xp + tid + k * BNS_THREADS);
+        const float K = bn_elem<T>(a.x, w.c * HW);
         if (!waited) {
+            pdl_launch_dependents();  // the next group's statistics may start
             pdl_wait();  // the statistics kernel has finished and its writes are visible
             waited = true;
         }
         if (warp == 0) {
             Stats st{0.f, 0.f, 0.f};
-            for (int64_t j = lane; j < a.batch; j += 32) {
-                const float2 qq = ws[c * a.batch + j];
-                st = combine(st, Stats{(float)HW, qq.x, qq.y});
+            for (int64_t j = lane; j < per_channel; j += 32) {
+                const float2 qq = ws[w.c * per_channel + j];
+                const int kk = (int)(j % u.nch);
+                const float cn = (float)(min(u.cpk, u.q - kk * u.cpk) * V);
+                st = combine(st, Stats{cn, qq.x, qq.y});
             }
             st = warp_stats_down(st);
             if (lane == 0) {
@@ -282,14 +296,14 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
         }
         __syncthreads();
         const float md = stat[par][0], rstd = stat[par][1];
-        if (n == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[par][2], rstd);
-        const float g = bn_param<T>(a.gamma, c, 1.f);
-        const float bb = bn_param<T>(a.beta, c, 0.f);
+        if (w.n == 0 && w.k == 0 && tid == 0) bn_write_channel_stats(a, w.c, K, md, stat[par][2], rstd);
+        const float g = bn_param<T>(a.gamma, w.c, 1.f);
+        const float bb = bn_param<T>(a.beta, w.c, 0.f);
         const float2 nk = f2(-K), nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
-        uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + p * HW);
+        uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + base) + w.off;
 #pragma unroll
         for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < q) {
+            if (tid + k * BNS_THREADS < w.len) {
                 float2 f[H], o[H];
                 io2::unpack(v[k], f);
 #pragma unroll
@@ -298,7 +312,10 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a) {
                 __stcs(yp + tid + k * BNS_THREADS, io2::pack(o));
             }
     }
-    if (!waited) pdl_wait();
+    if (!waited) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -577,29 +594,29 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
 
 template <typename T>
 cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
-    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
-    bn_stats_kernel<T><<<grid, BNS_THREADS, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(BNS_THREADS);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, bn_norm_kernel<T>, a);
-    return e == cudaSuccess ? cudaGetLastError() : e;
+    BnChunks u = bn_chunks(a.HW / IO<T>::V);
+    const int64_t G = bn_group_channels(a.C, a.batch * a.HW * (int64_t)sizeof(T),
+                                        (int64_t)bn_group_bytes());
+    cudaError_t e = cudaSuccess;
+    for (int64_t c0 = 0; c0 < a.C && e == cudaSuccess; c0 += G) {
+        u.c0 = c0;
+        u.G = (a.C - c0) < G ? (a.C - c0) : G;
+        const unsigned grid = bn_grid(a.batch * u.G * u.nch, num_sms);
+        // the first group's statistics follow the stream's earlier work; later
+        // groups read other channels and only overlap the previous group
+        e = launch_pdl(bn_stats_kernel<T>, grid, BNS_THREADS, s, c0 > 0, a, u);
+        if (e == cudaSuccess) e = launch_pdl(bn_norm_kernel<T>, grid, BNS_THREADS, s, true, a, u);
+    }
+    return e;
 }
 
 template <typename T>
 cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int *used) {
     constexpr int V = IO<T>::V;
     const bool aligned = (a.HW % V == 0) && bn_aligned16(a.x) && bn_aligned16(a.y);
-    const bool stream_ok = aligned && a.HW / V <= (int64_t)BNS_THREADS * BNS_PACKS;
-    if (aligned && a.fault && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_CLUSTER)) {
+    const bool stream_ok = aligned && a.HW / V < kBnMaxPlanePacks;
+    if (aligned && a.fault &&
+        (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_CLUSTER || a.bn_plan == BN_PLAN_NO_STREAM)) {
         bool launched = false;
         const cudaError_t e = launch_bn_cluster<T>(a, s, &launched);
         if (launched) {
@@ -679,6 +696,11 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
     if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / 4) return NRM_ERR_SHAPE;
     if (batch * HW < 2) return NRM_ERR_SHAPE;
     if (batch * C > kBnStaticPlanes) return NRM_ERR_TOO_LARGE;
+    // the streaming plan keeps one partial per chunk of at most kBnChunkPacks
+    // packs; when those do not fit, the per-plane plans still do
+    const int64_t V = dtype == NRM_F32 ? 4 : 8;
+    const int64_t nch = ((HW + V - 1) / V + kBnChunkPacks - 1) / kBnChunkPacks;
+    const int bn_plan = batch * C * nch > kBnStaticPlanes ? BN_PLAN_NO_STREAM : BN_PLAN_AUTO;
     if (!std::isfinite(eps) || eps < 0.f || !(momentum >= 0.f && momentum <= 1.f))
         return NRM_ERR_VALUE;
     if (!x || !y) return NRM_ERR_NULL;
@@ -722,7 +744,7 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
         return NRM_ERR_DEVICE;
     }
     BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
-             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, BN_PLAN_AUTO};
+             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, bn_plan};
     int used = 0;
     return launch_bn_train(a, dtype, sms, stream, &used) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

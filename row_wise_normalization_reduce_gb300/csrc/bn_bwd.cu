@@ -31,17 +31,15 @@ namespace nrm {
 
 namespace {
 
-constexpr int BBS_THREADS = 256;
-constexpr int BBS_PACKS = 4;  // packs of dy and of x per thread
 constexpr int BB_THREADS = 256;
 
-// Fold the batch partials of channel c (warp 0; lane j takes partials j,
+// Fold the `count` partials of channel c (warp 0; lane j takes partials j,
 // j + 32, ... in order, then a butterfly): the same bits in every CTA.
-__device__ __forceinline__ float2 bn_bwd_fold(const float2 *ws, int64_t c, int64_t batch) {
+__device__ __forceinline__ float2 bn_bwd_fold(const float2 *ws, int64_t c, int64_t count) {
     float2 s = f2(0.f);
     const int lane = threadIdx.x & 31;
-    for (int64_t j = lane; j < batch; j += 32) {
-        const float2 q = ws[c * batch + j];
+    for (int64_t j = lane; j < count; j += 32) {
+        const float2 q = ws[c * count + j];
         s.x += q.x;
         s.y += q.y;
     }
@@ -49,36 +47,39 @@ __device__ __forceinline__ float2 bn_bwd_fold(const float2 *ws, int64_t c, int64
 }
 
 // ---------------------------------------------------------------------------
-// Streaming plan
+// Streaming plan: units are chunks of at most 1024 packs of one plane, and
+// the channels are processed in groups whose dy and x fit comfortably in L2
+// (bn_common.cuh), so stage 2 re-reads them from L2.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(BBS_THREADS) bn_bwd_sums_kernel(const BnBwdArgs a) {
+__global__ void __launch_bounds__(BNS_THREADS) bn_bwd_sums_kernel(const BnBwdArgs a,
+                                                                  const BnChunks u) {
     using io2 = IO2<T>;
     constexpr int H = io2::H;
-    constexpr int NW = BBS_THREADS / 32;
+    constexpr int NW = BNS_THREADS / 32;
     __shared__ float2 s2[2][NW];
     const int tid = threadIdx.x;
-    const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q = (int)(HW / IO<T>::V);
+    const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
     float2 *ws = static_cast<float2 *>(a.ws);
     int par = 0;
-    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
-        const int64_t n = p / a.C, c = p - n * a.C;
-        const uint4 *gp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dy) + p * HW);
-        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
-        // default L2 policy: stage 2 reads the same planes again
-        uint4 vg[BBS_PACKS], vx[BBS_PACKS];
+    for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
+        const BnUnit w = bn_unit(u, idx);
+        const int64_t base = (w.n * a.C + w.c) * HW;
+        const uint4 *gp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dy) + base) + w.off;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + base) + w.off;
+        // default L2 policy: stage 2 reads the same chunks again
+        uint4 vg[BNS_PACKS], vx[BNS_PACKS];
 #pragma unroll
-        for (int k = 0; k < BBS_PACKS; ++k)
-            if (tid + k * BBS_THREADS < q) {
-                vg[k] = __ldg(gp + tid + k * BBS_THREADS);
-                vx[k] = __ldg(xp + tid + k * BBS_THREADS);
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < w.len) {
+                vg[k] = __ldg(gp + tid + k * BNS_THREADS);
+                vx[k] = __ldg(xp + tid + k * BNS_THREADS);
             }
-        const float2 nm = f2(-a.mean[c]);
+        const float2 nm = f2(-a.mean[w.c]);
         float2 sg = f2(0.f), sgx = f2(0.f);
 #pragma unroll
-        for (int k = 0; k < BBS_PACKS; ++k)
-            if (tid + k * BBS_THREADS < q) {
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < w.len) {
                 float2 g[H], x[H];
                 io2::unpack(vg[k], g);
                 io2::unpack(vx[k], x);
@@ -89,57 +90,60 @@ __global__ void __launch_bounds__(BBS_THREADS) bn_bwd_sums_kernel(const BnBwdArg
                 }
             }
         const float2 S = cta_sum_all<NW>(make_float2(hsum(sg), hsum(sgx)), s2[par]);
-        if (tid == 0) ws[c * a.batch + n] = S;
+        if (tid == 0) ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] = S;
     }
     pdl_launch_dependents();
+    pdl_wait();  // finish after the previous group's stage 2 (see bn.cu)
 }
 
 template <typename T>
-__global__ void __launch_bounds__(BBS_THREADS) bn_bwd_dx_kernel(const BnBwdArgs a) {
+__global__ void __launch_bounds__(BNS_THREADS) bn_bwd_dx_kernel(const BnBwdArgs a,
+                                                                const BnChunks u) {
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     __shared__ float2 sums[2];
     const int tid = threadIdx.x;
-    const int64_t planes = a.batch * a.C, HW = a.HW;
-    const int q = (int)(HW / IO<T>::V);
+    const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
     const float cnt = (float)(a.batch * HW);
     const float2 *ws = static_cast<const float2 *>(a.ws);
     bool waited = false;
     int par = 0;
-    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, par ^= 1) {
-        const int64_t n = p / a.C, c = p - n * a.C;
-        const uint4 *gp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dy) + p * HW);
-        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + p * HW);
-        uint4 vg[BBS_PACKS], vx[BBS_PACKS];
+    for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
+        const BnUnit w = bn_unit(u, idx);
+        const int64_t base = (w.n * a.C + w.c) * HW;
+        const uint4 *gp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dy) + base) + w.off;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) + base) + w.off;
+        uint4 vg[BNS_PACKS], vx[BNS_PACKS];
 #pragma unroll
-        for (int k = 0; k < BBS_PACKS; ++k)
-            if (tid + k * BBS_THREADS < q) {
-                vg[k] = __ldcs(gp + tid + k * BBS_THREADS);
-                vx[k] = __ldcs(xp + tid + k * BBS_THREADS);
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < w.len) {
+                vg[k] = __ldcs(gp + tid + k * BNS_THREADS);
+                vx[k] = __ldcs(xp + tid + k * BNS_THREADS);
             }
         if (!waited) {
+            pdl_launch_dependents();  // the next group's stage 1 may start
             pdl_wait();  // stage 1 has finished and its partials are visible
             waited = true;
         }
         if (tid < 32) {
-            const float2 S = bn_bwd_fold(ws, c, a.batch);
+            const float2 S = bn_bwd_fold(ws, w.c, a.batch * u.nch);
             if (tid == 0) sums[par] = S;
         }
         __syncthreads();
-        const float mean = a.mean[c], rstd = a.rstd[c];
+        const float mean = a.mean[w.c], rstd = a.rstd[w.c];
         const float2 S = sums[par];
         const float dgamma = S.y * rstd;  // sum dy * xhat
-        if (n == 0 && tid == 0) {
-            if (a.dbeta) a.dbeta[c] = S.x;
-            if (a.dgamma) a.dgamma[c] = dgamma;
+        if (w.n == 0 && w.k == 0 && tid == 0) {
+            if (a.dbeta) a.dbeta[w.c] = S.x;
+            if (a.dgamma) a.dgamma[w.c] = dgamma;
         }
-        const float gr = bn_param<T>(a.gamma, c, 1.f) * rstd;
+        const float gr = bn_param<T>(a.gamma, w.c, 1.f) * rstd;
         const float2 nm = f2(-mean), r2 = f2(rstd), na = f2(-(S.x / cnt)),
                      nb = f2(-(dgamma / cnt)), gr2 = f2(gr);
-        uint4 *dp = reinterpret_cast<uint4 *>(static_cast<T *>(a.dx) + p * HW);
+        uint4 *dp = reinterpret_cast<uint4 *>(static_cast<T *>(a.dx) + base) + w.off;
 #pragma unroll
-        for (int k = 0; k < BBS_PACKS; ++k)
-            if (tid + k * BBS_THREADS < q) {
+        for (int k = 0; k < BNS_PACKS; ++k)
+            if (tid + k * BNS_THREADS < w.len) {
                 float2 g[H], x[H], o[H];
                 io2::unpack(vg[k], g);
                 io2::unpack(vx[k], x);
@@ -148,10 +152,13 @@ __global__ void __launch_bounds__(BBS_THREADS) bn_bwd_dx_kernel(const BnBwdArgs 
                     const float2 xh = __fmul2_rn(__fadd2_rn(x[h], nm), r2);
                     o[h] = __fmul2_rn(gr2, __ffma2_rn(xh, nb, __fadd2_rn(g[h], na)));
                 }
-                __stcs(dp + tid + k * BBS_THREADS, io2::pack(o));
+                __stcs(dp + tid + k * BNS_THREADS, io2::pack(o));
             }
     }
-    if (!waited) pdl_wait();
+    if (!waited) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -217,27 +224,25 @@ __global__ void __launch_bounds__(BB_THREADS) bn_bwd_apply_kernel(const BnBwdArg
 template <typename T>
 cudaError_t launch_bn_bwd_t(const BnBwdArgs &a, int num_sms, cudaStream_t s, int *used) {
     constexpr int V = IO<T>::V;
-    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
     const bool stream_ok = a.bn_plan != BN_PLAN_SCALAR && a.HW % V == 0 &&
-                           a.HW / V <= (int64_t)BBS_THREADS * BBS_PACKS && bn_aligned16(a.dy) &&
+                           a.HW / V < kBnMaxPlanePacks && bn_aligned16(a.dy) &&
                            bn_aligned16(a.x) && bn_aligned16(a.dx);
     *used = stream_ok ? PLAN_CTA : PLAN_GENERIC;
     if (stream_ok) {
-        bn_bwd_sums_kernel<T><<<grid, BBS_THREADS, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(BBS_THREADS);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, bn_bwd_dx_kernel<T>, a);
-        return e == cudaSuccess ? cudaGetLastError() : e;
+        BnChunks u = bn_chunks(a.HW / V);
+        const int64_t G = bn_group_channels(a.C, 2 * a.batch * a.HW * (int64_t)sizeof(T),
+                                            (int64_t)bn_group_bytes());
+        cudaError_t e = cudaSuccess;
+        for (int64_t c0 = 0; c0 < a.C && e == cudaSuccess; c0 += G) {
+            u.c0 = c0;
+            u.G = (a.C - c0) < G ? (a.C - c0) : G;
+            const unsigned grid = bn_grid(a.batch * u.G * u.nch, num_sms);
+            e = launch_pdl(bn_bwd_sums_kernel<T>, grid, BNS_THREADS, s, c0 > 0, a, u);
+            if (e == cudaSuccess) e = launch_pdl(bn_bwd_dx_kernel<T>, grid, BNS_THREADS, s, true, a, u);
+        }
+        return e;
     }
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
     bn_bwd_partial_kernel<T><<<grid, BB_THREADS, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

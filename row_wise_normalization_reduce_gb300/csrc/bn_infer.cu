@@ -11,11 +11,18 @@
 // at HBM speed and avoids the cancellation of x * s_c against t_c when the
 // running mean is large compared with the spread.
 //
-// Mapping: the CTA's threads are split into groups of TPP threads (a power of
-// two, at most the CTA), one (n, c) plane per group; a group walks its plane
-// with 16-byte packs (PACKS in flight per thread).  Small planes thus share a
-// CTA instead of leaving most of its threads idle, and a plane's constants
-// are computed once per thread, not per element.
+// Main plan (16-byte packs, C <= 2048): the tensor is one flat array of
+// 16-byte packs walked by a grid of resident CTAs (BNI_PACKS packs in flight
+// per thread, consecutive threads on consecutive packs), so every SM streams
+// until the end whatever the plane size.  A pack's channel is
+// (pack / packs_per_plane) mod C, by multiply-high division; the channel
+// constants (mean, rstd, gamma, beta) are computed once per CTA into a
+// shared-memory table.
+//
+// Fallback plans: the CTA's threads are split into groups of TPP threads (a
+// power of two, at most the CTA), one (n, c) plane per group; a group walks
+// its plane with 16-byte packs, or elements when the layout does not allow
+// packs.
 #include <cmath>
 #include <cstdint>
 
@@ -40,6 +47,55 @@ __device__ __forceinline__ ChannelConst bn_infer_const(const BnInferArgs &a, int
     k.g = bn_param<T>(a.gamma, c, 1.f);
     k.b = bn_param<T>(a.beta, c, 0.f);
     return k;
+}
+
+constexpr int BNI_MAX_TABLE = 2048;  // channels of the shared-memory table (32 KB)
+
+// Resident CTAs per SM the flat kernel is compiled for (registers): binary32
+// fits 8 (32 registers), the 16-bit types 6 (their unpacking needs 40).
+template <typename T> constexpr int bni_ctas_per_sm() { return sizeof(T) == 4 ? 8 : 6; }
+
+template <typename T>
+__global__ void __launch_bounds__(BNI_THREADS, bni_ctas_per_sm<T>()) bn_infer_flat_kernel(const BnInferArgs a,
+                                                                    const uint32_t total,
+                                                                    const FastDiv per_plane,
+                                                                    const FastDiv channels) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
+    extern __shared__ float4 table[];  // C entries
+    for (int c = threadIdx.x; c < (int)a.C; c += BNI_THREADS) {
+        const ChannelConst k = bn_infer_const<T>(a, c);
+        table[c] = make_float4(-k.mean, k.rstd, k.g, k.b);
+    }
+    __syncthreads();
+    const uint4 *X = static_cast<const uint4 *>(a.x);
+    uint4 *Y = static_cast<uint4 *>(a.y);
+    const uint32_t stride = gridDim.x * BNI_THREADS;
+    for (uint32_t base = blockIdx.x * BNI_THREADS + threadIdx.x; base < total;
+         base += stride * BNI_PACKS) {
+        uint4 v[BNI_PACKS];
+#pragma unroll
+        for (int j = 0; j < BNI_PACKS; ++j) {
+            const uint32_t i = base + j * stride;
+            if (i < total) v[j] = ld_stream(X + i);
+        }
+#pragma unroll
+        for (int j = 0; j < BNI_PACKS; ++j) {
+            const uint32_t i = base + j * stride;
+            if (i < total) {
+                const uint32_t plane = fast_div(i, per_plane);
+                const uint32_t c = plane - fast_div(plane, channels) * channels.d;
+                const float4 k = table[c];
+                const float2 nm = f2(k.x), r2 = f2(k.y), g2 = f2(k.z), b2 = f2(k.w);
+                float2 f[H], o[H];
+                io2::unpack(v[j], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(f[h], nm), r2), g2, b2);
+                st_stream(Y + i, io2::pack(o));
+            }
+        }
+    }
 }
 
 // Vector plan: HW a multiple of the pack width, x and y 16-byte aligned.
@@ -111,10 +167,20 @@ cudaError_t launch_bn_infer_t(const BnInferArgs &a, int num_sms, cudaStream_t s,
     const int64_t planes = a.batch * a.C;
     const bool vec = a.bn_plan != BN_PLAN_SCALAR && a.HW % V == 0 && a.HW / V < (1 << 30) &&
                      bn_aligned16(a.x) && bn_aligned16(a.y);
+    *used = vec ? PLAN_CTA : PLAN_GENERIC;
+    const int64_t total = planes * (a.HW / V);
+    if (vec && a.C <= BNI_MAX_TABLE &&
+        total < ((int64_t)1 << 32) - (int64_t)num_sms * 8 * BNI_THREADS * BNI_PACKS) {
+        const int64_t need = (total + BNI_THREADS * BNI_PACKS - 1) / (BNI_THREADS * BNI_PACKS);
+        const int64_t slots = (int64_t)num_sms * bni_ctas_per_sm<T>();
+        const unsigned grid = (unsigned)(need < slots ? need : slots);
+        bn_infer_flat_kernel<T><<<grid, BNI_THREADS, (size_t)a.C * sizeof(float4), s>>>(
+            a, (uint32_t)total, make_fastdiv((uint32_t)(a.HW / V)), make_fastdiv((uint32_t)a.C));
+        return cudaGetLastError();
+    }
     const int l = tpp_log2_for(vec ? a.HW / V : a.HW);
     const int64_t ppi = BNI_THREADS >> l;
     const unsigned grid = bn_grid((planes + ppi - 1) / ppi, num_sms);
-    *used = vec ? PLAN_CTA : PLAN_GENERIC;
     if (vec) bn_infer_vec_kernel<T><<<grid, BNI_THREADS, 0, s>>>(a, l);
     else bn_infer_scalar_kernel<T><<<grid, BNI_THREADS, 0, s>>>(a, l);
     return cudaGetLastError();

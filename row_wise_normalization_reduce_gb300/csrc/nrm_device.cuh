@@ -156,6 +156,12 @@ __device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
     __stcs(reinterpret_cast<uint4 *>(p), v);
 }
 
+// Ask L2 to fetch [p, p + bytes) from HBM (bytes a multiple of 16, p 16-byte
+// aligned).  A hint: no register holds the data and nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Reduction engine.
 // ---------------------------------------------------------------------------

@@ -61,6 +61,7 @@ struct Plan {
     int smem_params;  // TMA: parameters widened to binary32 in shared memory
     int sms;       // SMs of the device
     int64_t grid;  // CTAs launched (TMA: set at launch from occupancy)
+    int prefetch;  // CTA: L2 prefetch distance in waves of resident CTAs (0: off)
 };
 
 // Address of the current device's fault word (set up once per device), or
@@ -96,7 +97,20 @@ struct BnArgs {
 // BatchNorm plans: automatic, streaming two kernels (registers + dependent
 // launch), one cluster of CTAs per channel (shared memory + DSMEM), and the
 // scalar two-kernel plan (any layout).
-enum BnPlan { BN_PLAN_AUTO = 0, BN_PLAN_STREAM = 1, BN_PLAN_CLUSTER = 2, BN_PLAN_SCALAR = 3 };
+// BN_PLAN_NO_STREAM: automatic choice without the streaming plan (whose
+// per-chunk partials may not fit a fixed partials array).
+enum BnPlan {
+    BN_PLAN_AUTO = 0,
+    BN_PLAN_STREAM = 1,
+    BN_PLAN_CLUSTER = 2,
+    BN_PLAN_SCALAR = 3,
+    BN_PLAN_NO_STREAM = 4
+};
+
+// Packs (16 bytes) per work unit of the streaming BatchNorm plans: a unit is
+// a chunk of at most this many packs of one plane; the workspace holds one
+// float2 per unit.
+constexpr int kBnChunkPacks = 1024;
 // The launchers report the plan they ran through *used as a PlanKind
 // (cluster: PLAN_TMA, streaming: PLAN_CTA, scalar: PLAN_GENERIC).
 cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, int *used);

@@ -14,7 +14,8 @@
 //                       so rows are always in flight while others are reduced
 //                       (row_pipe.cuh).
 //   row_persist_kernel  persistent CTAs; the next row's packs are loaded into
-//                       registers while the current row is reduced, and the
+//                       registers while the current row is reduced (and
+//                       later rows are prefetched into L2), and the
 //                       parameters are widened to binary32 in shared memory
 //                       once per CTA.
 //   row_wraw_kernel     warp per row with the raw packs of the whole row in
@@ -291,9 +292,13 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 #define NRM_MIN_BLOCKS(THREADS, PACKS)                                                   \
     (((PACKS) <= 2 && NRM_CTA_MIN_THREADS / (THREADS) > 0) ? NRM_CTA_MIN_THREADS / (THREADS) : 1)
 
+// One CTA per row.  With pf > 0, thread 0 first asks L2 to fetch the row
+// that the CTA taking this one's slot pf CTAs later will load (pf = a whole
+// number of waves of resident CTAs): the next waves then find their rows in
+// L2, which keeps HBM streaming without more registers per row in flight.
 template <int OP, typename T, int THREADS, int PACKS>
 __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
-    row_cta_kernel(const RowArgs a) {
+    row_cta_kernel(const RowArgs a, const int64_t pf) {
     constexpr int NW = THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
@@ -301,6 +306,11 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
     const T *R = static_cast<const T *>(a.res);
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
+        if (pf > 0 && threadIdx.x == 0 && row + pf < a.rows) {
+            const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+            prefetch_l2_bulk(X + (row + pf) * a.N, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, bytes);
+        }
         CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
         const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
         const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
@@ -312,10 +322,12 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
 // gridDim.x, as many CTAs as are resident).  Row r + G's packs are loaded
 // into registers before row r is reduced, so every CTA always has a row in
 // flight; parameters are widened to binary32 in shared memory once per CTA
-// (SmemParams layout) when smem_params is set.
+// (SmemParams layout) when smem_params is set.  With pf_waves > 0, thread 0
+// also asks L2 for the row pf_waves rows beyond the one in registers, so the
+// register prefetch of later rows hits L2.
 template <int OP, typename T, int THREADS, int PACKS>
 __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
-    row_persist_kernel(const RowArgs a, const int smem_params) {
+    row_persist_kernel(const RowArgs a, const int smem_params, const int pf_waves) {
     constexpr int NW = THREADS / 32;
     extern __shared__ __align__(16) float4 sparams[];
     __shared__ float s1[2][NW];
@@ -329,6 +341,8 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
     const SmemParams<T> sprm{sparams, P};
     const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
     const int64_t G = gridDim.x;
+    const int64_t pf = (int64_t)(pf_waves + 1) * G;
+    const uint32_t row_bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
 
     uint4 rx[PACKS], rr[PACKS];
     int64_t row = blockIdx.x;
@@ -338,6 +352,10 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
     }
     int parity = 0;
     for (; row < a.rows; row += G, parity ^= 1) {
+        if (pf_waves > 0 && threadIdx.x == 0 && row + pf < a.rows) {
+            prefetch_l2_bulk(X + (row + pf) * a.N, row_bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, row_bytes);
+        }
         uint4 nx[PACKS], nr[PACKS];
         const int64_t next = row + G;
         if (next < a.rows) {
@@ -631,7 +649,7 @@ cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Persistent register-pipeline launch: dynamic shared memory = parameters in
+// Persistent launch: dynamic shared memory = parameters in
 // binary32 (when smem_params), grid = min(rows, SMs x resident CTAs per SM).
 template <int OP, typename T, int THREADS, int PACKS>
 cudaError_t launch_persist(const RowArgs &a, const Plan &p, cudaStream_t s) {
@@ -663,7 +681,7 @@ cudaError_t launch_persist(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = a.rows < slots ? a.rows : slots;
-    kernel<<<(unsigned)grid, THREADS, smem, s>>>(a, p.smem_params);
+    kernel<<<(unsigned)grid, THREADS, smem, s>>>(a, p.smem_params, p.prefetch);
     return cudaGetLastError();
 }
 
@@ -704,6 +722,34 @@ cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// CTA-per-row launch: grid = rows (clamped); the L2 prefetch distance is
+// p.prefetch waves of resident CTAs (occupancy computed once per device and
+// kernel instance).
+template <int OP, typename T, int THREADS, int PACKS>
+cudaError_t launch_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    auto kernel = row_cta_kernel<OP, T, THREADS, PACKS>;
+    int64_t pf = 0;
+    if (p.prefetch > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        static std::mutex mu;  // one cache per kernel instance
+        static int cached_per_sm[64] = {};
+        int per_sm = 0;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!cached_per_sm[dev]) {
+                const cudaError_t e =
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, THREADS, 0);
+                if (e != cudaSuccess) return e;
+            }
+            per_sm = cached_per_sm[dev];
+        }
+        pf = (int64_t)p.prefetch * p.sms * per_sm;
+    }
+    kernel<<<(unsigned)p.grid, THREADS, 0, s>>>(a, pf);
+    return cudaGetLastError();
+}
+
 template <int OP, typename T>
 cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const dim3 grid((unsigned)p.grid);
@@ -725,10 +771,7 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         }
     } else if (p.kind == PLAN_CTA) {
 #define NRM_CTA_CASE(TH, PK)                                                       \
-    if (p.threads == TH && p.packs == PK) {                                        \
-        row_cta_kernel<OP, T, TH, PK><<<grid, TH, 0, s>>>(a);                      \
-        return cudaGetLastError();                                                 \
-    }
+    if (p.threads == TH && p.packs == PK) return launch_cta<OP, T, TH, PK>(a, p, s);
         NRM_CTA_CASE(128, 1) NRM_CTA_CASE(256, 1) NRM_CTA_CASE(512, 1) NRM_CTA_CASE(1024, 1)
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
         NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)

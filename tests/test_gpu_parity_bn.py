@@ -119,3 +119,25 @@ def test_bn_forward_then_backward_on_gpu():
     s = dx.double().sum(dim=(0, 2, 3)).abs()
     assert torch.all(s <= 1e-4 * dx.double().abs().sum(dim=(0, 2, 3)))
     assert torch.allclose(db.double(), dy.double().sum(dim=(0, 2, 3)), rtol=1e-5, atol=1e-3)
+
+
+@pytest.mark.parametrize("op", ["bn", "bn_bwd"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("group_bytes", [0, 1], ids=["default_groups", "one_channel_groups"])
+@pytest.mark.parametrize("shape", [(2, 5, 64, 80), (1, 2, 96, 96), (2, 3, 70, 70), (3, 4, 40, 200)])
+def test_bn_stream_chunks_and_groups(orc, shape, group_bytes, dtype, op):
+    # planes longer than one 1024-pack unit (several chunks per plane, the
+    # last one shorter where the plane does not divide evenly), and channel
+    # groups down to one channel per group (two launches per channel)
+    w = W.BN_F32_32x64x56x56 if op == "bn" else W.BN_BWD_F32_32x64x56x56
+    inp = W.make_inputs(w, shape=shape, dtype=dtype)
+    nrm.force_plan(nrm.PLAN_CTA)
+    old = nrm.set_bn_group_bytes(group_bytes)
+    try:
+        gpu = RN.run_gpu(op, inp, 1e-5, 0.1)
+        again = RN.run_gpu(op, inp, 1e-5, 0.1)
+    finally:
+        nrm.set_bn_group_bytes(old)
+    for k in gpu:
+        assert (gpu[k] == again[k]).all(), k
+    RN.compare(op, inp, gpu, RN.run_oracle(orc, op, inp, 1e-5, 0.1))
