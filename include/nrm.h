@@ -314,10 +314,11 @@ int nrm_set_pointer_checks(int enable);
 /*
  * The streaming BatchNorm plans (bn_fwd_train's NRM_PLAN_CTA plan, bn_bwd)
  * read each input twice: once for the channel statistics, once to normalize.
- * They process the channels in groups whose inputs take at most `bytes`
- * (default 48 MiB, a third of GB300's L2), so the second read of a group
- * comes from L2.  Sets the budget (0 restores the default) and returns the
- * previous one.  Process-wide; a measurement hook.
+ * With a budget of `bytes` they process the channels in groups whose inputs
+ * take at most that many bytes (a launch pair per group), so that the
+ * second read of a group can come from L2; 0, the default, makes one group
+ * of all channels (measured fastest on GB300).  Returns the previous budget.
+ * Process-wide; a measurement hook.
  */
 size_t nrm_set_bn_group_bytes(size_t bytes);
 

@@ -55,7 +55,10 @@ std::atomic<int> g_force_kind{0}, g_force_threads{0}, g_force_packs{0}, g_force_
     g_force_groups{0};
 std::atomic<unsigned> g_wait_limit{1u << 20};
 std::atomic<int> g_pointer_checks{0};
-std::atomic<size_t> g_bn_group_bytes{(size_t)48 << 20};
+// 0 = no grouping: one group of all channels (measured fastest at both
+// [32, 64, 56, 56] and [64, 64, 112, 112]; smaller groups only added the
+// statistics-to-normalize serialization once per group)
+std::atomic<size_t> g_bn_group_bytes{0};
 thread_local int t_last_kind = 0, t_last_threads = 0, t_last_packs = 0, t_last_stages = 0,
                  t_last_groups = 0;
 
@@ -163,7 +166,8 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
 
     // Automatic choice, from measurements on GB300 (cold L2): rows of up to
     // 1024 packs (8192 bf16 / 4096 fp32 values) run fastest as one CTA per row
-    // with the row in registers (256 threads x 2 packs at 4096 bf16); rows of
+    // with the row in registers (256 threads x 2 packs at 4096 bf16, 128 x 4
+    // for LayerNorm) and the next wave's rows prefetched into L2; rows of
     // up to 2048 packs on persistent CTAs that prefetch the next row (1024 x 2
     // at 16384 bf16); longer rows through the bulk-copy row-group pipeline.
     if (kind == PLAN_AUTO) {
@@ -214,7 +218,10 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     case PLAN_CTA: {
         if (!vec_ok) return NRM_ERR_UNSUPPORTED;
         int packs = fpacks, threads = fthreads;
-        if (!packs) packs = P <= 256 ? 1 : P <= 1024 ? 2 : 4;  // 256 x 2 for 512 packs
+        // 256 x 2 for 512 packs; LayerNorm: 128 x 4 (measured 12.3 us against
+        // 14.0 us for 256 x 2 at 4096 x 4096 bf16: half the per-element share
+        // of its two row-wide sums)
+        if (!packs) packs = P <= 256 ? 1 : (op == OP_LN && P <= 512) ? 4 : P <= 1024 ? 2 : 4;
         if (!threads) {
             threads = round_up_pow2((P + packs - 1) / packs);
             if (threads < 128) threads = 128;
@@ -240,6 +247,8 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.threads = threads;
         p.packs = packs;
         p.smem_params = smem_params ? 1 : 0;
+        p.prefetch = fstages == 0 ? 1 : fstages - 1;  // as the CTA plan
+        p.stages = fstages;
         break;
     }
     case PLAN_PERSIST: {
@@ -603,8 +612,6 @@ unsigned nrm_set_wait_limit(unsigned tries) { return g_wait_limit.exchange(tries
 
 int nrm_set_pointer_checks(int enable) { return g_pointer_checks.exchange(enable ? 1 : 0); }
 
-size_t nrm_set_bn_group_bytes(size_t bytes) {
-    return g_bn_group_bytes.exchange(bytes ? bytes : (size_t)48 << 20);
-}
+size_t nrm_set_bn_group_bytes(size_t bytes) { return g_bn_group_bytes.exchange(bytes); }
 
 }  // extern "C"

@@ -528,13 +528,12 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
 }
 
 // Plan choice (measured on GB300 at [32, 64, 56, 56] binary32: cluster
-// 15.9 us, streaming 17.2 us, scalar 24.3 us).  One cluster of up to 8 CTAs
+// 16.0 us, streaming 17.9 us, scalar 24.3 us).  One cluster of up to 8 CTAs
 // per channel when the channel's planes fit the clusters' shared memory and
 // every channel's cluster can be resident at once (one buffer); when there
 // are more channels than resident clusters, each cluster pipelines its
 // channels through two buffers.  Otherwise the streaming two kernels when
-// the planes are 16-byte aligned and fit one CTA's registers; else the
-// scalar plan.
+// the planes are 16-byte aligned and one unit long; else the scalar plan.
 template <typename T>
 cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     *launched = false;
@@ -596,7 +595,7 @@ template <typename T>
 cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
     BnChunks u = bn_chunks(a.HW / IO<T>::V);
     const int64_t G = bn_group_channels(a.C, a.batch * a.HW * (int64_t)sizeof(T),
-                                        (int64_t)bn_group_bytes());
+                                        bn_group_budget());
     cudaError_t e = cudaSuccess;
     for (int64_t c0 = 0; c0 < a.C && e == cudaSuccess; c0 += G) {
         u.c0 = c0;
@@ -624,7 +623,11 @@ cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int 
             return e;
         }
     }
-    if (stream_ok && (a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_STREAM)) {
+    // automatic choice: the streaming plan only for planes of one unit; longer
+    // planes run faster on the scalar plan's per-plane loops (measured at
+    // [64, 64, 112, 112]: 108 us against 150 us)
+    const bool one_unit = a.HW / V <= kBnChunkPacks;
+    if (stream_ok && ((a.bn_plan == BN_PLAN_AUTO && one_unit) || a.bn_plan == BN_PLAN_STREAM)) {
         *used = PLAN_CTA;
         return launch_bn_stream<T>(a, num_sms, s);
     }

@@ -231,7 +231,7 @@ cudaError_t launch_bn_bwd_t(const BnBwdArgs &a, int num_sms, cudaStream_t s, int
     if (stream_ok) {
         BnChunks u = bn_chunks(a.HW / V);
         const int64_t G = bn_group_channels(a.C, 2 * a.batch * a.HW * (int64_t)sizeof(T),
-                                            (int64_t)bn_group_bytes());
+                                            bn_group_budget());
         cudaError_t e = cudaSuccess;
         for (int64_t c0 = 0; c0 < a.C && e == cudaSuccess; c0 += G) {
             u.c0 = c0;

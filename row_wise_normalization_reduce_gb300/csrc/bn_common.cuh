@@ -139,7 +139,11 @@ inline cudaError_t launch_pdl(K kernel, unsigned grid, unsigned threads, cudaStr
 }
 
 // Input bytes per channel group of the streaming BatchNorm plans (api.cpp;
-// nrm_set_bn_group_bytes).
+// nrm_set_bn_group_bytes), 0 for a single group.
 size_t bn_group_bytes();
+inline int64_t bn_group_budget() {
+    const size_t b = bn_group_bytes();
+    return b == 0 || b > (size_t)INT64_MAX ? INT64_MAX : (int64_t)b;
+}
 
 }  // namespace nrm

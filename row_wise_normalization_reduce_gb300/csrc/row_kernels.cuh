@@ -281,23 +281,33 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
     row_compute<OP, T, PACKS, STRIDE>(a, row, t, red, rx, rr, prm, after_sync);
 }
 
-// Resident threads per SM the CTA and persistent kernels with at most 2
-// packs per thread are compiled for (caps registers at 65536 /
-// NRM_CTA_MIN_THREADS): measured on GB300, 1280 (five 256-thread CTAs per SM,
-// at most 51 registers) keeps the most row loads in flight; 1024 and 1536
-// were slower.  Wider per-thread rows get no cap (they would spill).
+// Resident CTAs per SM the CTA and persistent kernels are compiled for
+// (__launch_bounds__ minimum blocks, which caps registers at 65536 /
+// (CTAs x THREADS)), measured on GB300 with cold L2:
+//  * at most 2 packs per thread: 1280 threads per SM (five 256-thread CTAs,
+//    at most 51 registers) kept the most row loads in flight; 1024 and 1536
+//    were slower;
+//  * LayerNorm with 4 packs per thread: 896 threads (seven 128-thread CTAs,
+//    at most 73 registers): 12.3 us at 4096 x 4096 bf16 against 13.4 us
+//    uncapped (92 registers, five CTAs) and 12.9 / 12.7 us at six / eight;
+//  * anything else is left uncapped (caps made it spill or run slower).
+// NRM_CTA_MIN_THREADS / NRM_LN4_MIN_THREADS override the two caps for
+// experiments.
 #ifndef NRM_CTA_MIN_THREADS
 #define NRM_CTA_MIN_THREADS 1280
 #endif
-#define NRM_MIN_BLOCKS(THREADS, PACKS)                                                   \
-    (((PACKS) <= 2 && NRM_CTA_MIN_THREADS / (THREADS) > 0) ? NRM_CTA_MIN_THREADS / (THREADS) : 1)
+#ifndef NRM_LN4_MIN_THREADS
+#define NRM_LN4_MIN_THREADS 896
+#endif
+template <int OP, int THREADS, int PACKS>
+constexpr int row_min_blocks() {
+    return (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0)                 ? NRM_CTA_MIN_THREADS / THREADS
+           : (OP == OP_LN && PACKS == 4 && NRM_LN4_MIN_THREADS / THREADS > 0) ? NRM_LN4_MIN_THREADS / THREADS
+                                                                              : 1;
+}
 
-// One CTA per row.  With pf > 0, thread 0 first asks L2 to fetch the row
-// that the CTA taking this one's slot pf CTAs later will load (pf = a whole
-// number of waves of resident CTAs): the next waves then find their rows in
-// L2, which keeps HBM streaming without more registers per row in flight.
 template <int OP, typename T, int THREADS, int PACKS>
-__global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
+__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()))
     row_cta_kernel(const RowArgs a, const int64_t pf) {
     constexpr int NW = THREADS / 32;
     __shared__ float s1[2][NW];
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
 // also asks L2 for the row pf_waves rows beyond the one in registers, so the
 // register prefetch of later rows hits L2.
 template <int OP, typename T, int THREADS, int PACKS>
-__global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
+__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()))
     row_persist_kernel(const RowArgs a, const int smem_params, const int pf_waves) {
     constexpr int NW = THREADS / 32;
     extern __shared__ __align__(16) float4 sparams[];
@@ -384,7 +394,8 @@ __global__ void __launch_bounds__(THREADS, NRM_MIN_BLOCKS(THREADS, PACKS))
 // Sized so that an SM keeps well over 100 KB of row loads in flight, which
 // GB300's loaded memory latency needs to stream at HBM speed.
 template <int OP, typename T, int PACKS, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, const int smem_params) {
+__global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, const int smem_params,
+                                                              const int pf_waves) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
@@ -401,8 +412,14 @@ __global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, c
     const T *X = static_cast<const T *>(a.x);
     const T *R = static_cast<const T *>(a.res);
 
+    const int64_t pf = (int64_t)pf_waves * gridDim.x * WARPS;
     for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < a.rows;
          row += (int64_t)gridDim.x * WARPS) {
+        if (pf > 0 && lane == 0 && row + pf < a.rows) {
+            const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+            prefetch_l2_bulk(X + (row + pf) * a.N, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, bytes);
+        }
         const T *xr = X + row * a.N;
         uint4 raw[PACKS];
 #pragma unroll
@@ -718,7 +735,7 @@ cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const int64_t need = (a.rows + WARPS - 1) / WARPS;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = need < slots ? need : slots;
-    kernel<<<(unsigned)grid, WARPS * 32, smem, s>>>(a, p.smem_params);
+    kernel<<<(unsigned)grid, WARPS * 32, smem, s>>>(a, p.smem_params, p.prefetch);
     return cudaGetLastError();
 }
 
@@ -774,7 +791,7 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.threads == TH && p.packs == PK) return launch_cta<OP, T, TH, PK>(a, p, s);
         NRM_CTA_CASE(128, 1) NRM_CTA_CASE(256, 1) NRM_CTA_CASE(512, 1) NRM_CTA_CASE(1024, 1)
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
-        NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)
+        NRM_CTA_CASE(128, 4) NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)
 #undef NRM_CTA_CASE
         return cudaErrorInvalidConfiguration;
     } else if (p.kind == PLAN_WRAW) {
