@@ -64,6 +64,8 @@ def algorithmic_bytes(w: W.Workload, stats: bool = True) -> int:
         return 2 * t + n * es + (rows * 4 if stats else 0)
     if w.op == "add_rms":
         return 4 * t + n * es + (rows * 4 if stats else 0)
+    if w.op == "softmax":  # x, y (the timed call writes no statistics)
+        return 2 * t
     raise ValueError(w.op)
 
 
@@ -240,6 +242,8 @@ class Step:
                        rstd=s["rstd"])
         elif w.op == "rms":
             nrm.rms_fwd(s["x"], p["w"], w.eps, out=s["y"], rstd=s["rstd"])
+        elif w.op == "softmax":
+            nrm.softmax_fwd(s["x"], out=s["y"])
         elif w.op == "bn":
             nrm.bn_fwd_train(s["x"], p["gamma"], p["beta"], p["running_mean"], p["running_var"],
                              w.eps, w.momentum, out=s["y"], save_mean=s["save_mean"],
@@ -448,7 +452,8 @@ def secondary(args, device, stream, l2):
     out = []
     for w in (W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384,
               W.BN_F32_32x64x56x56, W.LN_F32_64x1024, W.BN_INFER_F32_32x64x56x56,
-              W.BN_BWD_F32_32x64x56x56, W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112):
+              W.BN_BWD_F32_32x64x56x56, W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112,
+              W.SOFTMAX_F32_128x4096, W.SOFTMAX_BF16_4096x4096):
         st = Step(w, device, l2)
         k = 2000
         sec, _, _ = time_graphs(st, k, 20, stream)

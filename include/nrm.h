@@ -9,6 +9,7 @@
  *   bn_fwd_train  BatchNorm2d training forward over an NCHW tensor
  *   bn_fwd_infer  BatchNorm2d inference forward (running statistics)
  *   bn_bwd        BatchNorm2d training backward (dx, dgamma, dbeta)
+ *   softmax_fwd   row softmax over a [rows, N] tensor
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -122,6 +123,22 @@ int rms_fwd(const void *x, const void *w, void *y, float *rstd,
 int add_rms_fwd(const void *x, const void *residual, const void *w,
                 void *residual_out, void *y, float *rstd,
                 int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream);
+
+/*
+ * Row softmax over each row of x[rows, N]:
+ *   m = max_j x_j,   d = sum_j exp(x_j - m),   y_i = exp(x_i - m) / d
+ * Definition: LLM-ops page (smarter.xin), section 1 "Softmax", with its
+ * online (max, sum) form and the rule that merges two partial pairs by
+ * rescaling both sums to the larger max; one CTA-wide merge per row.
+ *   x        [rows, N] dtype, read only; -inf entries (masked) give y = 0
+ *   y        [rows, N] dtype, written; must not overlap x
+ *   row_max  [rows] binary32 = m, or NULL
+ *   row_sum  [rows] binary32 = d, or NULL
+ * A row whose entries are all -inf has no defined result (NaN).
+ * Exponentials are binary32 expf; the output is rounded once to its type.
+ */
+int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum,
+                int64_t rows, int64_t N, int dtype, cudaStream_t stream);
 
 /*
  * Bytes of device workspace bn_fwd_train needs for this shape (0 on invalid

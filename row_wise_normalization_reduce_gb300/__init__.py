@@ -1,7 +1,7 @@
 """Row-wise normalization reduce for GB300 (sm_103a).
 
 LayerNorm, RMSNorm, fused residual-add + RMSNorm, BatchNorm2d training
-forward, inference forward and training backward, computed by the
+forward, inference forward and training backward, and row softmax, computed by the
 hand-written CUDA kernels of libnrm.so (C ABI in include/nrm.h).  This
 package is the thin Python binding over that library.
 """
@@ -10,7 +10,7 @@ from ._binding import (  # noqa: F401
     PLAN_PERSIST, PLAN_TMA, PLAN_WRAW, PLAN_WARP, NrmError, add_rms_fwd, bn_bwd,
     bn_bwd_workspace_size, bn_fwd_infer, bn_fwd_train, bn_fwd_train_noalloc,
     bn_fwd_train_workspace_size, device_fault, force_plan, last_plan, lib, ln_fwd, rms_fwd,
-    set_bn_group_bytes, set_pointer_checks, set_wait_limit, status_string)
+    set_bn_group_bytes, set_pointer_checks, set_wait_limit, softmax_fwd, status_string)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -56,6 +56,8 @@ def _declare(lib):
     lib.bn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P,
                            ctypes.c_size_t, _P]
     lib.bn_bwd.restype = _INT
+    lib.softmax_fwd.argtypes = [_P, _P, _P, _P, _I64, _I64, _INT, _P]
+    lib.softmax_fwd.restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
     lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
@@ -244,6 +246,24 @@ def bn_fwd_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_va
             stream if stream is not None else _stream(x.device))
     _check(st, "bn_fwd_train_noalloc")
     return out, save_mean, save_rstd
+
+
+def softmax_fwd(x, *, out=None, row_max=None, row_sum=None, want_stats=False, stream=None):
+    """Softmax over the last dimension of x.  Returns (y, row_max, row_sum);
+    the statistics are None unless requested or passed in."""
+    _cuda(x, "x")
+    rows, n = _rows_view(x)
+    y = torch.empty_like(x) if out is None else out
+    if want_stats:
+        if row_max is None:
+            row_max = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+        if row_sum is None:
+            row_sum = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
+    with torch.cuda.device(x.device):
+        st = lib().softmax_fwd(_ptr(x), _ptr(y), _ptr(row_max), _ptr(row_sum), rows, n,
+                               _dtype_code(x), stream if stream is not None else _stream(x.device))
+    _check(st, "softmax_fwd")
+    return y, row_max, row_sum
 
 
 def _nchw(x):

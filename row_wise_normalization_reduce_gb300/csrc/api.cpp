@@ -325,6 +325,47 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     return NRM_OK;
 }
 
+// Plan choice for the row softmax: one CTA per row with the row in
+// registers while it fits 1024 threads x 4 packs, else the generic plan.
+int choose_softmax_plan(const RowArgs &a, int dtype, const DevInfo &dev, Plan *plan) {
+    const int64_t V = 16 / (int64_t)elem_size(dtype);
+    const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16);
+    const int64_t P = vec_ok ? a.N / V : 0;
+    const int64_t kMaxGrid = 0x7fffffff;
+    int kind = g_force_kind.load(std::memory_order_relaxed);
+    int threads = g_force_threads.load(std::memory_order_relaxed);
+    int packs = g_force_packs.load(std::memory_order_relaxed);
+    const int fstages = g_force_stages.load(std::memory_order_relaxed);
+    if (kind == PLAN_AUTO) {
+        threads = packs = 0;
+        kind = (vec_ok && P <= 4096) ? PLAN_CTA : PLAN_GENERIC;
+    }
+    Plan p{};
+    p.kind = kind;
+    p.sms = dev.sms;
+    p.grid = a.rows < kMaxGrid ? a.rows : kMaxGrid;
+    if (kind == PLAN_GENERIC) {
+        p.threads = threads ? threads : (a.N >= 4096 ? 512 : 256);
+        p.packs = 1;
+    } else if (kind == PLAN_CTA) {
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        if (!threads || !packs) {
+            threads = P <= 128 ? 128 : P <= 256 ? 256 : P <= 512 ? 128 : P <= 1024 ? 256
+                      : P <= 2048 ? 512 : 1024;
+            packs = P <= 256 ? 1 : 4;
+        }
+        if ((int64_t)threads * packs < P) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.prefetch = fstages == 0 ? 1 : fstages - 1;
+        p.stages = fstages;
+    } else {
+        return NRM_ERR_UNSUPPORTED;
+    }
+    *plan = p;
+    return NRM_OK;
+}
+
 int run_row(Op op, RowArgs a, int dtype, cudaStream_t stream) {
     DevInfo dev;
     int st = device_info(&dev);
@@ -334,12 +375,14 @@ int run_row(Op op, RowArgs a, int dtype, cudaStream_t stream) {
     a.fN = (float)a.N;
     a.invN = 1.0f / a.fN;
     Plan plan;
-    st = choose_plan(op, a, dtype, dev, &plan);
+    st = op == OP_SOFTMAX ? choose_softmax_plan(a, dtype, dev, &plan)
+                          : choose_plan(op, a, dtype, dev, &plan);
     if (st != NRM_OK) return st;
     cudaError_t e;
     switch (op) {
     case OP_LN: e = launch_ln(a, plan, dtype, stream); break;
     case OP_RMS: e = launch_rms(a, plan, dtype, stream); break;
+    case OP_SOFTMAX: e = launch_softmax(a, plan, dtype, stream); break;
     default: e = launch_add_rms(a, plan, dtype, stream); break;
     }
     if (e == cudaErrorInvalidConfiguration) {
@@ -445,6 +488,27 @@ int add_rms_fwd(const void *x, const void *residual, const void *w, void *residu
     if ((st = check_pointers({x, residual, w, residual_out, y, rstd})) != NRM_OK) return st;
     RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
     return run_row(OP_ADD_RMS, a, dtype, stream);
+}
+
+int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum, int64_t rows, int64_t N,
+                int dtype, cudaStream_t stream) {
+    size_t tb = 0;
+    int st = validate_rows(rows, N, 0.f, dtype, &tb);
+    if (st != NRM_OK) return st;
+    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
+    if (!x || !y) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({row_max, row_sum}, 4)) != NRM_OK) return st;
+    const Span sx = span(x, tb), sy = span(y, tb), sm = span(row_max, rows * 4),
+               ss = span(row_sum, rows * 4);
+    for (const Span &o : {sy, sm, ss})
+        if (overlap(o, sx)) return NRM_ERR_ALIAS;
+    if (overlap(sy, sm) || overlap(sy, ss) || overlap(sm, ss)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, y, row_max, row_sum})) != NRM_OK) return st;
+    RowArgs a{x, nullptr, nullptr, nullptr, nullptr, y, row_max, row_sum, rows, N, 0.f,
+              nullptr, 0, 0.f, 0.f};
+    return run_row(OP_SOFTMAX, a, dtype, stream);
 }
 
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {

@@ -8,7 +8,7 @@
 
 namespace nrm {
 
-enum Op { OP_LN = 0, OP_RMS = 1, OP_ADD_RMS = 2 };
+enum Op { OP_LN = 0, OP_RMS = 1, OP_ADD_RMS = 2, OP_SOFTMAX = 3 };
 enum DType { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 enum PlanKind {
     PLAN_AUTO = 0,
@@ -41,8 +41,8 @@ struct RowArgs {
     const void *p1;
     void *res_out;        // add+RMS only
     void *y;
-    float *mean;          // LayerNorm only
-    float *rstd;
+    float *mean;          // LayerNorm: row mean; softmax: row max
+    float *rstd;          // norms: 1/sqrt(...); softmax: row sum of exp(x - max)
     int64_t rows;
     int64_t N;
     float eps;
@@ -74,6 +74,8 @@ unsigned *fault_word();
 cudaError_t launch_ln(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 cudaError_t launch_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 cudaError_t launch_add_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
+// Row softmax (softmax.cu): PLAN_CTA (row in registers) or PLAN_GENERIC.
+cudaError_t launch_softmax(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 
 // BatchNorm training forward.  x, gamma, beta, y are stored in the call's
 // dtype; statistics are binary32.  ws holds batch*C float2 partials.

@@ -19,7 +19,7 @@ DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "ln" | "rms" | "add_rms" | "bn" | "bn_infer" | "bn_bwd"
+    op: str                 # "ln" | "rms" | "add_rms" | "bn" | "bn_infer" | "bn_bwd" | "softmax"
     dtype: str              # "f32" | "f16" | "bf16"
     shape: tuple            # [rows, N] or [batch, C, H, W]
     seed: int
@@ -71,9 +71,21 @@ BN_BWD_F32_64x64x112x112 = Workload(
     "bn_bwd_f32_64x64x112x112", "bn_bwd", "f32", (64, 64, 112, 112), seed=9, eps=1e-5,
     note="as bn_bwd_f32_32x64x56x56")
 
+# Softmax: the LLM-ops page's benchmark shape (section 1 table: Batch=128,
+# Seq=4096, binary32), and the 4096 x 4096 bf16 shape of the norm headline
+# for a working set larger than L2.  The page gives no input values; logits
+# are drawn as 4*randn (a spread that exercises the max subtraction).
+SOFTMAX_F32_128x4096 = Workload(
+    "softmax_f32_128x4096", "softmax", "f32", (128, 4096), seed=10, eps=0.0,
+    note="x = 4*randn")
+SOFTMAX_BF16_4096x4096 = Workload(
+    "softmax_bf16_4096x4096", "softmax", "bf16", (4096, 4096), seed=11, eps=0.0,
+    note="x = 4*randn")
+
 ALL = [LN_F32_64x1024, RMS_F16_2048x4096, ADD_RMS_BF16_4096x4096, LN_BF16_1024x16384,
        BN_F32_32x64x56x56, LN_BF16_4096x4096, BN_INFER_F32_32x64x56x56, BN_BWD_F32_32x64x56x56,
-       BN_F32_64x64x112x112, BN_BWD_F32_64x64x112x112]
+       BN_F32_64x64x112x112, BN_BWD_F32_64x64x112x112, SOFTMAX_F32_128x4096,
+       SOFTMAX_BF16_4096x4096]
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -110,6 +122,9 @@ def make_inputs(w: Workload, shape=None, dtype=None) -> dict:
         x = torch.where(mask, x * 20.0, x)
         wgt = 1.0 + 0.05 * randn(n)
         return {"x": x.to(dt), "w": wgt.to(dt)}
+    if w.op == "softmax":
+        rows, n = shape
+        return {"x": (4.0 * randn(rows, n)).to(dt)}
     if w.op == "add_rms":
         rows, n = shape
         x = randn(rows, n)
@@ -154,4 +169,6 @@ def generic_rows(op: str, dtype: str, rows: int, n: int, seed: int, scale=1.0, s
     if op == "add_rms":
         res = (scale * torch.randn(rows, n, generator=g)).to(dt)
         return {"x": x, "residual": res, "w": p1}
+    if op == "softmax":
+        return {"x": x}
     raise ValueError(op)

@@ -42,6 +42,9 @@ def run_gpu(op, inp, eps, momentum=0.1, device="cuda", residual_inplace=False):
     elif op == "bn_bwd":
         dx, dg, db = nrm.bn_bwd(d["dy"], d["x"], d["save_mean"], d["save_rstd"], d.get("gamma"))
         out = {"dx": dx, "dgamma": dg, "dbeta": db}
+    elif op == "softmax":
+        y, m, sm = nrm.softmax_fwd(d["x"], want_stats=True)
+        out = {"y": y, "row_max": m, "row_sum": sm}
     torch.cuda.synchronize()
     return {k: B.torch_to_np(v.cpu()) for k, v in out.items()}
 
@@ -78,6 +81,8 @@ def run_oracle(orc, op, inp, eps, momentum=0.1):
         r["dx"] = r["dx"].reshape(x.shape)
         r["dx_wide"] = r["dx_wide"].reshape(x.shape)
         return r
+    if op == "softmax":
+        return orc.softmax(dt, n["x"], wide=True)
     raise ValueError(op)
 
 
@@ -164,4 +169,10 @@ def compare(op, inp, gpu, ref):
                                    "dx")
         rep["dbeta"] = T.check_stat(gpu["dbeta"], ref["dbeta"], "dbeta", scale=s1)
         rep["dgamma"] = T.check_stat(gpu["dgamma"], ref["dgamma"], "dgamma", scale=s2)
+    elif op == "softmax":
+        rep["y"] = T.check_softmax(dt, gpu["y"], ref["y"], ref["y_wide"])
+        # the max of stored values is exact in any precision
+        assert np.array_equal(gpu["row_max"].astype(np.float64), ref["row_max"]), "row_max"
+        rep["row_sum"] = T.check_stat(gpu["row_sum"], ref["row_sum"], "row_sum",
+                                      scale=np.abs(ref["row_sum"]) * (T.SOFTMAX_REL / T.STAT_REL))
     return rep

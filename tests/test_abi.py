@@ -166,6 +166,21 @@ def test_bn_bwd_validation(lib):
     assert call() in (OK, DEVICE)
 
 
+def test_softmax_validation(lib):
+    rows, n = 4, 64
+    x, y, m, d = A, A * 4, A * 8, A * 9
+    assert lib.softmax_fwd(None, y, None, None, rows, n, 0, None) == NULL
+    assert lib.softmax_fwd(x, None, None, None, rows, n, 0, None) == NULL
+    assert lib.softmax_fwd(None, None, None, None, 0, n, 0, None) == OK   # empty
+    assert lib.softmax_fwd(x, y, None, None, rows, 0, 0, None) == SHAPE
+    assert lib.softmax_fwd(x, y, None, None, rows, n, 4, None) == DTYPE
+    assert lib.softmax_fwd(x, x + 64, None, None, rows, n, 2, None) == ALIAS
+    assert lib.softmax_fwd(x, y, x, None, rows, n, 2, None) == ALIAS
+    assert lib.softmax_fwd(x, y, m, m + 4, rows, n, 2, None) == ALIAS
+    assert lib.softmax_fwd(x + 2, y, None, None, rows, n, 0, None) == VALUE
+    assert lib.softmax_fwd(x, y, m, d, rows, n, 1, None) in (OK, DEVICE)
+
+
 def test_force_plan_api(lib):
     assert lib.nrm_force_plan(99, 0, 0, 0, 0) == UNSUP
     assert lib.nrm_force_plan(-1, 0, 0, 0, 0) == UNSUP

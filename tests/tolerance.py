@@ -21,6 +21,15 @@
   S = |gamma|*rstd*(|dy| + (|s1| + sum|dy|)/cnt + |xhat|*(|s2| + sum|dy*xhat|)/cnt),
   about 5 times that estimate; 16-bit dx may instead be within 1 ulp of the
   oracle rounded.  dbeta, dgamma: |err| <= 1e-5 * sum|dy| and 1e-5 * sum|dy*xhat|.
+* Softmax y = exp(x - m) / d in binary32: each expf is within 2 ulp (CUDA's
+  documented bound), the row sum d carries at most one roundoff per term a
+  thread adds (up to N / 512 = 128 terms in the generic plan at N = 65536)
+  plus two exponentials and an add per merge level (about 9 levels), and the
+  output adds an exponential, a division and a product: at most about 160
+  unit roundoffs (1e-5) in all.  Bound: |err| <= 2e-5 * y + 2^-126 (the
+  absolute part covers results below the normal range); binary16/bfloat16 y
+  within 1 ulp of the oracle rounded; row_max bit-exact (the max of stored
+  values is exact); row_sum relative 2e-5.
 """
 import numpy as np
 
@@ -30,6 +39,7 @@ TOL_F32 = 2e-5
 CANCEL_REL = 2.0 ** -20
 STAT_REL = 1e-5
 BWD_REL = 1e-5
+SOFTMAX_REL = 2e-5
 
 
 def check_y(dt, got, ref_bits, ref_wide, affine_scale=None, what="y"):
@@ -49,7 +59,7 @@ def check_y(dt, got, ref_bits, ref_wide, affine_scale=None, what="y"):
         assert affine_scale is not None, (
             f"{what}: {int(bad.sum())} elements > 1 ulp (max {int(ulps.max())} ulp)")
         bound = CANCEL_REL * affine_scale[bad]
-        over = err[bad] > bound
+        over = ~(err[bad] <= bound)  # NaN fails
         assert not np.any(over), (
             f"{what}: {int(over.sum())} elements > 1 ulp and beyond the cancellation bound; "
             f"worst err {float(np.max(err[bad][over]))}")
@@ -64,7 +74,7 @@ def check_scaled(dt, got, ref_bits, ref_wide, scale, rel, what):
     got = np.asarray(got)
     g64 = B.bits_to_f64(dt, got)
     err = np.abs(g64 - ref_wide)
-    over = err > rel * scale
+    over = ~(err <= rel * scale)  # NaN fails
     if dt != 0 and np.any(over):
         over &= B.ulp_diff(dt, got, ref_bits) > 1
     assert not np.any(over), (
@@ -72,6 +82,24 @@ def check_scaled(dt, got, ref_bits, ref_wide, scale, rel, what):
         f"{float(np.max(err[over] / (rel * scale[over])))}")
     return {"max_abs_err": float(np.max(err)) if err.size else 0.0,
             "max_err_over_scale": float(np.max(err / scale)) if err.size else 0.0}
+
+
+def check_softmax(dt, got, ref_bits, ref_wide, what="y"):
+    got = np.asarray(got)
+    g64 = B.bits_to_f64(dt, got)
+    err = np.abs(g64 - ref_wide)
+    if dt == 0:
+        bound = SOFTMAX_REL * np.abs(ref_wide) + 2.0 ** -126
+        over = ~(err <= bound)  # NaN fails
+        assert not np.any(over), (
+            f"{what}: {int(over.sum())} elements beyond 2e-5 relative; worst "
+            f"{float(np.max(err[over] / bound[over]))} x the bound")
+        return {"max_rel_err": float(np.max(err / np.maximum(np.abs(ref_wide), 2.0 ** -126)))
+                if err.size else 0.0}
+    assert not np.any(np.isnan(g64) & ~np.isnan(ref_wide)), f"{what}: NaN where the oracle has none"
+    ulps = B.ulp_diff(dt, got, ref_bits)
+    assert not np.any(ulps > 1), f"{what}: {int((ulps > 1).sum())} elements > 1 ulp"
+    return {"max_ulp": int(ulps.max()) if ulps.size else 0}
 
 
 def check_stat(got, ref, what, scale=None):
