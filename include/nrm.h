@@ -10,6 +10,8 @@
  *   bn_fwd_infer  BatchNorm2d inference forward (running statistics)
  *   bn_bwd        BatchNorm2d training backward (dx, dgamma, dbeta)
  *   softmax_fwd   row softmax over a [rows, N] tensor
+ *   bn_fwd_partial_stats / bn_fwd_apply_stats, bn_bwd_partial_sums /
+ *   bn_bwd_apply_sums   the local halves of synchronized BatchNorm
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -18,7 +20,8 @@
  *   and keeps no per-call state; it only caches device attributes.  A host
  *   pointer is not detected unless pointer checks are switched on
  *   (nrm_set_pointer_checks); without them it makes the kernel fault.
- * Layout.  Row operators: row-major [rows, N], contiguous (row stride N).
+ * Layout.  Row operators: row-major [rows, N], contiguous (row stride N;
+ *   the *_ld entry points take a row stride per tensor).
  *   BatchNorm: NCHW with H*W flattened to HW; element (n, c, k) at
  *   ((n*C + c)*HW + k).  Parameters (gamma, beta, w) are [N] (rows ops) or
  *   [C] (BatchNorm) in the I/O type; statistics are always binary32.
@@ -123,6 +126,33 @@ int rms_fwd(const void *x, const void *w, void *y, float *rstd,
 int add_rms_fwd(const void *x, const void *residual, const void *w,
                 void *residual_out, void *y, float *rstd,
                 int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream);
+
+/*
+ * The row operators on strided rows: row r of x starts at element r * ldx
+ * (likewise ldr for residual, ldro for residual_out, ldy for y), for views
+ * such as a column slice or a padded buffer (row stride 1028 for N = 1024),
+ * the case the LayerNorm walkthrough (lpnh.cn/news/2756757) lists in §7.
+ * Every ld* >= N; the contiguous entry points above are these with all
+ * strides equal to N.  Vectorised kernels run when every row start is
+ * 16-byte aligned (base pointers aligned and ld * element size a multiple
+ * of 16); otherwise the scalar kernel runs.  Two strided tensors with the
+ * same row stride are tested for overlap exactly (so y may share a padded
+ * buffer with x in other columns); with different strides their outer
+ * bounds are compared.  residual_out == residual in place requires
+ * ldro == ldr.  Other arguments, results and errors as the contiguous
+ * versions; ld < N returns NRM_ERR_SHAPE.
+ */
+int ln_fwd_ld(const void *x, int64_t ldx, const void *gamma, const void *beta, void *y,
+              int64_t ldy, float *mean, float *rstd, int64_t rows, int64_t N, float eps,
+              int dtype, cudaStream_t stream);
+int rms_fwd_ld(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy, float *rstd,
+               int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream);
+int add_rms_fwd_ld(const void *x, int64_t ldx, const void *residual, int64_t ldr,
+                   const void *w, void *residual_out, int64_t ldro, void *y, int64_t ldy,
+                   float *rstd, int64_t rows, int64_t N, float eps, int dtype,
+                   cudaStream_t stream);
+int softmax_fwd_ld(const void *x, int64_t ldx, void *y, int64_t ldy, float *row_max,
+                   float *row_sum, int64_t rows, int64_t N, int dtype, cudaStream_t stream);
 
 /*
  * Row softmax over each row of x[rows, N]:
@@ -248,6 +278,47 @@ int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_m
            const float *save_rstd, void *dx, float *dgamma, float *dbeta,
            int64_t batch, int64_t C, int64_t HW, int dtype, void *workspace,
            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronized BatchNorm over a batch split across processes (BatchNorm CUDA
+ * implementation walkthrough, jianying88.com/news/30214, §7.1: every device
+ * reduces its part, the partial statistics are combined across devices, and
+ * each device normalizes -- and runs the backward -- with the global ones).
+ * The library computes the local parts; the caller exchanges the small
+ * binary64 arrays (an all-gather in rank order) and passes them all back.
+ * With one part these reduce to bn_fwd_train / bn_bwd.
+ *
+ * bn_fwd_partial_stats: stats[3*c + {0,1,2}] = (count, mean, M2) of channel c
+ *   over this process's x[batch, C, HW], binary64, written.  workspace: at
+ *   least batch * C * 8 bytes, 16-byte aligned, scratch.
+ * bn_fwd_apply_stats: parts = nparts arrays as above, concatenated in rank
+ *   order ([nparts][C][3]); they are combined in that order (Chan's pairwise
+ *   rule, binary64), so every process computes the same statistics.  Then as
+ *   bn_fwd_train on the local x: y, save_mean/save_rstd (global mean and
+ *   1/sqrt(var + eps)) and the running statistics (unbiased with the global
+ *   count, which must be at least 2).
+ * bn_bwd_partial_sums: sums[2*c + {0,1}] = (sum dy, sum dy * xhat) of channel
+ *   c over this process's batch, xhat from save_mean/save_rstd (the global
+ *   statistics the forward saved), binary64.  workspace as above.
+ * bn_bwd_apply_sums: parts = [nparts][C][2] in rank order, summed in that
+ *   order; count = the global batch * HW.  Writes dx of the local batch
+ *   (the bn_bwd formula with the global sums and count) and dgamma/dbeta =
+ *   the global sums (binary32), or NULL.
+ */
+int bn_fwd_partial_stats(const void *x, double *stats, int64_t batch, int64_t C, int64_t HW,
+                         int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+int bn_fwd_apply_stats(const void *x, const void *gamma, const void *beta, void *y,
+                       const double *parts, int64_t nparts, float *save_mean, float *save_rstd,
+                       float *running_mean, float *running_var, int64_t batch, int64_t C,
+                       int64_t HW, float eps, float momentum, int dtype, cudaStream_t stream);
+int bn_bwd_partial_sums(const void *dy, const void *x, const float *save_mean,
+                        const float *save_rstd, double *sums, int64_t batch, int64_t C,
+                        int64_t HW, int dtype, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+int bn_bwd_apply_sums(const void *dy, const void *x, const void *gamma, const float *save_mean,
+                      const float *save_rstd, const double *parts, int64_t nparts,
+                      int64_t count, void *dx, float *dgamma, float *dbeta, int64_t batch,
+                      int64_t C, int64_t HW, int dtype, cudaStream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char *nrm_status_string(int status);

@@ -58,6 +58,23 @@ def _declare(lib):
     lib.bn_bwd.restype = _INT
     lib.softmax_fwd.argtypes = [_P, _P, _P, _P, _I64, _I64, _INT, _P]
     lib.softmax_fwd.restype = _INT
+    lib.ln_fwd_ld.argtypes = [_P, _I64, _P, _P, _P, _I64, _P, _P, _I64, _I64, _F, _INT, _P]
+    lib.rms_fwd_ld.argtypes = [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _F, _INT, _P]
+    lib.add_rms_fwd_ld.argtypes = [_P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _P, _I64, _I64,
+                                   _F, _INT, _P]
+    lib.softmax_fwd_ld.argtypes = [_P, _I64, _P, _I64, _P, _P, _I64, _I64, _INT, _P]
+    for f in ("ln_fwd_ld", "rms_fwd_ld", "add_rms_fwd_ld", "softmax_fwd_ld"):
+        getattr(lib, f).restype = _INT
+    lib.bn_fwd_partial_stats.argtypes = [_P, _P, _I64, _I64, _I64, _INT, _P, ctypes.c_size_t, _P]
+    lib.bn_fwd_apply_stats.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64,
+                                       _F, _F, _INT, _P]
+    lib.bn_bwd_partial_sums.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P,
+                                        ctypes.c_size_t, _P]
+    lib.bn_bwd_apply_sums.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I64,
+                                      _I64, _INT, _P]
+    for f in ("bn_fwd_partial_stats", "bn_fwd_apply_stats", "bn_bwd_partial_sums",
+              "bn_bwd_apply_sums"):
+        getattr(lib, f).restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
     lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
@@ -133,39 +150,59 @@ def _rows_view(x: torch.Tensor):
     return x.numel() // n if n else 0, n
 
 
+def _rows(t: torch.Tensor, name: str):
+    """(rows, N, row stride) of a row-operator tensor: contiguous, or 2-D with
+    unit column stride (a column slice or a padded buffer)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    n = t.shape[-1]
+    if t.is_contiguous():
+        return (t.numel() // n if n else 0), n, n
+    if t.dim() == 2 and t.stride(1) == 1 and t.stride(0) >= n:
+        return t.shape[0], n, t.stride(0)
+    raise ValueError(f"{name} must be contiguous, or 2-D with unit column stride")
+
+
+def _same_rows(t, x, name):
+    if t.shape != x.shape or t.dtype != x.dtype or t.device != x.device:
+        raise ValueError(f"{name} must match x in shape, dtype and device")
+    return _rows(t, name)[2]
+
+
 # ---------------------------------------------------------------------------
 # Operators (same names as the C ABI).
 # ---------------------------------------------------------------------------
 def ln_fwd(x, gamma=None, beta=None, eps=1e-5, *, out=None, mean=None, rstd=None,
            want_stats=True, stream=None):
-    """LayerNorm over the last dimension of x.  Returns (y, mean, rstd)."""
-    _cuda(x, "x")
-    rows, n = _rows_view(x)
+    """LayerNorm over the last dimension of x.  Returns (y, mean, rstd).  x
+    (and out) may be 2-D views with a row stride (ln_fwd_ld)."""
+    rows, n, ldx = _rows(x, "x")
     gamma = _param(gamma, n, x.dtype, x.device, "gamma")
     beta = _param(beta, n, x.dtype, x.device, "beta")
-    y = torch.empty_like(x) if out is None else out
+    y = torch.empty(x.shape, device=x.device, dtype=x.dtype) if out is None else out
+    ldy = _same_rows(y, x, "out")
     if want_stats:
         mean = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32) if mean is None else mean
         rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32) if rstd is None else rstd
     with torch.cuda.device(x.device):
-        st = lib().ln_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
-                          rows, n, eps, _dtype_code(x),
-                          stream if stream is not None else _stream(x.device))
+        st = lib().ln_fwd_ld(_ptr(x), ldx, _ptr(gamma), _ptr(beta), _ptr(y), ldy, _ptr(mean),
+                             _ptr(rstd), rows, n, eps, _dtype_code(x),
+                             stream if stream is not None else _stream(x.device))
     _check(st, "ln_fwd")
     return y, mean, rstd
 
 
 def rms_fwd(x, w=None, eps=1e-6, *, out=None, rstd=None, want_stats=False, stream=None):
     """RMSNorm over the last dimension of x.  Returns (y, rstd or None)."""
-    _cuda(x, "x")
-    rows, n = _rows_view(x)
+    rows, n, ldx = _rows(x, "x")
     w = _param(w, n, x.dtype, x.device, "w")
-    y = torch.empty_like(x) if out is None else out
+    y = torch.empty(x.shape, device=x.device, dtype=x.dtype) if out is None else out
+    ldy = _same_rows(y, x, "out")
     if want_stats and rstd is None:
         rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
     with torch.cuda.device(x.device):
-        st = lib().rms_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), rows, n, eps, _dtype_code(x),
-                           stream if stream is not None else _stream(x.device))
+        st = lib().rms_fwd_ld(_ptr(x), ldx, _ptr(w), _ptr(y), ldy, _ptr(rstd), rows, n, eps,
+                              _dtype_code(x), stream if stream is not None else _stream(x.device))
     _check(st, "rms_fwd")
     return y, rstd
 
@@ -175,20 +212,19 @@ def add_rms_fwd(x, residual, w=None, eps=1e-6, *, residual_out=None, out=None, r
     """residual_out = x + residual (rounded to x.dtype); y = RMSNorm(residual_out, w).
     Returns (residual_out, y, rstd or None).  Pass residual_out=residual to update
     the residual stream in place."""
-    _cuda(x, "x")
-    _cuda(residual, "residual")
-    if residual.shape != x.shape or residual.dtype != x.dtype:
-        raise ValueError("residual must match x in shape and dtype")
-    rows, n = _rows_view(x)
+    rows, n, ldx = _rows(x, "x")
+    ldr = _same_rows(residual, x, "residual")
     w = _param(w, n, x.dtype, x.device, "w")
-    ro = torch.empty_like(x) if residual_out is None else residual_out
-    y = torch.empty_like(x) if out is None else out
+    ro = torch.empty(x.shape, device=x.device, dtype=x.dtype) if residual_out is None else residual_out
+    ldro = _same_rows(ro, x, "residual_out")
+    y = torch.empty(x.shape, device=x.device, dtype=x.dtype) if out is None else out
+    ldy = _same_rows(y, x, "out")
     if want_stats and rstd is None:
         rstd = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
     with torch.cuda.device(x.device):
-        st = lib().add_rms_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(ro), _ptr(y), _ptr(rstd),
-                               rows, n, eps, _dtype_code(x),
-                               stream if stream is not None else _stream(x.device))
+        st = lib().add_rms_fwd_ld(_ptr(x), ldx, _ptr(residual), ldr, _ptr(w), _ptr(ro), ldro,
+                                  _ptr(y), ldy, _ptr(rstd), rows, n, eps, _dtype_code(x),
+                                  stream if stream is not None else _stream(x.device))
     _check(st, "add_rms_fwd")
     return ro, y, rstd
 
@@ -251,17 +287,18 @@ def bn_fwd_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_va
 def softmax_fwd(x, *, out=None, row_max=None, row_sum=None, want_stats=False, stream=None):
     """Softmax over the last dimension of x.  Returns (y, row_max, row_sum);
     the statistics are None unless requested or passed in."""
-    _cuda(x, "x")
-    rows, n = _rows_view(x)
-    y = torch.empty_like(x) if out is None else out
+    rows, n, ldx = _rows(x, "x")
+    y = torch.empty(x.shape, device=x.device, dtype=x.dtype) if out is None else out
+    ldy = _same_rows(y, x, "out")
     if want_stats:
         if row_max is None:
             row_max = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
         if row_sum is None:
             row_sum = torch.empty(x.shape[:-1], device=x.device, dtype=torch.float32)
     with torch.cuda.device(x.device):
-        st = lib().softmax_fwd(_ptr(x), _ptr(y), _ptr(row_max), _ptr(row_sum), rows, n,
-                               _dtype_code(x), stream if stream is not None else _stream(x.device))
+        st = lib().softmax_fwd_ld(_ptr(x), ldx, _ptr(y), ldy, _ptr(row_max), _ptr(row_sum),
+                                  rows, n, _dtype_code(x),
+                                  stream if stream is not None else _stream(x.device))
     _check(st, "softmax_fwd")
     return y, row_max, row_sum
 
@@ -329,6 +366,87 @@ def bn_bwd(dy, x, save_mean, save_rstd, gamma=None, *, out=None, dgamma=None, db
                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                           stream if stream is not None else _stream(x.device))
     _check(st, "bn_bwd")
+    return dx, dgamma, dbeta
+
+
+def _scratch(batch, c, device, workspace):
+    need = max(batch * c * 8, 16)
+    if workspace is None:
+        return torch.empty(need, device=device, dtype=torch.uint8)
+    return workspace
+
+
+def bn_fwd_partial_stats(x, *, out=None, workspace=None, stream=None):
+    """Per-channel (count, mean, M2) of this process's batch, [C, 3] float64."""
+    batch, c, hw = _nchw(x)
+    stats = torch.empty(c, 3, device=x.device, dtype=torch.float64) if out is None else out
+    ws = _scratch(batch, c, x.device, workspace)
+    with torch.cuda.device(x.device):
+        st = lib().bn_fwd_partial_stats(_ptr(x), _ptr(stats), batch, c, hw, _dtype_code(x),
+                                        _ptr(ws), ws.numel() * ws.element_size(),
+                                        stream if stream is not None else _stream(x.device))
+    _check(st, "bn_fwd_partial_stats")
+    return stats
+
+
+def bn_fwd_apply_stats(x, parts, gamma=None, beta=None, running_mean=None, running_var=None,
+                       eps=1e-5, momentum=0.1, *, out=None, save_mean=None, save_rstd=None,
+                       stream=None):
+    """Training forward of the local batch from the exchanged [nparts, C, 3]
+    float64 statistics.  Returns (y, save_mean, save_rstd)."""
+    batch, c, hw = _nchw(x)
+    if parts.dtype != torch.float64 or parts.dim() != 3 or parts.shape[1:] != (c, 3):
+        raise ValueError(f"parts must be [nparts, {c}, 3] float64")
+    _cuda(parts, "parts")
+    gamma = _param(gamma, c, x.dtype, x.device, "gamma")
+    beta = _param(beta, c, x.dtype, x.device, "beta")
+    y = torch.empty_like(x) if out is None else out
+    save_mean = torch.empty(c, device=x.device, dtype=torch.float32) if save_mean is None else save_mean
+    save_rstd = torch.empty(c, device=x.device, dtype=torch.float32) if save_rstd is None else save_rstd
+    with torch.cuda.device(x.device):
+        st = lib().bn_fwd_apply_stats(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(parts),
+                                      parts.shape[0], _ptr(save_mean), _ptr(save_rstd),
+                                      _ptr(running_mean), _ptr(running_var), batch, c, hw, eps,
+                                      momentum, _dtype_code(x),
+                                      stream if stream is not None else _stream(x.device))
+    _check(st, "bn_fwd_apply_stats")
+    return y, save_mean, save_rstd
+
+
+def bn_bwd_partial_sums(dy, x, save_mean, save_rstd, *, out=None, workspace=None, stream=None):
+    """Per-channel (sum dy, sum dy * xhat) of this process's batch, [C, 2] float64."""
+    batch, c, hw = _nchw(x)
+    _cuda(dy, "dy")
+    sums = torch.empty(c, 2, device=x.device, dtype=torch.float64) if out is None else out
+    ws = _scratch(batch, c, x.device, workspace)
+    with torch.cuda.device(x.device):
+        st = lib().bn_bwd_partial_sums(_ptr(dy), _ptr(x), _ptr(save_mean), _ptr(save_rstd),
+                                       _ptr(sums), batch, c, hw, _dtype_code(x), _ptr(ws),
+                                       ws.numel() * ws.element_size(),
+                                       stream if stream is not None else _stream(x.device))
+    _check(st, "bn_bwd_partial_sums")
+    return sums
+
+
+def bn_bwd_apply_sums(dy, x, save_mean, save_rstd, parts, count, gamma=None, *, out=None,
+                      dgamma=None, dbeta=None, stream=None):
+    """Backward of the local batch from the exchanged [nparts, C, 2] float64
+    sums and the global count.  Returns (dx, dgamma, dbeta)."""
+    batch, c, hw = _nchw(x)
+    _cuda(dy, "dy")
+    if parts.dtype != torch.float64 or parts.dim() != 3 or parts.shape[1:] != (c, 2):
+        raise ValueError(f"parts must be [nparts, {c}, 2] float64")
+    gamma = _param(gamma, c, x.dtype, x.device, "gamma")
+    dx = torch.empty_like(x) if out is None else out
+    dgamma = torch.empty(c, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    dbeta = torch.empty(c, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    with torch.cuda.device(x.device):
+        st = lib().bn_bwd_apply_sums(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(save_mean),
+                                     _ptr(save_rstd), _ptr(parts), parts.shape[0], count,
+                                     _ptr(dx), _ptr(dgamma), _ptr(dbeta), batch, c, hw,
+                                     _dtype_code(x),
+                                     stream if stream is not None else _stream(x.device))
+    _check(st, "bn_bwd_apply_sums")
     return dx, dgamma, dbeta
 
 

@@ -143,7 +143,9 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     const int64_t V = 16 / (int64_t)elem_size(dtype);
     const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16) &&
                         (!a.res || aligned(a.res, 16)) && (!a.res_out || aligned(a.res_out, 16)) &&
-                        (!a.p0 || aligned(a.p0, 16)) && (!a.p1 || aligned(a.p1, 16));
+                        (!a.p0 || aligned(a.p0, 16)) && (!a.p1 || aligned(a.p1, 16)) &&
+                        a.ldx % V == 0 && a.ldy % V == 0 && (!a.res || a.ldr % V == 0) &&
+                        (!a.res_out || a.ldro % V == 0);
     const int64_t P = vec_ok ? a.N / V : 0;
     const int64_t kMaxGrid = 0x7fffffff;
 
@@ -329,7 +331,8 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
 // registers while it fits 1024 threads x 4 packs, else the generic plan.
 int choose_softmax_plan(const RowArgs &a, int dtype, const DevInfo &dev, Plan *plan) {
     const int64_t V = 16 / (int64_t)elem_size(dtype);
-    const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16);
+    const bool vec_ok = (a.N % V == 0) && aligned(a.x, 16) && aligned(a.y, 16) &&
+                        a.ldx % V == 0 && a.ldy % V == 0;
     const int64_t P = vec_ok ? a.N / V : 0;
     const int64_t kMaxGrid = 0x7fffffff;
     int kind = g_force_kind.load(std::memory_order_relaxed);
@@ -398,16 +401,64 @@ int run_row(Op op, RowArgs a, int dtype, cudaStream_t stream) {
     return NRM_OK;
 }
 
-// Shared validation of the row operators: extents, type, alignment to the
-// element size, eps.  Fills the byte size of one [rows, N] tensor.
-int validate_rows(int64_t rows, int64_t N, float eps, int dtype, size_t *tensor_bytes) {
+// Shared validation of the row operators: extents, type, eps.
+int validate_rows(int64_t rows, int64_t N, float eps, int dtype) {
     if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
     if (rows < 0 || N < 1) return NRM_ERR_SHAPE;
     const size_t es = elem_size(dtype);
     if (rows > 0 && (uint64_t)N > (uint64_t)INT64_MAX / (uint64_t)rows / es) return NRM_ERR_SHAPE;
     if (!eps_ok(eps)) return NRM_ERR_VALUE;
-    *tensor_bytes = (size_t)rows * (size_t)N * es;
     return NRM_OK;
+}
+
+// Row strides: at least N (rows must not overlap) and small enough that the
+// last row's end fits a 64-bit byte offset.
+int validate_ld(int64_t rows, int64_t N, size_t es, std::initializer_list<int64_t> lds) {
+    for (int64_t ld : lds) {
+        if (ld < N) return NRM_ERR_SHAPE;
+        if ((uint64_t)ld > (uint64_t)INT64_MAX / (uint64_t)rows / es) return NRM_ERR_SHAPE;
+    }
+    return NRM_OK;
+}
+
+// A strided 2-D extent in bytes: `rows` rows of `width` bytes, `ld` bytes
+// apart (a contiguous vector is one row).
+struct RSpan {
+    uintptr_t base = 0;
+    int64_t ld = 0, width = 0, rows = 0;
+    bool live() const { return base && width > 0 && rows > 0; }
+    uintptr_t end() const { return base + (uintptr_t)((rows - 1) * ld + width); }
+};
+RSpan rspan(const void *p, int64_t ld_elems, int64_t rows, int64_t width_elems, size_t es) {
+    RSpan s;
+    if (p && rows > 0) {
+        s.base = reinterpret_cast<uintptr_t>(p);
+        s.ld = ld_elems * (int64_t)es;
+        s.width = width_elems * (int64_t)es;
+        s.rows = rows;
+    }
+    return s;
+}
+
+int64_t floor_div(int64_t a, int64_t b) {  // b > 0
+    const int64_t q = a / b;
+    return (a % b != 0 && a < 0) ? q - 1 : q;
+}
+
+// Whether two extents share a byte.  Two extents with the same row stride and
+// row count (columns of one padded buffer, for instance) are tested exactly:
+// rows i of A and j of B meet iff for k = j - i, d + k*ld lies in
+// (-width_b, width_a), d = base_b - base_a.  Anything else is compared by its
+// outer bounds (conservative).
+bool roverlap(const RSpan &a, const RSpan &b) {
+    if (!a.live() || !b.live()) return false;
+    if (!(a.base < b.end() && b.base < a.end())) return false;
+    if (a.rows == 1 || b.rows == 1 || a.ld != b.ld || a.rows != b.rows) return true;
+    const int64_t d = (int64_t)(b.base - a.base);  // two's complement difference
+    const int64_t L = a.ld;
+    int64_t k = floor_div(-b.width - d, L) + 1;    // smallest k with d + k*L > -width_b
+    if (k < -(a.rows - 1)) k = -(a.rows - 1);
+    return k <= a.rows - 1 && d + k * L < a.width;
 }
 
 int check_elem_alignment(std::initializer_list<const void *> ps, size_t es) {
@@ -424,91 +475,121 @@ size_t bn_group_bytes() { return g_bn_group_bytes.load(std::memory_order_relaxed
 
 extern "C" {
 
-int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
-           float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
-    size_t tb = 0;
-    int st = validate_rows(rows, N, eps, dtype, &tb);
+int ln_fwd_ld(const void *x, int64_t ldx, const void *gamma, const void *beta, void *y,
+              int64_t ldy, float *mean, float *rstd, int64_t rows, int64_t N, float eps, int dtype,
+              cudaStream_t stream) {
+    int st = validate_rows(rows, N, eps, dtype);
     if (st != NRM_OK) return st;
     if (rows == 0) return NRM_OK;  // empty input: no pointer is used
     if (!x || !y) return NRM_ERR_NULL;
     const size_t es = elem_size(dtype);
+    if ((st = validate_ld(rows, N, es, {ldx, ldy})) != NRM_OK) return st;
     if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({mean, rstd}, 4)) != NRM_OK) return st;
-    const Span sx = span(x, tb), sy = span(y, tb), sg = span(gamma, N * es),
-               sb = span(beta, N * es), sm = span(mean, rows * 4), sr = span(rstd, rows * 4);
-    for (const Span &o : {sy, sm, sr})
-        for (const Span &i : {sx, sg, sb})
-            if (overlap(o, i)) return NRM_ERR_ALIAS;
-    if (overlap(sy, sm) || overlap(sy, sr) || overlap(sm, sr)) return NRM_ERR_ALIAS;
+    const RSpan sx = rspan(x, ldx, rows, N, es), sy = rspan(y, ldy, rows, N, es),
+                sg = rspan(gamma, N, 1, N, es), sb = rspan(beta, N, 1, N, es),
+                sm = rspan(mean, rows, 1, rows, 4), sr = rspan(rstd, rows, 1, rows, 4);
+    for (const RSpan &o : {sy, sm, sr})
+        for (const RSpan &i : {sx, sg, sb})
+            if (roverlap(o, i)) return NRM_ERR_ALIAS;
+    if (roverlap(sy, sm) || roverlap(sy, sr) || roverlap(sm, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, gamma, beta, y, mean, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
+    RowArgs a{x, nullptr, gamma, beta, nullptr, y, mean, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f,
+              ldx, N, N, ldy};
     return run_row(OP_LN, a, dtype, stream);
+}
+
+int ln_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
+           float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    return ln_fwd_ld(x, N, gamma, beta, y, N, mean, rstd, rows, N, eps, dtype, stream);
+}
+
+int rms_fwd_ld(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy, float *rstd,
+               int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    int st = validate_rows(rows, N, eps, dtype);
+    if (st != NRM_OK) return st;
+    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
+    if (!x || !y) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = validate_ld(rows, N, es, {ldx, ldy})) != NRM_OK) return st;
+    if ((st = check_elem_alignment({x, w, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({rstd}, 4)) != NRM_OK) return st;
+    const RSpan sx = rspan(x, ldx, rows, N, es), sy = rspan(y, ldy, rows, N, es),
+                sw = rspan(w, N, 1, N, es), sr = rspan(rstd, rows, 1, rows, 4);
+    for (const RSpan &o : {sy, sr})
+        for (const RSpan &i : {sx, sw})
+            if (roverlap(o, i)) return NRM_ERR_ALIAS;
+    if (roverlap(sy, sr)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, w, y, rstd})) != NRM_OK) return st;
+    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f,
+              ldx, N, N, ldy};
+    return run_row(OP_RMS, a, dtype, stream);
 }
 
 int rms_fwd(const void *x, const void *w, void *y, float *rstd, int64_t rows, int64_t N,
             float eps, int dtype, cudaStream_t stream) {
-    size_t tb = 0;
-    int st = validate_rows(rows, N, eps, dtype, &tb);
-    if (st != NRM_OK) return st;
-    if (rows == 0) return NRM_OK;  // empty input: no pointer is used
-    if (!x || !y) return NRM_ERR_NULL;
-    const size_t es = elem_size(dtype);
-    if ((st = check_elem_alignment({x, w, y}, es)) != NRM_OK) return st;
-    if ((st = check_elem_alignment({rstd}, 4)) != NRM_OK) return st;
-    const Span sx = span(x, tb), sy = span(y, tb), sw = span(w, N * es), sr = span(rstd, rows * 4);
-    for (const Span &o : {sy, sr})
-        for (const Span &i : {sx, sw})
-            if (overlap(o, i)) return NRM_ERR_ALIAS;
-    if (overlap(sy, sr)) return NRM_ERR_ALIAS;
-    if ((st = check_pointers({x, w, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, nullptr, w, nullptr, nullptr, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
-    return run_row(OP_RMS, a, dtype, stream);
+    return rms_fwd_ld(x, N, w, y, N, rstd, rows, N, eps, dtype, stream);
 }
 
-int add_rms_fwd(const void *x, const void *residual, const void *w, void *residual_out, void *y,
-                float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
-    size_t tb = 0;
-    int st = validate_rows(rows, N, eps, dtype, &tb);
+int add_rms_fwd_ld(const void *x, int64_t ldx, const void *residual, int64_t ldr, const void *w,
+                   void *residual_out, int64_t ldro, void *y, int64_t ldy, float *rstd,
+                   int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    int st = validate_rows(rows, N, eps, dtype);
     if (st != NRM_OK) return st;
     if (rows == 0) return NRM_OK;  // empty input: no pointer is used
     if (!x || !residual || !residual_out || !y) return NRM_ERR_NULL;
     const size_t es = elem_size(dtype);
+    if ((st = validate_ld(rows, N, es, {ldx, ldr, ldro, ldy})) != NRM_OK) return st;
     if ((st = check_elem_alignment({x, residual, w, residual_out, y}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({rstd}, 4)) != NRM_OK) return st;
-    const Span sx = span(x, tb), sres = span(residual, tb), sw = span(w, N * es),
-               sro = span(residual_out, tb), sy = span(y, tb), sr = span(rstd, rows * 4);
-    // residual_out may be exactly residual (in-place residual stream)
-    const bool inplace = residual_out == residual;
-    for (const Span &i : {sx, sw})
-        for (const Span &o : {sro, sy, sr})
-            if (overlap(o, i)) return NRM_ERR_ALIAS;
-    if (!inplace && overlap(sro, sres)) return NRM_ERR_ALIAS;
-    if (overlap(sy, sres) || overlap(sr, sres)) return NRM_ERR_ALIAS;
-    if (overlap(sro, sy) || overlap(sro, sr) || overlap(sy, sr)) return NRM_ERR_ALIAS;
+    const RSpan sx = rspan(x, ldx, rows, N, es), sres = rspan(residual, ldr, rows, N, es),
+                sw = rspan(w, N, 1, N, es), sro = rspan(residual_out, ldro, rows, N, es),
+                sy = rspan(y, ldy, rows, N, es), sr = rspan(rstd, rows, 1, rows, 4);
+    // residual_out may be exactly residual, with the same row stride (the
+    // residual stream updated in place)
+    const bool inplace = residual_out == residual && ldro == ldr;
+    for (const RSpan &i : {sx, sw})
+        for (const RSpan &o : {sro, sy, sr})
+            if (roverlap(o, i)) return NRM_ERR_ALIAS;
+    if (!inplace && roverlap(sro, sres)) return NRM_ERR_ALIAS;
+    if (roverlap(sy, sres) || roverlap(sr, sres)) return NRM_ERR_ALIAS;
+    if (roverlap(sro, sy) || roverlap(sro, sr) || roverlap(sy, sr)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, residual, w, residual_out, y, rstd})) != NRM_OK) return st;
-    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0, 0.f, 0.f};
+    RowArgs a{x, residual, w, nullptr, residual_out, y, nullptr, rstd, rows, N, eps, nullptr, 0,
+              0.f, 0.f, ldx, ldr, ldro, ldy};
     return run_row(OP_ADD_RMS, a, dtype, stream);
 }
 
-int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum, int64_t rows, int64_t N,
-                int dtype, cudaStream_t stream) {
-    size_t tb = 0;
-    int st = validate_rows(rows, N, 0.f, dtype, &tb);
+int add_rms_fwd(const void *x, const void *residual, const void *w, void *residual_out, void *y,
+                float *rstd, int64_t rows, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    return add_rms_fwd_ld(x, N, residual, N, w, residual_out, N, y, N, rstd, rows, N, eps, dtype,
+                          stream);
+}
+
+int softmax_fwd_ld(const void *x, int64_t ldx, void *y, int64_t ldy, float *row_max,
+                   float *row_sum, int64_t rows, int64_t N, int dtype, cudaStream_t stream) {
+    int st = validate_rows(rows, N, 0.f, dtype);
     if (st != NRM_OK) return st;
     if (rows == 0) return NRM_OK;  // empty input: no pointer is used
     if (!x || !y) return NRM_ERR_NULL;
     const size_t es = elem_size(dtype);
+    if ((st = validate_ld(rows, N, es, {ldx, ldy})) != NRM_OK) return st;
     if ((st = check_elem_alignment({x, y}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({row_max, row_sum}, 4)) != NRM_OK) return st;
-    const Span sx = span(x, tb), sy = span(y, tb), sm = span(row_max, rows * 4),
-               ss = span(row_sum, rows * 4);
-    for (const Span &o : {sy, sm, ss})
-        if (overlap(o, sx)) return NRM_ERR_ALIAS;
-    if (overlap(sy, sm) || overlap(sy, ss) || overlap(sm, ss)) return NRM_ERR_ALIAS;
+    const RSpan sx = rspan(x, ldx, rows, N, es), sy = rspan(y, ldy, rows, N, es),
+                sm = rspan(row_max, rows, 1, rows, 4), ss = rspan(row_sum, rows, 1, rows, 4);
+    for (const RSpan &o : {sy, sm, ss})
+        if (roverlap(o, sx)) return NRM_ERR_ALIAS;
+    if (roverlap(sy, sm) || roverlap(sy, ss) || roverlap(sm, ss)) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, y, row_max, row_sum})) != NRM_OK) return st;
     RowArgs a{x, nullptr, nullptr, nullptr, nullptr, y, row_max, row_sum, rows, N, 0.f,
-              nullptr, 0, 0.f, 0.f};
+              nullptr, 0, 0.f, 0.f, ldx, N, N, ldy};
     return run_row(OP_SOFTMAX, a, dtype, stream);
+}
+
+int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum, int64_t rows, int64_t N,
+                int dtype, cudaStream_t stream) {
+    return softmax_fwd_ld(x, N, y, N, row_max, row_sum, rows, N, dtype, stream);
 }
 
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
@@ -632,6 +713,143 @@ int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_m
                 bn_plan_from_forced()};
     int used = 0;
     return record_bn(launch_bn_bwd(a, dtype, dev.sms, stream, &used), used);
+}
+
+// ---------------------------------------------------------------------------
+// Synchronized BatchNorm pieces.
+// ---------------------------------------------------------------------------
+namespace {
+int bn_sync_shape(int64_t batch, int64_t C, int64_t HW, int dtype) {
+    if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
+    if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / 8) return NRM_ERR_SHAPE;
+    return NRM_OK;
+}
+}  // namespace
+
+int bn_fwd_partial_stats(const void *x, double *stats, int64_t batch, int64_t C, int64_t HW,
+                         int dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int st = bn_sync_shape(batch, C, HW, dtype);
+    if (st != NRM_OK) return st;
+    if (!x || !stats) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({stats}, 8)) != NRM_OK) return st;
+    const size_t need = (size_t)batch * (size_t)C * 8;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
+    const Span sx = span(x, (size_t)batch * C * HW * es), ss = span(stats, (size_t)C * 24),
+               sw = span(workspace, need);
+    if (overlap(ss, sx) || overlap(sw, sx) || overlap(ss, sw)) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, stats, workspace})) != NRM_OK) return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnArgs a{x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, batch, C, HW, 0.f,
+             0.f, workspace, nullptr, 0, BN_PLAN_SCALAR};
+    cudaError_t e = launch_bn_plane_stats(a, dtype, dev.sms, stream);
+    if (e == cudaSuccess)
+        e = launch_bn_fold_stats(static_cast<const float2 *>(workspace), x, stats, batch, C, HW,
+                                 dtype, stream);
+    return record_bn(e, PLAN_GENERIC);
+}
+
+int bn_fwd_apply_stats(const void *x, const void *gamma, const void *beta, void *y,
+                       const double *parts, int64_t nparts, float *save_mean, float *save_rstd,
+                       float *running_mean, float *running_var, int64_t batch, int64_t C,
+                       int64_t HW, float eps, float momentum, int dtype, cudaStream_t stream) {
+    int st = bn_sync_shape(batch, C, HW, dtype);
+    if (st != NRM_OK) return st;
+    if (nparts < 1 || (uint64_t)nparts > (uint64_t)INT64_MAX / 24 / (uint64_t)C) return NRM_ERR_SHAPE;
+    if (!eps_ok(eps) || !(momentum >= 0.f && momentum <= 1.f)) return NRM_ERR_VALUE;
+    if (!x || !y || !parts) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({save_mean, save_rstd, running_mean, running_var}, 4)) != NRM_OK)
+        return st;
+    if ((st = check_elem_alignment({parts}, 8)) != NRM_OK) return st;
+    const size_t tb = (size_t)batch * C * HW * es, cb = (size_t)C * 4;
+    const Span outs[] = {span(y, tb), span(save_mean, cb), span(save_rstd, cb),
+                         span(running_mean, cb), span(running_var, cb)};
+    const Span ins[] = {span(x, tb), span(gamma, C * es), span(beta, C * es),
+                        span(parts, (size_t)nparts * C * 24)};
+    for (const Span &o : outs)
+        for (const Span &i : ins)
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    for (int i = 0; i < 5; ++i)
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(outs[i], outs[j])) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({x, gamma, beta, y, parts, save_mean, save_rstd, running_mean,
+                              running_var})) != NRM_OK)
+        return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnSyncArgs a{x, nullptr, gamma, beta, y, nullptr, nullptr, parts, nparts, 0, save_mean,
+                 save_rstd, running_mean, running_var, nullptr, nullptr, batch, C, HW, eps,
+                 momentum};
+    return record_bn(launch_bn_apply_stats(a, dtype, dev.sms, stream), PLAN_GENERIC);
+}
+
+int bn_bwd_partial_sums(const void *dy, const void *x, const float *save_mean,
+                        const float *save_rstd, double *sums, int64_t batch, int64_t C,
+                        int64_t HW, int dtype, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+    int st = bn_sync_shape(batch, C, HW, dtype);
+    if (st != NRM_OK) return st;
+    if (!dy || !x || !save_mean || !save_rstd || !sums) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({dy, x}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({save_mean, save_rstd}, 4)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({sums}, 8)) != NRM_OK) return st;
+    const size_t need = (size_t)batch * (size_t)C * 8;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
+    const size_t tb = (size_t)batch * C * HW * es;
+    const Span outs[] = {span(sums, (size_t)C * 16), span(workspace, need)};
+    const Span ins[] = {span(dy, tb), span(x, tb), span(save_mean, C * 4), span(save_rstd, C * 4)};
+    for (const Span &o : outs)
+        for (const Span &i : ins)
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    if (overlap(outs[0], outs[1])) return NRM_ERR_ALIAS;
+    if ((st = check_pointers({dy, x, save_mean, save_rstd, sums, workspace})) != NRM_OK) return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnBwdArgs a{dy, x, nullptr, save_mean, save_rstd, nullptr, nullptr, nullptr, batch, C, HW,
+                workspace, BN_PLAN_SCALAR};
+    cudaError_t e = launch_bn_bwd_plane_sums(a, dtype, dev.sms, stream);
+    if (e == cudaSuccess)
+        e = launch_bn_fold_sums(static_cast<const float2 *>(workspace), save_rstd, sums, batch, C,
+                                stream);
+    return record_bn(e, PLAN_GENERIC);
+}
+
+int bn_bwd_apply_sums(const void *dy, const void *x, const void *gamma, const float *save_mean,
+                      const float *save_rstd, const double *parts, int64_t nparts, int64_t count,
+                      void *dx, float *dgamma, float *dbeta, int64_t batch, int64_t C, int64_t HW,
+                      int dtype, cudaStream_t stream) {
+    int st = bn_sync_shape(batch, C, HW, dtype);
+    if (st != NRM_OK) return st;
+    if (nparts < 1 || (uint64_t)nparts > (uint64_t)INT64_MAX / 16 / (uint64_t)C) return NRM_ERR_SHAPE;
+    if (count < batch * HW) return NRM_ERR_SHAPE;  // the global count includes this batch
+    if (!dy || !x || !save_mean || !save_rstd || !parts || !dx) return NRM_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if ((st = check_elem_alignment({dy, x, gamma, dx}, es)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({save_mean, save_rstd, dgamma, dbeta}, 4)) != NRM_OK) return st;
+    if ((st = check_elem_alignment({parts}, 8)) != NRM_OK) return st;
+    const size_t tb = (size_t)batch * C * HW * es;
+    const Span outs[] = {span(dx, tb), span(dgamma, C * 4), span(dbeta, C * 4)};
+    const Span ins[] = {span(dy, tb), span(x, tb), span(gamma, C * es), span(save_mean, C * 4),
+                        span(save_rstd, C * 4), span(parts, (size_t)nparts * C * 16)};
+    for (const Span &o : outs)
+        for (const Span &i : ins)
+            if (overlap(o, i)) return NRM_ERR_ALIAS;
+    if (overlap(outs[0], outs[1]) || overlap(outs[0], outs[2]) || overlap(outs[1], outs[2]))
+        return NRM_ERR_ALIAS;
+    if ((st = check_pointers({dy, x, gamma, save_mean, save_rstd, parts, dx, dgamma, dbeta})) !=
+        NRM_OK)
+        return st;
+    DevInfo dev;
+    if ((st = device_info(&dev)) != NRM_OK) return st;
+    BnSyncArgs a{x, dy, gamma, nullptr, dx, save_mean, save_rstd, parts, nparts, count, nullptr,
+                 nullptr, nullptr, nullptr, dgamma, dbeta, batch, C, HW, 0.f, 0.f};
+    return record_bn(launch_bn_apply_sums(a, dtype, dev.sms, stream), PLAN_GENERIC);
 }
 
 const char *nrm_status_string(int status) {

@@ -642,6 +642,17 @@ cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int 
 
 }  // namespace
 
+cudaError_t launch_bn_plane_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s) {
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    switch (dtype) {
+    case DT_F32: bn_partial_kernel<float><<<grid, BN_THREADS, 0, s>>>(a); break;
+    case DT_F16: bn_partial_kernel<__half><<<grid, BN_THREADS, 0, s>>>(a); break;
+    case DT_BF16: bn_partial_kernel<__nv_bfloat16><<<grid, BN_THREADS, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, int *used) {
     switch (dtype) {
     case DT_F32: return launch_bn_train_t<float>(a, num_sms, s, used);

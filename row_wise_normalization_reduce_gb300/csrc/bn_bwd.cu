@@ -252,6 +252,17 @@ cudaError_t launch_bn_bwd_t(const BnBwdArgs &a, int num_sms, cudaStream_t s, int
 
 }  // namespace
 
+cudaError_t launch_bn_bwd_plane_sums(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s) {
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    switch (dtype) {
+    case DT_F32: bn_bwd_partial_kernel<float><<<grid, BB_THREADS, 0, s>>>(a); break;
+    case DT_F16: bn_bwd_partial_kernel<__half><<<grid, BB_THREADS, 0, s>>>(a); break;
+    case DT_BF16: bn_bwd_partial_kernel<__nv_bfloat16><<<grid, BB_THREADS, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bn_bwd(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
                           int *used) {
     switch (dtype) {

@@ -1,0 +1,256 @@
+// bn_sync.cu -- the pieces of synchronized BatchNorm, for a batch split over
+// processes (BatchNorm CUDA implementation walkthrough,
+// jianying88.com/news/30214, §7.1: each device reduces its own part, the
+// partial statistics are combined across devices, then every device
+// normalizes -- and runs the backward -- with the global statistics).
+//
+// Forward:  partial stats  per-channel (count, mean, M2) of the local batch
+//                          in binary64, for the exchange;
+//           apply stats    fold the exchanged [nparts][C] triples in rank
+//                          order (every process gets the same bits),
+//                          normalize the local batch, write save_* and the
+//                          running statistics (global count).
+// Backward: partial sums   per-channel (sum dy, sum dy * xhat) in binary64;
+//           apply sums     fold the exchanged pairs, write dx of the local
+//                          batch and dgamma/dbeta (global sums).
+//
+// The exchange itself (an all-gather of the small binary64 arrays) is the
+// caller's: the library has no communicator.  The local reductions reuse the
+// per-plane stage-1 kernels of bn.cu and bn_bwd.cu; the folds below combine
+// in binary64, where a plain sum over processes loses nothing that matters.
+#include <cmath>
+#include <cstdint>
+
+#include "bn_common.cuh"
+
+namespace nrm {
+
+namespace {
+
+constexpr int BSY_THREADS = 256;
+
+struct DStats {
+    double n, mean, m2;
+};
+
+// Chan's pairwise combine (LLM-ops page, smarter.xin, "Welford combine"),
+// in binary64.  An empty side leaves the other unchanged.
+__device__ __forceinline__ DStats dcombine(const DStats &a, const DStats &b) {
+    const double n = a.n + b.n;
+    if (n == 0.0) return a;
+    const double d = b.mean - a.mean;
+    return DStats{n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * (b.n / n))};
+}
+
+// One warp per channel: fold the batch's per-plane (mean, M2) of d = x - K
+// (K = x[0, c, 0]) in plane order; stats[c] = (count, mean, M2) of x.
+template <typename T>
+__global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *stats, int64_t batch,
+                                     int64_t C, int64_t HW) {
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (c >= C) return;
+    DStats st{0.0, 0.0, 0.0};
+    for (int64_t j = lane; j < batch; j += 32) {
+        const float2 q = ws[c * batch + j];
+        st = dcombine(st, DStats{(double)HW, (double)q.x, (double)q.y});
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const DStats t{__shfl_xor_sync(0xffffffffu, st.n, o), __shfl_xor_sync(0xffffffffu, st.mean, o),
+                       __shfl_xor_sync(0xffffffffu, st.m2, o)};
+        st = lane < (lane ^ o) ? dcombine(st, t) : dcombine(t, st);
+    }
+    if (lane == 0) {
+        const double K = (double)bn_elem<T>(x, c * HW);
+        stats[3 * c + 0] = st.n;
+        stats[3 * c + 1] = K + st.mean;
+        stats[3 * c + 2] = st.m2;
+    }
+}
+
+// One warp per channel: sums[c] = (sum dy, rstd_c * sum dy * (x - mean_c)).
+__global__ void bn_fold_sums_kernel(const float2 *ws, const float *rstd, double *sums,
+                                    int64_t batch, int64_t C) {
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (c >= C) return;
+    double s1 = 0.0, s2 = 0.0;
+    for (int64_t j = lane; j < batch; j += 32) {
+        const float2 q = ws[c * batch + j];
+        s1 += (double)q.x;
+        s2 += (double)q.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const double t1 = __shfl_xor_sync(0xffffffffu, s1, o);
+        const double t2 = __shfl_xor_sync(0xffffffffu, s2, o);
+        s1 = lane < (lane ^ o) ? s1 + t1 : t1 + s1;
+        s2 = lane < (lane ^ o) ? s2 + t2 : t2 + s2;
+    }
+    if (lane == 0) {
+        sums[2 * c + 0] = s1;
+        sums[2 * c + 1] = s2 * (double)rstd[c];
+    }
+}
+
+// Per (n, c) plane: fold the nparts exchanged triples in rank order, then
+// normalize with the shifted mean (K = x[0, c, 0] of this process's batch, so
+// x - K is exact for channels with a large mean).
+template <typename T>
+__global__ void __launch_bounds__(BSY_THREADS) bn_apply_stats_kernel(const BnSyncArgs a) {
+    constexpr int V = IO<T>::V;
+    __shared__ float s_stat[2][3];
+    const int tid = threadIdx.x;
+    const int64_t planes = a.batch * a.C, HW = a.HW;
+    const T *X = static_cast<const T *>(a.x);
+    T *Y = static_cast<T *>(a.out);
+    const bool vec = (HW % V == 0) && bn_aligned16(a.x) && bn_aligned16(a.out);
+    int buf = 0;
+    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, buf ^= 1) {
+        const int64_t n = p / a.C, c = p - n * a.C;
+        const float K = bn_elem<T>(a.x, c * HW);
+        if (tid == 0) {
+            DStats st{0.0, 0.0, 0.0};
+            for (int64_t r = 0; r < a.nparts; ++r) {
+                const double *q = a.parts + 3 * (r * a.C + c);
+                st = dcombine(st, DStats{q[0], q[1], q[2]});
+            }
+            const double var = st.m2 / st.n;
+            const double rstd = 1.0 / sqrt(var + (double)a.eps);
+            s_stat[buf][0] = (float)(st.mean - (double)K);  // shifted mean
+            s_stat[buf][1] = (float)rstd;
+            if (n == 0) {
+                if (a.save_mean) a.save_mean[c] = (float)st.mean;
+                if (a.save_rstd) a.save_rstd[c] = (float)rstd;
+                const double m = (double)a.momentum;
+                if (a.running_mean)
+                    a.running_mean[c] = (float)((1.0 - m) * a.running_mean[c] + m * st.mean);
+                if (a.running_var)
+                    a.running_var[c] =
+                        (float)((1.0 - m) * a.running_var[c] + m * var * st.n / (st.n - 1.0));
+            }
+        }
+        __syncthreads();
+        const float md = s_stat[buf][0], rs = s_stat[buf][1];
+        const float g = bn_param<T>(a.gamma, c, 1.f);
+        const float b = bn_param<T>(a.beta, c, 0.f);
+        const T *xp = X + p * HW;
+        T *yp = Y + p * HW;
+        if (vec) {
+            for (int64_t i = tid; i < HW / V; i += BSY_THREADS) {
+                float f[V], o[V];
+                IO<T>::unpack(ld_stream(xp + V * i), f);
+#pragma unroll
+                for (int j = 0; j < V; ++j) o[j] = fmaf(((f[j] - K) - md) * rs, g, b);
+                st_stream(yp + V * i, IO<T>::pack(o));
+            }
+        } else {
+            for (int64_t i = tid; i < HW; i += BSY_THREADS)
+                yp[i] = IO<T>::from_f(fmaf(((IO<T>::to_f(xp[i]) - K) - md) * rs, g, b));
+        }
+    }
+}
+
+// Per (n, c) plane: fold the nparts exchanged sums in rank order, then
+// dx = gamma * rstd * ((dy - s1/count) - xhat * s2/count).
+template <typename T>
+__global__ void __launch_bounds__(BSY_THREADS) bn_apply_sums_kernel(const BnSyncArgs a) {
+    constexpr int V = IO<T>::V;
+    __shared__ float s_sum[2][2];
+    const int tid = threadIdx.x;
+    const int64_t planes = a.batch * a.C, HW = a.HW;
+    const T *X = static_cast<const T *>(a.x);
+    const T *G = static_cast<const T *>(a.dy);
+    T *D = static_cast<T *>(a.out);
+    const bool vec = (HW % V == 0) && bn_aligned16(a.x) && bn_aligned16(a.dy) &&
+                     bn_aligned16(a.out);
+    int buf = 0;
+    for (int64_t p = blockIdx.x; p < planes; p += gridDim.x, buf ^= 1) {
+        const int64_t n = p / a.C, c = p - n * a.C;
+        if (tid == 0) {
+            double s1 = 0.0, s2 = 0.0;
+            for (int64_t r = 0; r < a.nparts; ++r) {
+                s1 += a.parts[2 * (r * a.C + c) + 0];
+                s2 += a.parts[2 * (r * a.C + c) + 1];
+            }
+            s_sum[buf][0] = (float)(s1 / (double)a.count);
+            s_sum[buf][1] = (float)(s2 / (double)a.count);
+            if (n == 0) {
+                if (a.dbeta) a.dbeta[c] = (float)s1;
+                if (a.dgamma) a.dgamma[c] = (float)s2;
+            }
+        }
+        __syncthreads();
+        const float ma = s_sum[buf][0], mb = s_sum[buf][1];
+        const float mean = a.mean[c], rstd = a.rstd[c];
+        const float gr = bn_param<T>(a.gamma, c, 1.f) * rstd;
+        const T *xp = X + p * HW;
+        const T *gp = G + p * HW;
+        T *dp = D + p * HW;
+        if (vec) {
+            for (int64_t i = tid; i < HW / V; i += BSY_THREADS) {
+                float fx[V], fg[V], o[V];
+                IO<T>::unpack(ld_stream(xp + V * i), fx);
+                IO<T>::unpack(ld_stream(gp + V * i), fg);
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const float xh = (fx[j] - mean) * rstd;
+                    o[j] = gr * fmaf(-xh, mb, fg[j] - ma);
+                }
+                st_stream(dp + V * i, IO<T>::pack(o));
+            }
+        } else {
+            for (int64_t i = tid; i < HW; i += BSY_THREADS) {
+                const float xh = (IO<T>::to_f(xp[i]) - mean) * rstd;
+                dp[i] = IO<T>::from_f(gr * fmaf(-xh, mb, IO<T>::to_f(gp[i]) - ma));
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t batch,
+                                 int64_t C, int64_t HW, int dtype, cudaStream_t s) {
+    const unsigned grid = (unsigned)((C + 7) / 8);  // 8 channels (warps) per CTA
+    switch (dtype) {
+    case DT_F32: bn_fold_stats_kernel<float><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW); break;
+    case DT_F16: bn_fold_stats_kernel<__half><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW); break;
+    case DT_BF16:
+        bn_fold_stats_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW);
+        break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums, int64_t batch,
+                                int64_t C, cudaStream_t s) {
+    bn_fold_sums_kernel<<<(unsigned)((C + 7) / 8), 256, 0, s>>>(ws, rstd, sums, batch, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s) {
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    switch (dtype) {
+    case DT_F32: bn_apply_stats_kernel<float><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_F16: bn_apply_stats_kernel<__half><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_BF16: bn_apply_stats_kernel<__nv_bfloat16><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bn_apply_sums(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s) {
+    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
+    switch (dtype) {
+    case DT_F32: bn_apply_sums_kernel<float><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_F16: bn_apply_sums_kernel<__half><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_BF16: bn_apply_sums_kernel<__nv_bfloat16><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace nrm

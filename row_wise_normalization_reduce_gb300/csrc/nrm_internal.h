@@ -50,6 +50,7 @@ struct RowArgs {
     unsigned wait_limit;  // tries per bounded wait (0: give up at once)
     float fN;             // (float)N, and its correctly rounded reciprocal,
     float invN;           // computed once on the host
+    int64_t ldx, ldr, ldro, ldy;  // row strides (elements) of x, res, res_out, y
 };
 
 struct Plan {
@@ -151,5 +152,35 @@ struct BnBwdArgs {
 };
 cudaError_t launch_bn_bwd(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
                           int *used);
+
+// Stage 1 alone, per (n, c) plane into a.ws (scalar plans, any layout):
+// (mean, M2) of d = x - x[0, c, 0] for the forward; (sum dy, sum dy*(x - mean))
+// for the backward.
+cudaError_t launch_bn_plane_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s);
+cudaError_t launch_bn_bwd_plane_sums(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s);
+
+// Synchronized BatchNorm pieces (bn_sync.cu).
+struct BnSyncArgs {
+    const void *x;       // forward: x; backward: x
+    const void *dy;      // backward only
+    const void *gamma;
+    const void *beta;
+    void *out;           // y or dx
+    const float *mean;   // backward: saved statistics
+    const float *rstd;
+    const double *parts; // [nparts][C][3] (forward) or [nparts][C][2] (backward)
+    int64_t nparts;
+    int64_t count;       // backward: global batch * HW
+    float *save_mean, *save_rstd, *running_mean, *running_var;  // forward outputs
+    float *dgamma, *dbeta;                                       // backward outputs
+    int64_t batch, C, HW;
+    float eps, momentum;
+};
+cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t batch,
+                                 int64_t C, int64_t HW, int dtype, cudaStream_t s);
+cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums, int64_t batch,
+                                int64_t C, cudaStream_t s);
+cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
+cudaError_t launch_bn_apply_sums(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
 
 }  // namespace nrm

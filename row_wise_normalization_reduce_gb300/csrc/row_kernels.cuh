@@ -162,8 +162,8 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
     const int P = (int)(a.N / V);  // 16-byte packs per row (< 2^31 by construction)
     const float fN = a.fN;
     const float invN = a.invN;
-    T *__restrict__ Y = static_cast<T *>(a.y) + row * a.N;
-    T *__restrict__ RO = static_cast<T *>(a.res_out) + row * a.N;
+    T *__restrict__ Y = static_cast<T *>(a.y) + row * a.ldy;
+    T *__restrict__ RO = static_cast<T *>(a.res_out) + row * a.ldro;
 
     // v: the row's values (add+RMS: the rounded residual-stream value)
     float2 v[PACKS][H];
@@ -318,11 +318,11 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
         if (pf > 0 && threadIdx.x == 0 && row + pf < a.rows) {
             const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
-            prefetch_l2_bulk(X + (row + pf) * a.N, bytes);
-            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, bytes);
+            prefetch_l2_bulk(X + (row + pf) * a.ldx, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.ldr, bytes);
         }
         CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
-        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        const GlobalSrc<T> src{X + row * a.ldx, R + row * a.ldr};
         const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
         row_body<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, src, prm, NoHook{});
     }
@@ -357,19 +357,19 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
     uint4 rx[PACKS], rr[PACKS];
     int64_t row = blockIdx.x;
     if (row < a.rows) {
-        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        const GlobalSrc<T> src{X + row * a.ldx, R + row * a.ldr};
         row_load<OP, PACKS, THREADS>(src, threadIdx.x, P, rx, rr);
     }
     int parity = 0;
     for (; row < a.rows; row += G, parity ^= 1) {
         if (pf_waves > 0 && threadIdx.x == 0 && row + pf < a.rows) {
-            prefetch_l2_bulk(X + (row + pf) * a.N, row_bytes);
-            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, row_bytes);
+            prefetch_l2_bulk(X + (row + pf) * a.ldx, row_bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.ldr, row_bytes);
         }
         uint4 nx[PACKS], nr[PACKS];
         const int64_t next = row + G;
         if (next < a.rows) {
-            const GlobalSrc<T> src{X + next * a.N, R + next * a.N};
+            const GlobalSrc<T> src{X + next * a.ldx, R + next * a.ldr};
             row_load<OP, PACKS, THREADS>(src, threadIdx.x, P, nx, nr);
         }
         CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
@@ -417,17 +417,17 @@ __global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, c
          row += (int64_t)gridDim.x * WARPS) {
         if (pf > 0 && lane == 0 && row + pf < a.rows) {
             const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
-            prefetch_l2_bulk(X + (row + pf) * a.N, bytes);
-            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.N, bytes);
+            prefetch_l2_bulk(X + (row + pf) * a.ldx, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + pf) * a.ldr, bytes);
         }
-        const T *xr = X + row * a.N;
+        const T *xr = X + row * a.ldx;
         uint4 raw[PACKS];
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
             if (lane + 32 * k < P) raw[k] = ld_stream(xr + (size_t)(lane + 32 * k) * V);
         if (OP == OP_ADD_RMS) {
-            const T *rr = R + row * a.N;
-            T *RO = static_cast<T *>(a.res_out) + row * a.N;
+            const T *rr = R + row * a.ldr;
+            T *RO = static_cast<T *>(a.res_out) + row * a.ldro;
 #pragma unroll
             for (int k = 0; k < PACKS; ++k) {
                 const int idx = lane + 32 * k;
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, c
             if (lane == 0 && a.rstd) a.rstd[row] = rstd;
         }
         // pass 3: normalize, scale (and shift), round once, store
-        T *Y = static_cast<T *>(a.y) + row * a.N;
+        T *Y = static_cast<T *>(a.y) + row * a.ldy;
         const float2 r2 = f2(rstd), nm = f2(-m0), nc = f2(-c);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(WARPS * 32) row_warp_kernel(const RowArgs a) {
     const T *R = static_cast<const T *>(a.res);
     for (int64_t row = (int64_t)blockIdx.x * WARPS + warp; row < a.rows;
          row += (int64_t)gridDim.x * WARPS) {
-        const GlobalSrc<T> src{X + row * a.N, R + row * a.N};
+        const GlobalSrc<T> src{X + row * a.ldx, R + row * a.ldr};
         const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
         row_body<OP, T, PACKS, 32>(a, row, lane, red, src, prm, NoHook{});
     }
@@ -554,17 +554,17 @@ __global__ void __launch_bounds__(THREADS) row_generic_kernel(const RowArgs a) {
 
     int buf = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, buf ^= 1) {
-        const int64_t base = row * a.N;
-        const float K = (OP == OP_LN) ? io::to_f(X[base]) : 0.f;
+        const int64_t bx = row * a.ldx, br = row * a.ldr, bro = row * a.ldro, by = row * a.ldy;
+        const float K = (OP == OP_LN) ? io::to_f(X[bx]) : 0.f;
         float n = 0.f, mean = 0.f, m2 = 0.f, ss = 0.f;
         for (int64_t i = tid; i < a.N; i += THREADS) {
             float v;
             if (OP == OP_ADD_RMS) {
-                const T r = io::from_f(__fadd_rn(io::to_f(X[base + i]), io::to_f(R[base + i])));
-                RO[base + i] = r;
+                const T r = io::from_f(__fadd_rn(io::to_f(X[bx + i]), io::to_f(R[br + i])));
+                RO[bro + i] = r;
                 v = io::to_f(r);
             } else {
-                v = io::to_f(X[base + i]);
+                v = io::to_f(X[bx + i]);
             }
             if (OP == OP_LN) {
                 const float d = v - K;
@@ -611,14 +611,14 @@ __global__ void __launch_bounds__(THREADS) row_generic_kernel(const RowArgs a) {
             if (OP == OP_LN) {
                 const float g = G ? io::to_f(G[i]) : 1.f;
                 const float b = Bt ? io::to_f(Bt[i]) : 0.f;
-                const float t = (io::to_f(X[base + i]) - K) - shift;
+                const float t = (io::to_f(X[bx + i]) - K) - shift;
                 out = fmaf(t * rstd, g, b);
             } else {
-                const float v = (OP == OP_ADD_RMS) ? io::to_f(RO[base + i]) : io::to_f(X[base + i]);
+                const float v = (OP == OP_ADD_RMS) ? io::to_f(RO[bro + i]) : io::to_f(X[bx + i]);
                 const float w = G ? io::to_f(G[i]) : 1.f;
                 out = (v * rstd) * w;
             }
-            Y[base + i] = io::from_f(out);
+            Y[by + i] = io::from_f(out);
         }
     }
 }

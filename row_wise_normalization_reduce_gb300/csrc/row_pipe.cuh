@@ -42,9 +42,9 @@ __device__ __forceinline__ void pipe_claim(const RowArgs &a, unsigned long long 
         slot_row[s] = r;
         unsigned char *dst = ring + (size_t)s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        bulk_g2s(dst, static_cast<const T *>(a.x) + r * a.N, row_bytes, &full[s]);
+        bulk_g2s(dst, static_cast<const T *>(a.x) + r * a.ldx, row_bytes, &full[s]);
         if (OP == OP_ADD_RMS)
-            bulk_g2s(dst + row_bytes, static_cast<const T *>(a.res) + r * a.N, row_bytes,
+            bulk_g2s(dst + row_bytes, static_cast<const T *>(a.res) + r * a.ldr, row_bytes,
                      &full[s]);
     } else {
         slot_row[s] = -1;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
                     for (int h = 0; h < H; ++h) fx[h] = __fadd2_rn(fx[h], fr[h]);
                     raw[k] = io2::pack(fx);  // round once to T
                     if (valid)
-                        st_stream(static_cast<T *>(a.res_out) + row * a.N + (size_t)idx * V, raw[k]);
+                        st_stream(static_cast<T *>(a.res_out) + row * a.ldro + (size_t)idx * V, raw[k]);
                 }
             }
         }
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
         }
 
         // pass 3: normalize, scale (and shift), round once, store
-        T *Y = static_cast<T *>(a.y) + row * a.N;
+        T *Y = static_cast<T *>(a.y) + row * a.ldy;
         const float2 r2 = f2(rstd), nm = f2(-m0), nc = f2(-c);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {

@@ -19,8 +19,12 @@
 // with the per-element online update to get (m, d), merges, then reads the
 // row again to write y.
 //
-// Exponentials use expf (CUDA documents at most 2 ulp of error); statistics
-// and outputs are binary32 until the single rounding to the output type.
+// Exponentials: expf for binary32 outputs (CUDA documents at most 2 ulp);
+// for binary16/bfloat16 outputs the fast __expf, whose documented error
+// (2 + floor(|1.173 x|) binary32 ulp, below 1e-5 relative wherever exp(x) is
+// a normal binary32) is far inside the 1-ulp tolerance of those types.
+// Statistics and outputs are binary32 until the single rounding to the
+// output type.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -36,15 +40,19 @@ struct MaxSum {
     float m, d;
 };
 
+template <typename T> __device__ __forceinline__ float smx_exp(float x) { return __expf(x); }
+template <> __device__ __forceinline__ float smx_exp<float>(float x) { return expf(x); }
+
 // Merge of two (max, sum) pairs (the rescaling rule above).  A side with no
 // elements (m = -inf, d = 0) leaves the other unchanged; the merge is
 // symmetric in its arguments bit for bit (max and + commute), so butterfly
 // partners agree.
+template <typename T>
 __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
     if (b.m == -INFINITY) return a;
     if (a.m == -INFINITY) return b;
     const float M = fmaxf(a.m, b.m);
-    return MaxSum{M, a.d * expf(a.m - M) + b.d * expf(b.m - M)};
+    return MaxSum{M, a.d * smx_exp<T>(a.m - M) + b.d * smx_exp<T>(b.m - M)};
 }
 
 __device__ __forceinline__ MaxSum ms_shfl_xor(MaxSum v, int o) {
@@ -54,18 +62,18 @@ __device__ __forceinline__ MaxSum ms_shfl_xor(MaxSum v, int o) {
 // CTA-wide merge returned to every thread (same bits everywhere): warp
 // butterfly, one exchange through `slot` (two alternating slots per CTA, as
 // cta_sum_all), then a butterfly over the NW warp results.
-template <int NW>
+template <typename T, int NW>
 __device__ __forceinline__ MaxSum cta_merge_all(MaxSum v, float2 *slot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = ms_merge(v, ms_shfl_xor(v, o));
+    for (int o = 16; o > 0; o >>= 1) v = ms_merge<T>(v, ms_shfl_xor(v, o));
     if (NW == 1) return v;
     if (lane == 0) slot[warp] = make_float2(v.m, v.d);
     __syncthreads();
     const float2 w = slot[lane & (NW - 1)];
     v = MaxSum{w.x, w.y};
 #pragma unroll
-    for (int o = NW / 2; o > 0; o >>= 1) v = ms_merge(v, ms_shfl_xor(v, o));
+    for (int o = NW / 2; o > 0; o >>= 1) v = ms_merge<T>(v, ms_shfl_xor(v, o));
     return v;
 }
 
@@ -85,8 +93,8 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
         if (pf > 0 && t == 0 && row + pf < a.rows)
-            prefetch_l2_bulk(X + (row + pf) * a.N, (uint32_t)(a.N * (int64_t)sizeof(T)));
-        const T *xr = X + row * a.N;
+            prefetch_l2_bulk(X + (row + pf) * a.ldx, (uint32_t)(a.N * (int64_t)sizeof(T)));
+        const T *xr = X + row * a.ldx;
         uint4 raw[PACKS];
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
@@ -112,19 +120,19 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
             if (t + k * THREADS < P) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    v[k][h] = make_float2(expf(v[k][h].x - sh), expf(v[k][h].y - sh));
+                    v[k][h] = make_float2(smx_exp<T>(v[k][h].x - sh), smx_exp<T>(v[k][h].y - sh));
                     dt += v[k][h].x + v[k][h].y;
                 }
             }
         }
-        const MaxSum r = cta_merge_all<NW>(MaxSum{mt, dt}, slot[parity]);
+        const MaxSum r = cta_merge_all<T, NW>(MaxSum{mt, dt}, slot[parity]);
         if (t == 0) {
             if (a.mean) a.mean[row] = r.m;  // row max
             if (a.rstd) a.rstd[row] = r.d;  // row sum of exp(x - max)
         }
-        const float s = (mt == -INFINITY ? 0.f : expf(mt - r.m)) / r.d;
+        const float s = (mt == -INFINITY ? 0.f : smx_exp<T>(mt - r.m)) / r.d;
         const float2 s2 = f2(s);
-        T *Y = static_cast<T *>(a.y) + row * a.N;
+        T *Y = static_cast<T *>(a.y) + row * a.ldy;
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             const int idx = t + k * THREADS;
@@ -149,24 +157,24 @@ __global__ void __launch_bounds__(THREADS) softmax_generic_kernel(const RowArgs 
     T *Y = static_cast<T *>(a.y);
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
-        const int64_t base = row * a.N;
+        const int64_t bx = row * a.ldx, by = row * a.ldy;
         // the online update of the LLM-ops page, one element at a time
         MaxSum st{-INFINITY, 0.f};
         for (int64_t i = threadIdx.x; i < a.N; i += THREADS) {
-            const float x = IO<T>::to_f(X[base + i]);
+            const float x = IO<T>::to_f(X[bx + i]);
             if (x == -INFINITY) continue;
             const float M = fmaxf(st.m, x);
-            st.d = (st.m == -INFINITY ? 0.f : st.d * expf(st.m - M)) + expf(x - M);
+            st.d = (st.m == -INFINITY ? 0.f : st.d * smx_exp<T>(st.m - M)) + smx_exp<T>(x - M);
             st.m = M;
         }
-        const MaxSum r = cta_merge_all<NW>(st, slot[parity]);
+        const MaxSum r = cta_merge_all<T, NW>(st, slot[parity]);
         if (threadIdx.x == 0) {
             if (a.mean) a.mean[row] = r.m;
             if (a.rstd) a.rstd[row] = r.d;
         }
         const float inv = 1.0f / r.d;
         for (int64_t i = threadIdx.x; i < a.N; i += THREADS)
-            Y[base + i] = IO<T>::from_f(expf(IO<T>::to_f(X[base + i]) - r.m) * inv);
+            Y[by + i] = IO<T>::from_f(smx_exp<T>(IO<T>::to_f(X[bx + i]) - r.m) * inv);
     }
 }
 

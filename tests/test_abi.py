@@ -204,3 +204,80 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle." not in text, f
+
+
+def _model_overlap(a, lda, wa, b, ldb, wb, rows):
+    """Byte-level model of the library's overlap rule (exact for equal strides,
+    outer bounds otherwise), for fake addresses."""
+    ea, eb = a + (rows - 1) * lda + wa, b + (rows - 1) * ldb + wb
+    if not (a < eb and b < ea):
+        return False
+    if lda != ldb or rows == 1:
+        return True
+    ra = set()
+    for i in range(rows):
+        ra.update(range(a + i * lda, a + i * lda + wa))
+    return any(any(x in ra for x in range(b + j * ldb, b + j * ldb + wb)) for j in range(rows))
+
+
+def test_sync_bn_validation(lib):
+    b, c, hw = 2, 3, 5
+    x, st, ws, y, parts, dy, dx = A, A * 16, A * 32, A * 48, A * 64, A * 80, A * 96
+    assert lib.bn_fwd_partial_stats(None, st, b, c, hw, 0, ws, 64, None) == NULL
+    assert lib.bn_fwd_partial_stats(x, st, b, c, hw, 0, ws, 8, None) == WS
+    assert lib.bn_fwd_partial_stats(x, st + 4, b, c, hw, 0, ws, 64, None) == VALUE
+    assert lib.bn_fwd_partial_stats(x, x + 8, b, c, hw, 0, ws, 64, None) == ALIAS
+    assert lib.bn_fwd_partial_stats(x, st, b, c, hw, 0, ws, 64, None) in (OK, DEVICE)
+    args = (None, None, None, None, None, None)
+    assert lib.bn_fwd_apply_stats(x, None, None, y, parts, 0, *args[:4], b, c, hw, 1e-5, 0.1, 0,
+                                  None) == SHAPE
+    assert lib.bn_fwd_apply_stats(x, None, None, x, parts, 1, *args[:4], b, c, hw, 1e-5, 0.1, 0,
+                                  None) == ALIAS
+    assert lib.bn_fwd_apply_stats(x, None, None, y, parts, 2, *args[:4], b, c, hw, 1e-5, 2.0, 0,
+                                  None) == VALUE
+    assert lib.bn_fwd_apply_stats(x, None, None, y, parts, 2, *args[:4], b, c, hw, 1e-5, 0.1, 0,
+                                  None) in (OK, DEVICE)
+    assert lib.bn_bwd_partial_sums(dy, x, None, st, parts, b, c, hw, 0, ws, 64, None) == NULL
+    assert lib.bn_bwd_partial_sums(dy, x, st, st + 64, parts, b, c, hw, 0, ws, 64,
+                                   None) in (OK, DEVICE)
+    assert lib.bn_bwd_apply_sums(dy, x, None, st, st + 64, parts, 2, b * hw - 1, dx, None, None,
+                                 b, c, hw, 0, None) == SHAPE
+    assert lib.bn_bwd_apply_sums(dy, x, None, st, st + 64, parts, 2, 2 * b * hw, dy, None, None,
+                                 b, c, hw, 0, None) == ALIAS
+    assert lib.bn_bwd_apply_sums(dy, x, None, st, st + 64, parts, 2, 2 * b * hw, dx, None, None,
+                                 b, c, hw, 0, None) in (OK, DEVICE)
+
+
+def test_strided_alias_rule_matches_byte_model(lib):
+    import random
+    rng = random.Random(5)
+    base = 1 << 20
+    for _ in range(400):
+        rows = rng.randint(1, 5)
+        n = rng.randint(1, 12)
+        ldx = n + rng.randint(0, 12)
+        ldy = ldx if rng.random() < 0.7 else n + rng.randint(0, 12)
+        off = rng.randint(-3 * ldx, 3 * ldx)
+        x = base
+        y = base + 4 * off
+        if y <= 0:
+            continue
+        want = _model_overlap(x, 4 * ldx, 4 * n, y, 4 * ldy, 4 * n, rows)
+        st = lib.rms_fwd_ld(x, ldx, None, y, ldy, None, rows, n, 1e-6, 0, None)
+        assert (st == ALIAS) == want, (rows, n, ldx, ldy, off, st)
+
+
+def test_strided_validation(lib):
+    x, y = A, A * 64
+    assert lib.ln_fwd_ld(x, 7, None, None, y, 8, None, None, 3, 8, 1e-5, 0, None) == SHAPE
+    assert lib.ln_fwd_ld(x, 8, None, None, y, 7, None, None, 3, 8, 1e-5, 0, None) == SHAPE
+    assert lib.softmax_fwd_ld(x, 2 ** 62, y, 8, None, None, 3, 8, 0, None) == SHAPE
+    # y in the columns next to x in one padded buffer: allowed
+    assert lib.ln_fwd_ld(x, 16, None, None, x + 32, 16, None, None, 3, 8, 1e-5, 0, None) in (OK, DEVICE)
+    # ... but not one column further left
+    assert lib.ln_fwd_ld(x, 16, None, None, x + 28, 16, None, None, 3, 8, 1e-5, 0, None) == ALIAS
+    # in-place residual needs the same stride
+    assert lib.add_rms_fwd_ld(x, 8, y, 16, None, y, 12, y + 4096, 8, None, 3, 8, 1e-6, 0,
+                              None) == ALIAS
+    assert lib.add_rms_fwd_ld(x, 8, y, 16, None, y, 16, y + 4096, 8, None, 3, 8, 1e-6, 0,
+                              None) in (OK, DEVICE)
