@@ -448,19 +448,100 @@ def run_reference(args, w, rank, world):
     emit(line)
 
 
+class StridedLnStep:
+    """LayerNorm bf16 4096 x 4096 on a strided view: x is the first 4096
+    columns of [4096, 4160] buffers (row stride 4160), y contiguous."""
+
+    name = "ln_bf16_4096x4096_rowstride4160"
+
+    def __init__(self, device, l2_bytes):
+        import row_wise_normalization_reduce_gb300 as nrm
+        self.nrm = nrm
+        w = W.LN_BF16_4096x4096
+        self.w = w
+        inp = W.make_inputs(w)
+        self.bytes = algorithmic_bytes(w, stats=False)
+        self.nsets = max(2, int(np.ceil(3 * l2_bytes / self.bytes)) + 1)
+        self.g, self.b = inp["gamma"].to(device), inp["beta"].to(device)
+        self.sets = []
+        for _ in range(self.nsets):
+            buf = torch.zeros(4096, 4160, dtype=torch.bfloat16, device=device)
+            buf[:, :4096].copy_(inp["x"].to(device))
+            self.sets.append((buf[:, :4096], torch.empty(4096, 4096, dtype=torch.bfloat16,
+                                                         device=device)))
+        self.i = 0
+        self()
+        torch.cuda.synchronize()
+        self.plan = nrm.PLAN_NAMES.get(nrm.last_plan()[0])
+        self.launches_per_step = 1
+
+    def __call__(self):
+        x, y = self.sets[self.i % self.nsets]
+        self.i += 1
+        self.nrm.ln_fwd(x, self.g, self.b, self.w.eps, out=y, want_stats=False)
+
+
+class SyncBnStep:
+    """Synchronized BatchNorm training forward through its two library halves
+    (partial statistics, then apply with the one part), binary32
+    [32, 64, 56, 56]: the single-process cost of the exchange-ready path."""
+
+    name = "sync_bn_train_f32_32x64x56x56_one_part"
+
+    def __init__(self, device, l2_bytes):
+        import row_wise_normalization_reduce_gb300 as nrm
+        self.nrm = nrm
+        w = W.BN_F32_32x64x56x56
+        self.w = w
+        inp = W.make_inputs(w)
+        self.bytes = algorithmic_bytes(w)
+        self.nsets = max(2, int(np.ceil(3 * l2_bytes / self.bytes)) + 1)
+        self.g, self.b = inp["gamma"].to(device), inp["beta"].to(device)
+        self.rm, self.rv = inp["running_mean"].to(device), inp["running_var"].to(device)
+        self.sets = [(inp["x"].to(device), torch.empty(w.shape, device=device))
+                     for _ in range(self.nsets)]
+        c = w.shape[1]
+        self.parts = torch.empty(1, c, 3, dtype=torch.float64, device=device)
+        self.ws = torch.empty(w.shape[0] * c * 8, dtype=torch.uint8, device=device)
+        self.sm = torch.empty(c, device=device)
+        self.sr = torch.empty(c, device=device)
+        self.i = 0
+        self()
+        torch.cuda.synchronize()
+        self.plan = "partial+apply"
+        self.launches_per_step = 3
+
+    def __call__(self):
+        x, y = self.sets[self.i % self.nsets]
+        self.i += 1
+        self.nrm.bn_fwd_partial_stats(x, out=self.parts[0], workspace=self.ws)
+        self.nrm.bn_fwd_apply_stats(x, self.parts, self.g, self.b, self.rm, self.rv, self.w.eps,
+                                    self.w.momentum, out=y, save_mean=self.sm, save_rstd=self.sr)
+
+
 def secondary(args, device, stream, l2):
+    import dataclasses
+    bn_bf16 = dataclasses.replace(W.BN_F32_32x64x56x56, name="bn_train_bf16_32x64x56x56",
+                                  dtype="bf16")
+    steps = [(w, None) for w in (
+        W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384, W.BN_F32_32x64x56x56,
+        W.LN_F32_64x1024, W.BN_INFER_F32_32x64x56x56, W.BN_BWD_F32_32x64x56x56,
+        W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112, W.SOFTMAX_F32_128x4096,
+        W.SOFTMAX_BF16_4096x4096, bn_bf16)]
+    steps += [(None, StridedLnStep), (None, SyncBnStep)]
     out = []
-    for w in (W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384,
-              W.BN_F32_32x64x56x56, W.LN_F32_64x1024, W.BN_INFER_F32_32x64x56x56,
-              W.BN_BWD_F32_32x64x56x56, W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112,
-              W.SOFTMAX_F32_128x4096, W.SOFTMAX_BF16_4096x4096):
-        st = Step(w, device, l2)
+    for w, cls in steps:
+        if w is not None:
+            st = Step(w, device, l2)
+            name, b = w.name, algorithmic_bytes(w)
+        else:
+            st = cls(device, l2)
+            name, b = st.name, st.bytes
         k = 2000
         sec, _, _ = time_graphs(st, k, 20, stream)
         per = sec / k
-        b = algorithmic_bytes(w)
         peak, _ = measured_peak()
-        out.append({"workload": w.name, "us_per_call": per * 1e6, "gbs": b / per / 1e9,
+        out.append({"workload": name, "us_per_call": per * 1e6, "gbs": b / per / 1e9,
                     "frac_of_measured_peak": b / per / 1e9 / peak,
                     "frac_of_8tbs": b / per / 1e9 / 8000.0, "bytes": b,
                     "launches_per_call": st.launches_per_step, "plan": st.plan})
