@@ -9,14 +9,6 @@
 
 namespace nrm {
 
-// Programmatic dependent launch: the primary grid allows the secondary one to
-// start (launch_dependents); the secondary waits until the primary grid has
-// completed and its memory operations are visible (wait).
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Element i of a tensor stored as T, widened to binary32.
 template <typename T>
 __device__ __forceinline__ float bn_elem(const void *p, int64_t i) {

@@ -162,6 +162,15 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch: the primary grid allows the secondary one to
+// start (launch_dependents); the secondary waits until the primary grid has
+// completed and its memory operations are visible (wait).  Both are no-ops in
+// a kernel launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Reduction engine.
 // ---------------------------------------------------------------------------

@@ -296,6 +296,9 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 #ifndef NRM_CTA_MIN_THREADS
 #define NRM_CTA_MIN_THREADS 1280
 #endif
+#ifndef NRM_ROW_PDL
+#define NRM_ROW_PDL 1
+#endif
 #ifndef NRM_LN4_MIN_THREADS
 #define NRM_LN4_MIN_THREADS 896
 #endif
@@ -314,6 +317,13 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
     __shared__ float2 s2[2][NW];
     const T *X = static_cast<const T *>(a.x);
     const T *R = static_cast<const T *>(a.res);
+#if NRM_ROW_PDL
+    // launched as a programmatic dependent: wait for the previous grid on the
+    // stream (its outputs may be this call's inputs), then let the next one
+    // get its CTAs resident while this grid runs
+    pdl_wait();
+    pdl_launch_dependents();
+#endif
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
         if (pf > 0 && threadIdx.x == 0 && row + pf < a.rows) {
@@ -763,8 +773,22 @@ cudaError_t launch_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
         }
         pf = (int64_t)p.prefetch * p.sms * per_sm;
     }
+#if NRM_ROW_PDL
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, pf);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+#else
     kernel<<<(unsigned)p.grid, THREADS, 0, s>>>(a, pf);
     return cudaGetLastError();
+#endif
 }
 
 template <int OP, typename T>
