@@ -155,6 +155,31 @@ int softmax_fwd_ld(const void *x, int64_t ldx, void *y, int64_t ldy, float *row_
                    float *row_sum, int64_t rows, int64_t N, int dtype, cudaStream_t stream);
 
 /*
+ * add_rms_fwd on tensors in HOST memory (x, residual, residual_out, y; page-
+ * locked memory is fastest), streamed through the device in chunks of rows
+ * (about 4 MB of each tensor per chunk): the host->device copy of chunk k+1,
+ * the kernel of chunk k and the device->host copy of chunk k-1 run at once
+ * (two copy streams of the library and `stream`), so a call costs about the
+ * time of moving its bytes over the host link.  No page describes this
+ * entry point; it is the library's own host-memory path.
+ *   w        [N] dtype, DEVICE memory, or NULL
+ *   rstd     [rows] binary32, DEVICE memory, or NULL
+ *   workspace  device memory, 256-byte aligned, at least
+ *              add_rms_fwd_host_workspace_size(N, dtype) bytes (staging for
+ *              three chunks); calls sharing one workspace must be ordered on
+ *              the GPU (same stream or events).
+ * residual_out may be the same host buffer as residual.  Asynchronous: the
+ * host outputs are complete when `stream` is (e.g. after
+ * cudaStreamSynchronize); the host inputs must stay valid until then.
+ * Returns an nrm_status; a failure after some chunks were enqueued leaves the
+ * outputs undefined.
+ */
+size_t add_rms_fwd_host_workspace_size(int64_t N, int dtype);
+int add_rms_fwd_host(const void *x, const void *residual, const void *w, void *residual_out,
+                     void *y, float *rstd, int64_t rows, int64_t N, float eps, int dtype,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Row softmax over each row of x[rows, N]:
  *   m = max_j x_j,   d = sum_j exp(x_j - m),   y_i = exp(x_i - m) / d
  * Definition: LLM-ops page (smarter.xin), section 1 "Softmax", with its

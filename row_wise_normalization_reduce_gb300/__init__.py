@@ -12,7 +12,8 @@ from ._binding import (  # noqa: F401
     bn_bwd_workspace_size, bn_fwd_infer, bn_fwd_train, bn_fwd_train_noalloc,
     bn_fwd_train_workspace_size, device_fault, force_plan, last_plan, lib, ln_fwd, rms_fwd,
     set_bn_group_bytes, set_pointer_checks, set_wait_limit, softmax_fwd, status_string,
-    bn_fwd_partial_stats, bn_fwd_apply_stats, bn_bwd_partial_sums, bn_bwd_apply_sums)
+    bn_fwd_partial_stats, bn_fwd_apply_stats, bn_bwd_partial_sums, bn_bwd_apply_sums,
+    add_rms_fwd_host, add_rms_fwd_host_workspace)
 from .sync import exchange_parts, global_count, sync_bn_bwd, sync_bn_fwd_train  # noqa: F401
 
 

@@ -75,6 +75,11 @@ def _declare(lib):
     for f in ("bn_fwd_partial_stats", "bn_fwd_apply_stats", "bn_bwd_partial_sums",
               "bn_bwd_apply_sums"):
         getattr(lib, f).restype = _INT
+    lib.add_rms_fwd_host_workspace_size.argtypes = [_I64, _INT]
+    lib.add_rms_fwd_host_workspace_size.restype = ctypes.c_size_t
+    lib.add_rms_fwd_host.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _INT, _P,
+                                     ctypes.c_size_t, _P]
+    lib.add_rms_fwd_host.restype = _INT
     lib.nrm_status_string.argtypes = [_INT]
     lib.nrm_status_string.restype = ctypes.c_char_p
     lib.nrm_force_plan.argtypes = [_INT, _INT, _INT, _INT, _INT]
@@ -227,6 +232,45 @@ def add_rms_fwd(x, residual, w=None, eps=1e-6, *, residual_out=None, out=None, r
                                   stream if stream is not None else _stream(x.device))
     _check(st, "add_rms_fwd")
     return ro, y, rstd
+
+
+def add_rms_fwd_host_workspace(n, dtype, device=None):
+    """Device staging buffer for add_rms_fwd_host on rows of length n."""
+    nbytes = lib().add_rms_fwd_host_workspace_size(n, _DT[dtype])
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                       device=device if device is not None else torch.device("cuda"))
+
+
+def add_rms_fwd_host(x, residual, w=None, eps=1e-6, *, residual_out=None, out=None, rstd=None,
+                     workspace=None, stream=None, synchronize=True):
+    """add_rms_fwd on HOST tensors (pinned memory is fastest), streamed through
+    the current device in chunks.  w and rstd are device tensors.  Returns
+    (residual_out, y); with synchronize=False they are complete only once the
+    stream is."""
+    if x.is_cuda or residual.is_cuda:
+        raise ValueError("x and residual must be host tensors")
+    if not (x.is_contiguous() and residual.is_contiguous()):
+        raise ValueError("x and residual must be contiguous")
+    if residual.shape != x.shape or residual.dtype != x.dtype:
+        raise ValueError("residual must match x in shape and dtype")
+    rows, n = _rows_view(x)
+    device = torch.device("cuda", torch.cuda.current_device())
+    w = _param(w, n, x.dtype, device, "w")
+    ro = torch.empty_like(x) if residual_out is None else residual_out
+    y = torch.empty_like(x) if out is None else out
+    for t, name in ((ro, "residual_out"), (y, "out")):
+        if t.is_cuda or not t.is_contiguous() or t.shape != x.shape or t.dtype != x.dtype:
+            raise ValueError(f"{name} must be a contiguous host tensor like x")
+    ws = add_rms_fwd_host_workspace(n, x.dtype, device) if workspace is None else workspace
+    s = stream if stream is not None else _stream(device)
+    st = lib().add_rms_fwd_host(_ptr(x), _ptr(residual), _ptr(w), _ptr(ro), _ptr(y), _ptr(rstd),
+                                rows, n, eps, _dtype_code(x), _ptr(ws),
+                                ws.numel() * ws.element_size(), s)
+    _check(st, "add_rms_fwd_host")
+    if synchronize:
+        torch.cuda.current_stream(device).synchronize() if stream is None else \
+            torch.cuda.synchronize(device)
+    return ro, y
 
 
 def bn_fwd_train_workspace_size(batch, c, hw, dtype=torch.float32) -> int:

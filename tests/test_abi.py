@@ -248,6 +248,27 @@ def test_sync_bn_validation(lib):
                                  b, c, hw, 0, None) in (OK, DEVICE)
 
 
+def test_host_pipe_validation(lib):
+    rows, n = 8, 64
+    x, r, ro, y = A, A * 2, A * 3, A * 4
+    need = lib.add_rms_fwd_host_workspace_size(n, 2)
+    assert need > 0 and lib.add_rms_fwd_host_workspace_size(0, 2) == 0
+    ws = A * 1024
+    call = lambda **k: lib.add_rms_fwd_host(k.get("x", x), k.get("r", r), None, k.get("ro", ro),
+                                            k.get("y", y), None, k.get("rows", rows), n, 1e-6,
+                                            k.get("dt", 2), k.get("ws", ws), k.get("wsb", need),
+                                            None)
+    assert call(rows=0, x=None) == OK
+    assert call(x=None) == NULL
+    assert call(dt=9) == DTYPE
+    assert call(wsb=need - 1) == WS
+    assert call(ws=ws + 16) == WS                 # not 256-byte aligned
+    assert call(y=x) == ALIAS
+    assert call(ro=r + 64) == ALIAS
+    assert call(ro=r) in (OK, DEVICE)             # in place on the host
+    assert call() in (OK, DEVICE)
+
+
 def test_strided_alias_rule_matches_byte_model(lib):
     import random
     rng = random.Random(5)
