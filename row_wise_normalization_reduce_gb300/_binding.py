@@ -413,8 +413,8 @@ def bn_bwd(dy, x, save_mean, save_rstd, gamma=None, *, out=None, dgamma=None, db
     return dx, dgamma, dbeta
 
 
-def _scratch(batch, c, device, workspace):
-    need = max(batch * c * 8, 16)
+def _scratch(batch, c, hw, dtype, device, workspace):
+    need = max(lib().bn_fwd_train_workspace_size(batch, c, hw, _DT[dtype]), 16)
     if workspace is None:
         return torch.empty(need, device=device, dtype=torch.uint8)
     return workspace
@@ -424,7 +424,7 @@ def bn_fwd_partial_stats(x, *, out=None, workspace=None, stream=None):
     """Per-channel (count, mean, M2) of this process's batch, [C, 3] float64."""
     batch, c, hw = _nchw(x)
     stats = torch.empty(c, 3, device=x.device, dtype=torch.float64) if out is None else out
-    ws = _scratch(batch, c, x.device, workspace)
+    ws = _scratch(batch, c, hw, x.dtype, x.device, workspace)
     with torch.cuda.device(x.device):
         st = lib().bn_fwd_partial_stats(_ptr(x), _ptr(stats), batch, c, hw, _dtype_code(x),
                                         _ptr(ws), ws.numel() * ws.element_size(),
@@ -462,7 +462,7 @@ def bn_bwd_partial_sums(dy, x, save_mean, save_rstd, *, out=None, workspace=None
     batch, c, hw = _nchw(x)
     _cuda(dy, "dy")
     sums = torch.empty(c, 2, device=x.device, dtype=torch.float64) if out is None else out
-    ws = _scratch(batch, c, x.device, workspace)
+    ws = _scratch(batch, c, hw, x.dtype, x.device, workspace)
     with torch.cuda.device(x.device):
         st = lib().bn_bwd_partial_sums(_ptr(dy), _ptr(x), _ptr(save_mean), _ptr(save_rstd),
                                        _ptr(sums), batch, c, hw, _dtype_code(x), _ptr(ws),

@@ -735,7 +735,7 @@ int bn_fwd_partial_stats(const void *x, double *stats, int64_t batch, int64_t C,
     const size_t es = elem_size(dtype);
     if ((st = check_elem_alignment({x}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({stats}, 8)) != NRM_OK) return st;
-    const size_t need = (size_t)batch * (size_t)C * 8;
+    const size_t need = bn_fwd_train_workspace_size(batch, C, HW, dtype);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
     const Span sx = span(x, (size_t)batch * C * HW * es), ss = span(stats, (size_t)C * 24),
                sw = span(workspace, need);
@@ -745,11 +745,24 @@ int bn_fwd_partial_stats(const void *x, double *stats, int64_t batch, int64_t C,
     if ((st = device_info(&dev)) != NRM_OK) return st;
     BnArgs a{x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, batch, C, HW, 0.f,
              0.f, workspace, nullptr, 0, BN_PLAN_SCALAR};
-    cudaError_t e = launch_bn_plane_stats(a, dtype, dev.sms, stream);
-    if (e == cudaSuccess)
-        e = launch_bn_fold_stats(static_cast<const float2 *>(workspace), x, stats, batch, C, HW,
-                                 dtype, stream);
-    return record_bn(e, PLAN_GENERIC);
+    const int64_t V = 16 / (int64_t)es;
+    const float2 *ws = static_cast<const float2 *>(workspace);
+    cudaError_t e;
+    int used;
+    if (HW % V == 0 && aligned(x, 16) && HW / V < kBnUnitPlaneLimit) {
+        int nch = 0, cpk = 0, q = 0;
+        e = launch_bn_unit_stats_host(a, dtype, dev.sms, stream, &nch, &cpk, &q);
+        if (e == cudaSuccess)
+            e = launch_bn_fold_stats(ws, x, stats, batch * nch, C, HW, nch, cpk, q, (int)V, dtype,
+                                     stream);
+        used = PLAN_CTA;
+    } else {
+        e = launch_bn_plane_stats(a, dtype, dev.sms, stream);
+        if (e == cudaSuccess)
+            e = launch_bn_fold_stats(ws, x, stats, batch, C, HW, 1, 0, 0, 0, dtype, stream);
+        used = PLAN_GENERIC;
+    }
+    return record_bn(e, used);
 }
 
 int bn_fwd_apply_stats(const void *x, const void *gamma, const void *beta, void *y,
@@ -799,7 +812,7 @@ int bn_bwd_partial_sums(const void *dy, const void *x, const float *save_mean,
     if ((st = check_elem_alignment({dy, x}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({save_mean, save_rstd}, 4)) != NRM_OK) return st;
     if ((st = check_elem_alignment({sums}, 8)) != NRM_OK) return st;
-    const size_t need = (size_t)batch * (size_t)C * 8;
+    const size_t need = bn_bwd_workspace_size(batch, C, HW, dtype);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
     const size_t tb = (size_t)batch * C * HW * es;
     const Span outs[] = {span(sums, (size_t)C * 16), span(workspace, need)};
@@ -813,11 +826,21 @@ int bn_bwd_partial_sums(const void *dy, const void *x, const float *save_mean,
     if ((st = device_info(&dev)) != NRM_OK) return st;
     BnBwdArgs a{dy, x, nullptr, save_mean, save_rstd, nullptr, nullptr, nullptr, batch, C, HW,
                 workspace, BN_PLAN_SCALAR};
-    cudaError_t e = launch_bn_bwd_plane_sums(a, dtype, dev.sms, stream);
-    if (e == cudaSuccess)
-        e = launch_bn_fold_sums(static_cast<const float2 *>(workspace), save_rstd, sums, batch, C,
-                                stream);
-    return record_bn(e, PLAN_GENERIC);
+    const int64_t V = 16 / (int64_t)es;
+    const float2 *ws = static_cast<const float2 *>(workspace);
+    cudaError_t e;
+    int used;
+    if (HW % V == 0 && aligned(x, 16) && aligned(dy, 16) && HW / V < kBnUnitPlaneLimit) {
+        int nch = 0;
+        e = launch_bn_bwd_unit_sums_host(a, dtype, dev.sms, stream, &nch);
+        if (e == cudaSuccess) e = launch_bn_fold_sums(ws, save_rstd, sums, batch * nch, C, stream);
+        used = PLAN_CTA;
+    } else {
+        e = launch_bn_bwd_plane_sums(a, dtype, dev.sms, stream);
+        if (e == cudaSuccess) e = launch_bn_fold_sums(ws, save_rstd, sums, batch, C, stream);
+        used = PLAN_GENERIC;
+    }
+    return record_bn(e, used);
 }
 
 int bn_bwd_apply_sums(const void *dy, const void *x, const void *gamma, const float *save_mean,

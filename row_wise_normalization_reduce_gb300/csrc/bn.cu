@@ -642,6 +642,22 @@ cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int 
 
 }  // namespace
 
+cudaError_t launch_bn_unit_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s,
+                                 BnChunks *u) {
+    const int V = dtype == DT_F32 ? 4 : 8;
+    *u = bn_chunks(a.HW / V);
+    u->c0 = 0;
+    u->G = a.C;
+    const unsigned grid = bn_grid(a.batch * a.C * u->nch, num_sms);
+    switch (dtype) {
+    case DT_F32: bn_stats_kernel<float><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
+    case DT_F16: bn_stats_kernel<__half><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
+    case DT_BF16: bn_stats_kernel<__nv_bfloat16><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bn_plane_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s) {
     const unsigned grid = bn_grid(a.batch * a.C, num_sms);
     switch (dtype) {

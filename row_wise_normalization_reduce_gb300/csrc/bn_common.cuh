@@ -60,7 +60,7 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
 constexpr int BNS_THREADS = 256;
 constexpr int BNS_PACKS = 4;
 static_assert(BNS_THREADS * BNS_PACKS == kBnChunkPacks, "a CTA holds one unit in registers");
-constexpr int64_t kBnMaxPlanePacks = (int64_t)1 << 20;  // chunking exact below this
+constexpr int64_t kBnMaxPlanePacks = kBnUnitPlaneLimit;  // chunking exact below this
 
 struct BnChunks {
     int64_t c0, G;  // channel group
@@ -129,6 +129,14 @@ inline cudaError_t launch_pdl(K kernel, unsigned grid, unsigned threads, cudaStr
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
+
+// Stage 1 of the streaming plans alone over all channels (synchronized
+// BatchNorm): per-unit partials into a.ws, the unit layout in *u.  The
+// planes must be 16-byte aligned and a whole number of packs.
+cudaError_t launch_bn_unit_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s,
+                                 BnChunks *u);
+cudaError_t launch_bn_bwd_unit_sums(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
+                                    BnChunks *u);
 
 // Input bytes per channel group of the streaming BatchNorm plans (api.cpp;
 // nrm_set_bn_group_bytes), 0 for a single group.

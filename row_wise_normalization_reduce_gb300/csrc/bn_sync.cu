@@ -16,8 +16,11 @@
 //
 // The exchange itself (an all-gather of the small binary64 arrays) is the
 // caller's: the library has no communicator.  The local reductions reuse the
-// per-plane stage-1 kernels of bn.cu and bn_bwd.cu; the folds below combine
-// in binary64, where a plain sum over processes loses nothing that matters.
+// stage-1 kernels of bn.cu and bn_bwd.cu (per unit of at most 1024 packs when
+// the planes are 16-byte aligned packs, per plane otherwise); the folds below
+// combine in binary64.  The apply kernels walk the tensor as one flat array
+// of packs (as the inference kernel) with a per-channel table every CTA folds
+// from the exchanged parts; per-plane kernels cover the other layouts.
 #include <cmath>
 #include <cstdint>
 
@@ -42,18 +45,24 @@ __device__ __forceinline__ DStats dcombine(const DStats &a, const DStats &b) {
     return DStats{n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * (b.n / n))};
 }
 
-// One warp per channel: fold the batch's per-plane (mean, M2) of d = x - K
-// (K = x[0, c, 0]) in plane order; stats[c] = (count, mean, M2) of x.
+// One warp per channel: fold the channel's `per_channel` partials (mean, M2)
+// of d = x - K (K = x[0, c, 0]) in order; stats[c] = (count, mean, M2) of x.
+// Partial j covers count(j) values: HW for per-plane partials; for per-unit
+// partials (chunks of at most cpk packs of V values) min(cpk, q - k*cpk) * V,
+// k = j mod nch.
 template <typename T>
-__global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *stats, int64_t batch,
-                                     int64_t C, int64_t HW) {
+__global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *stats,
+                                     int64_t per_channel, int64_t C, int64_t HW, int nch, int cpk,
+                                     int q, int V) {
     const int lane = threadIdx.x & 31;
     const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (c >= C) return;
     DStats st{0.0, 0.0, 0.0};
-    for (int64_t j = lane; j < batch; j += 32) {
-        const float2 q = ws[c * batch + j];
-        st = dcombine(st, DStats{(double)HW, (double)q.x, (double)q.y});
+    for (int64_t j = lane; j < per_channel; j += 32) {
+        const float2 p = ws[c * per_channel + j];
+        const int k = (int)(j % nch);
+        const double n = V ? (double)(min(cpk, q - k * cpk) * V) : (double)HW;
+        st = dcombine(st, DStats{n, (double)p.x, (double)p.y});
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -69,15 +78,16 @@ __global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *st
     }
 }
 
-// One warp per channel: sums[c] = (sum dy, rstd_c * sum dy * (x - mean_c)).
+// One warp per channel: sums[c] = (sum dy, rstd_c * sum dy * (x - mean_c))
+// over the channel's `per_channel` partials.
 __global__ void bn_fold_sums_kernel(const float2 *ws, const float *rstd, double *sums,
-                                    int64_t batch, int64_t C) {
+                                    int64_t per_channel, int64_t C) {
     const int lane = threadIdx.x & 31;
     const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (c >= C) return;
     double s1 = 0.0, s2 = 0.0;
-    for (int64_t j = lane; j < batch; j += 32) {
-        const float2 q = ws[c * batch + j];
+    for (int64_t j = lane; j < per_channel; j += 32) {
+        const float2 q = ws[c * per_channel + j];
         s1 += (double)q.x;
         s2 += (double)q.y;
     }
@@ -209,48 +219,239 @@ __global__ void __launch_bounds__(BSY_THREADS) bn_apply_sums_kernel(const BnSync
     }
 }
 
+// ---------------------------------------------------------------------------
+// Flat apply kernels (16-byte packs, C <= kSyncTable): the tensor as one
+// array of packs over a resident grid, as the inference kernel; every CTA
+// first folds the exchanged parts of all channels into a shared-memory table
+// (CTA 0 also writes the per-channel outputs).
+// ---------------------------------------------------------------------------
+constexpr int kSyncTable = 2048;
+constexpr int BSY_PACKS = 4;  // packs in flight per thread
+
+template <typename T>
+__global__ void __launch_bounds__(BSY_THREADS) bn_apply_stats_flat_kernel(const BnSyncArgs a,
+                                                                          const uint32_t total,
+                                                                          const FastDiv per_plane,
+                                                                          const FastDiv channels) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
+    extern __shared__ float4 tab[];  // [C] {mean_hi, mean_lo, rstd, gamma}, then [C] beta
+    float *tb = reinterpret_cast<float *>(tab + a.C);
+    for (int64_t c = threadIdx.x; c < a.C; c += BSY_THREADS) {
+        DStats st{0.0, 0.0, 0.0};
+        for (int64_t r = 0; r < a.nparts; ++r) {
+            const double *q = a.parts + 3 * (r * a.C + c);
+            st = dcombine(st, DStats{q[0], q[1], q[2]});
+        }
+        const double var = st.m2 / st.n;
+        const double rstd = 1.0 / sqrt(var + (double)a.eps);
+        const float hi = (float)st.mean;
+        // the mean as hi + lo: (x - hi) - lo keeps x - mean exact-ish for
+        // channels with a large mean
+        tab[c] = make_float4(hi, (float)(st.mean - (double)hi), (float)rstd,
+                             bn_param<T>(a.gamma, c, 1.f));
+        tb[c] = bn_param<T>(a.beta, c, 0.f);
+        if (blockIdx.x == 0) {
+            if (a.save_mean) a.save_mean[c] = hi;
+            if (a.save_rstd) a.save_rstd[c] = (float)rstd;
+            const double m = (double)a.momentum;
+            if (a.running_mean)
+                a.running_mean[c] = (float)((1.0 - m) * a.running_mean[c] + m * st.mean);
+            if (a.running_var)
+                a.running_var[c] = (float)((1.0 - m) * a.running_var[c] + m * var * st.n / (st.n - 1.0));
+        }
+    }
+    __syncthreads();
+    const uint4 *X = static_cast<const uint4 *>(a.x);
+    uint4 *Y = static_cast<uint4 *>(a.out);
+    const uint32_t stride = gridDim.x * BSY_THREADS;
+    for (uint32_t base = blockIdx.x * BSY_THREADS + threadIdx.x; base < total;
+         base += stride * BSY_PACKS) {
+        uint4 v[BSY_PACKS];
+#pragma unroll
+        for (int j = 0; j < BSY_PACKS; ++j)
+            if (base + j * stride < total) v[j] = ld_stream(X + base + j * stride);
+#pragma unroll
+        for (int j = 0; j < BSY_PACKS; ++j) {
+            const uint32_t i = base + j * stride;
+            if (i < total) {
+                const uint32_t plane = fast_div(i, per_plane);
+                const uint32_t c = plane - fast_div(plane, channels) * channels.d;
+                const float4 k = tab[c];
+                const float2 nh = f2(-k.x), nl = f2(-k.y), r2 = f2(k.z), g2 = f2(k.w),
+                             b2 = f2(tb[c]);
+                float2 f[H], o[H];
+                io2::unpack(v[j], f);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nh), nl), r2), g2, b2);
+                st_stream(Y + i, io2::pack(o));
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(BSY_THREADS) bn_apply_sums_flat_kernel(const BnSyncArgs a,
+                                                                         const uint32_t total,
+                                                                         const FastDiv per_plane,
+                                                                         const FastDiv channels) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
+    extern __shared__ float4 tab[];  // [C] {mean, rstd, gamma*rstd, s1/count}, then [C] s2/count
+    float *tb = reinterpret_cast<float *>(tab + a.C);
+    for (int64_t c = threadIdx.x; c < a.C; c += BSY_THREADS) {
+        double s1 = 0.0, s2 = 0.0;
+        for (int64_t r = 0; r < a.nparts; ++r) {
+            s1 += a.parts[2 * (r * a.C + c) + 0];
+            s2 += a.parts[2 * (r * a.C + c) + 1];
+        }
+        const float rstd = a.rstd[c];
+        tab[c] = make_float4(a.mean[c], rstd, bn_param<T>(a.gamma, c, 1.f) * rstd,
+                             (float)(s1 / (double)a.count));
+        tb[c] = (float)(s2 / (double)a.count);
+        if (blockIdx.x == 0) {
+            if (a.dbeta) a.dbeta[c] = (float)s1;
+            if (a.dgamma) a.dgamma[c] = (float)s2;
+        }
+    }
+    __syncthreads();
+    const uint4 *X = static_cast<const uint4 *>(a.x);
+    const uint4 *G = static_cast<const uint4 *>(a.dy);
+    uint4 *D = static_cast<uint4 *>(a.out);
+    const uint32_t stride = gridDim.x * BSY_THREADS;
+    for (uint32_t base = blockIdx.x * BSY_THREADS + threadIdx.x; base < total;
+         base += stride * BSY_PACKS) {
+        uint4 vx[BSY_PACKS], vg[BSY_PACKS];
+#pragma unroll
+        for (int j = 0; j < BSY_PACKS; ++j)
+            if (base + j * stride < total) {
+                vx[j] = ld_stream(X + base + j * stride);
+                vg[j] = ld_stream(G + base + j * stride);
+            }
+#pragma unroll
+        for (int j = 0; j < BSY_PACKS; ++j) {
+            const uint32_t i = base + j * stride;
+            if (i < total) {
+                const uint32_t plane = fast_div(i, per_plane);
+                const uint32_t c = plane - fast_div(plane, channels) * channels.d;
+                const float4 k = tab[c];
+                const float2 nm = f2(-k.x), r2 = f2(k.y), gr = f2(k.z), na = f2(-k.w),
+                             nb = f2(-tb[c]);
+                float2 fx[H], fg[H], o[H];
+                io2::unpack(vx[j], fx);
+                io2::unpack(vg[j], fg);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 xh = __fmul2_rn(__fadd2_rn(fx[h], nm), r2);
+                    o[h] = __fmul2_rn(gr, __ffma2_rn(xh, nb, __fadd2_rn(fg[h], na)));
+                }
+                st_stream(D + i, io2::pack(o));
+            }
+        }
+    }
+}
+
+// The flat plans' launch: HW a whole number of packs, 16-byte aligned
+// tensors, a table that fits, pack indices within 32 bits.
+template <typename T>
+bool bn_flat_ok(const BnSyncArgs &a, bool bwd) {
+    constexpr int V = IO<T>::V;
+    const int64_t total = a.batch * a.C * (a.HW / V);
+    // pack indices, and the loop's base + BSY_PACKS strides, stay below 2^32
+    return a.HW % V == 0 && a.C <= kSyncTable && total < ((int64_t)1 << 31) &&
+           bn_aligned16(a.x) && bn_aligned16(a.out) && (!bwd || bn_aligned16(a.dy));
+}
+
+template <typename T, typename K>
+cudaError_t launch_bn_flat(K kernel, const BnSyncArgs &a, int num_sms, cudaStream_t s) {
+    constexpr int V = IO<T>::V;
+    const int64_t total = a.batch * a.C * (a.HW / V);
+    const int64_t need = (total + BSY_THREADS * BSY_PACKS - 1) / (BSY_THREADS * BSY_PACKS);
+    const int64_t slots = (int64_t)num_sms * 8;
+    const unsigned grid = (unsigned)(need < slots ? need : slots);
+    const size_t smem = (size_t)a.C * (sizeof(float4) + sizeof(float));
+    kernel<<<grid, BSY_THREADS, smem, s>>>(a, (uint32_t)total, make_fastdiv((uint32_t)(a.HW / V)),
+                                           make_fastdiv((uint32_t)a.C));
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_apply_stats_t(const BnSyncArgs &a, int num_sms, cudaStream_t s) {
+    if (bn_flat_ok<T>(a, false)) return launch_bn_flat<T>(bn_apply_stats_flat_kernel<T>, a, num_sms, s);
+    bn_apply_stats_kernel<T><<<bn_grid(a.batch * a.C, num_sms), BSY_THREADS, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_apply_sums_t(const BnSyncArgs &a, int num_sms, cudaStream_t s) {
+    if (bn_flat_ok<T>(a, true)) return launch_bn_flat<T>(bn_apply_sums_flat_kernel<T>, a, num_sms, s);
+    bn_apply_sums_kernel<T><<<bn_grid(a.batch * a.C, num_sms), BSY_THREADS, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t batch,
-                                 int64_t C, int64_t HW, int dtype, cudaStream_t s) {
+cudaError_t launch_bn_unit_stats_host(const BnArgs &a, int dtype, int num_sms, cudaStream_t s,
+                                      int *nch, int *cpk, int *q) {
+    BnChunks u;
+    const cudaError_t e = launch_bn_unit_stats(a, dtype, num_sms, s, &u);
+    *nch = u.nch;
+    *cpk = u.cpk;
+    *q = u.q;
+    return e;
+}
+
+cudaError_t launch_bn_bwd_unit_sums_host(const BnBwdArgs &a, int dtype, int num_sms,
+                                         cudaStream_t s, int *nch) {
+    BnChunks u;
+    const cudaError_t e = launch_bn_bwd_unit_sums(a, dtype, num_sms, s, &u);
+    *nch = u.nch;
+    return e;
+}
+
+cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t per_channel,
+                                 int64_t C, int64_t HW, int nch, int cpk, int q, int V, int dtype,
+                                 cudaStream_t s) {
     const unsigned grid = (unsigned)((C + 7) / 8);  // 8 channels (warps) per CTA
     switch (dtype) {
-    case DT_F32: bn_fold_stats_kernel<float><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW); break;
-    case DT_F16: bn_fold_stats_kernel<__half><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW); break;
+    case DT_F32:
+        bn_fold_stats_kernel<float><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch, cpk, q, V);
+        break;
+    case DT_F16:
+        bn_fold_stats_kernel<__half><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch, cpk, q, V);
+        break;
     case DT_BF16:
-        bn_fold_stats_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ws, x, stats, batch, C, HW);
+        bn_fold_stats_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch,
+                                                                 cpk, q, V);
         break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums, int64_t batch,
-                                int64_t C, cudaStream_t s) {
-    bn_fold_sums_kernel<<<(unsigned)((C + 7) / 8), 256, 0, s>>>(ws, rstd, sums, batch, C);
+cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums,
+                                int64_t per_channel, int64_t C, cudaStream_t s) {
+    bn_fold_sums_kernel<<<(unsigned)((C + 7) / 8), 256, 0, s>>>(ws, rstd, sums, per_channel, C);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s) {
-    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
     switch (dtype) {
-    case DT_F32: bn_apply_stats_kernel<float><<<grid, BSY_THREADS, 0, s>>>(a); break;
-    case DT_F16: bn_apply_stats_kernel<__half><<<grid, BSY_THREADS, 0, s>>>(a); break;
-    case DT_BF16: bn_apply_stats_kernel<__nv_bfloat16><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_F32: return launch_apply_stats_t<float>(a, num_sms, s);
+    case DT_F16: return launch_apply_stats_t<__half>(a, num_sms, s);
+    case DT_BF16: return launch_apply_stats_t<__nv_bfloat16>(a, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bn_apply_sums(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s) {
-    const unsigned grid = bn_grid(a.batch * a.C, num_sms);
     switch (dtype) {
-    case DT_F32: bn_apply_sums_kernel<float><<<grid, BSY_THREADS, 0, s>>>(a); break;
-    case DT_F16: bn_apply_sums_kernel<__half><<<grid, BSY_THREADS, 0, s>>>(a); break;
-    case DT_BF16: bn_apply_sums_kernel<__nv_bfloat16><<<grid, BSY_THREADS, 0, s>>>(a); break;
+    case DT_F32: return launch_apply_sums_t<float>(a, num_sms, s);
+    case DT_F16: return launch_apply_sums_t<__half>(a, num_sms, s);
+    case DT_BF16: return launch_apply_sums_t<__nv_bfloat16>(a, num_sms, s);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace nrm

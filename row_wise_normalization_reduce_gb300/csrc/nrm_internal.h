@@ -157,6 +157,14 @@ cudaError_t launch_bn_bwd(const BnBwdArgs &a, int dtype, int num_sms, cudaStream
 // (mean, M2) of d = x - x[0, c, 0] for the forward; (sum dy, sum dy*(x - mean))
 // for the backward.
 cudaError_t launch_bn_plane_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s);
+// Stage 1 per unit (chunks of at most kBnChunkPacks packs; planes of 16-byte
+// aligned packs, fewer than kBnUnitPlaneLimit packs): the unit layout is
+// returned as chunks per plane, packs per chunk, packs per plane.
+constexpr int64_t kBnUnitPlaneLimit = (int64_t)1 << 20;
+cudaError_t launch_bn_unit_stats_host(const BnArgs &a, int dtype, int num_sms, cudaStream_t s,
+                                      int *nch, int *cpk, int *q);
+cudaError_t launch_bn_bwd_unit_sums_host(const BnBwdArgs &a, int dtype, int num_sms,
+                                         cudaStream_t s, int *nch);
 cudaError_t launch_bn_bwd_plane_sums(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s);
 
 // Synchronized BatchNorm pieces (bn_sync.cu).
@@ -176,10 +184,14 @@ struct BnSyncArgs {
     int64_t batch, C, HW;
     float eps, momentum;
 };
-cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t batch,
-                                 int64_t C, int64_t HW, int dtype, cudaStream_t s);
-cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums, int64_t batch,
-                                int64_t C, cudaStream_t s);
+// Folds of stage-1 partials into per-channel binary64 arrays: per_channel
+// partials per channel; for per-unit partials (V > 0) partial j counts
+// min(cpk, q - (j mod nch)*cpk)*V values, for per-plane partials (V = 0) HW.
+cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t per_channel,
+                                 int64_t C, int64_t HW, int nch, int cpk, int q, int V, int dtype,
+                                 cudaStream_t s);
+cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums,
+                                int64_t per_channel, int64_t C, cudaStream_t s);
 cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_bn_apply_sums(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
 
