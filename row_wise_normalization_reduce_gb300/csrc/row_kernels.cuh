@@ -151,7 +151,10 @@ struct NoHook {
 // add+RMS) hold its raw 16-byte packs.  `after_sync` runs right after the
 // first group-wide sum, when every member has its values in registers (the
 // bulk-copy pipeline refills the stage there).
-template <int OP, typename T, int PACKS, int STRIDE, class Red, class Prm, class Hook>
+// FULL: the row is exactly STRIDE x PACKS packs, so no pack index needs a
+// bounds test.
+template <int OP, typename T, int PACKS, int STRIDE, class Red, class Prm, class Hook,
+          bool FULL = false>
 __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row, const int t,
                                             Red &red, const uint4 (&rx)[PACKS],
                                             const uint4 (&rr)[PACKS], const Prm &prm,
@@ -170,7 +173,7 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
         const int idx = t + k * STRIDE;
-        if (idx < P) {
+        if (FULL || idx < P) {
             io2::unpack(rx[k], v[k]);
             if (OP == OP_ADD_RMS) {
                 float2 r[H];
@@ -205,7 +208,7 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
         float2 e1 = f2(0.f), e2 = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
-            if (t + k * STRIDE < P) {
+            if (FULL || t + k * STRIDE < P) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     const float2 e = __fadd2_rn(v[k][h], nm);
@@ -239,7 +242,7 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
         const int idx = t + k * STRIDE;
-        if (idx < P) {
+        if (FULL || idx < P) {
             float2 out[H], g[H];
             prm.p0_pack(idx, g);
             if (OP == OP_LN) {
@@ -258,13 +261,13 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
 }
 
 // Issue every load of one row (S1/S2) before any arithmetic.
-template <int OP, int PACKS, int STRIDE, class Src>
+template <int OP, int PACKS, int STRIDE, class Src, bool FULL = false>
 __device__ __forceinline__ void row_load(const Src &src, const int t, const int P,
                                          uint4 (&rx)[PACKS], uint4 (&rr)[PACKS]) {
 #pragma unroll
     for (int k = 0; k < PACKS; ++k) {
         const int idx = t + k * STRIDE;
-        if (idx < P) {
+        if (FULL || idx < P) {
             rx[k] = src.x_pack(idx);
             if (OP == OP_ADD_RMS) rr[k] = src.r_pack(idx);
         }
@@ -272,13 +275,14 @@ __device__ __forceinline__ void row_load(const Src &src, const int t, const int 
 }
 
 // One row: load, then compute.
-template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class Prm, class Hook>
+template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class Prm, class Hook,
+          bool FULL = false>
 __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, const int t,
                                          Red &red, const Src &src, const Prm &prm,
                                          const Hook &after_sync) {
     uint4 rx[PACKS], rr[PACKS];
-    row_load<OP, PACKS, STRIDE>(src, t, (int)(a.N / IO<T>::V), rx, rr);
-    row_compute<OP, T, PACKS, STRIDE>(a, row, t, red, rx, rr, prm, after_sync);
+    row_load<OP, PACKS, STRIDE, Src, FULL>(src, t, (int)(a.N / IO<T>::V), rx, rr);
+    row_compute<OP, T, PACKS, STRIDE, Red, Prm, Hook, FULL>(a, row, t, red, rx, rr, prm, after_sync);
 }
 
 // Resident CTAs per SM the CTA and persistent kernels are compiled for
@@ -309,7 +313,7 @@ constexpr int row_min_blocks() {
                                                                               : 1;
 }
 
-template <int OP, typename T, int THREADS, int PACKS>
+template <int OP, typename T, int THREADS, int PACKS, bool FULL = false>
 __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()))
     row_cta_kernel(const RowArgs a, const int64_t pf) {
     constexpr int NW = THREADS / 32;
@@ -334,7 +338,8 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
         CtaRed<NW> red{&s1[parity][0], &s2[parity][0]};
         const GlobalSrc<T> src{X + row * a.ldx, R + row * a.ldr};
         const GlobalParams<T> prm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
-        row_body<OP, T, PACKS, THREADS>(a, row, threadIdx.x, red, src, prm, NoHook{});
+        row_body<OP, T, PACKS, THREADS, CtaRed<NW>, GlobalSrc<T>, GlobalParams<T>, NoHook, FULL>(
+            a, row, threadIdx.x, red, src, prm, NoHook{});
     }
 }
 
@@ -752,9 +757,9 @@ cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
 // CTA-per-row launch: grid = rows (clamped); the L2 prefetch distance is
 // p.prefetch waves of resident CTAs (occupancy computed once per device and
 // kernel instance).
-template <int OP, typename T, int THREADS, int PACKS>
+template <int OP, typename T, int THREADS, int PACKS, bool FULL = false>
 cudaError_t launch_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
-    auto kernel = row_cta_kernel<OP, T, THREADS, PACKS>;
+    auto kernel = row_cta_kernel<OP, T, THREADS, PACKS, FULL>;
     int64_t pf = 0;
     if (p.prefetch > 0) {
         int dev = 0;
@@ -813,6 +818,14 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     } else if (p.kind == PLAN_CTA) {
 #define NRM_CTA_CASE(TH, PK)                                                       \
     if (p.threads == TH && p.packs == PK) return launch_cta<OP, T, TH, PK>(a, p, s);
+// the automatic shapes at power-of-two N also come without bounds tests
+// (LayerNorm 4096x4096 bf16 12.2 -> 11.4 us; RMSNorm measured 2 % slower
+// that way, so it keeps the tested form)
+#define NRM_CTA_FULL_CASE(TH, PK)                                                  \
+    if (OP != OP_RMS && p.threads == TH && p.packs == PK && a.N / IO<T>::V == TH * PK) \
+        return launch_cta<OP, T, TH, PK, true>(a, p, s);
+        NRM_CTA_FULL_CASE(128, 4) NRM_CTA_FULL_CASE(256, 2) NRM_CTA_FULL_CASE(256, 4)
+#undef NRM_CTA_FULL_CASE
         NRM_CTA_CASE(128, 1) NRM_CTA_CASE(256, 1) NRM_CTA_CASE(512, 1) NRM_CTA_CASE(1024, 1)
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
         NRM_CTA_CASE(128, 4) NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)

@@ -80,7 +80,8 @@ __device__ __forceinline__ MaxSum cta_merge_all(MaxSum v, float2 *slot) {
 // ---------------------------------------------------------------------------
 // CTA plan
 // ---------------------------------------------------------------------------
-template <typename T, int THREADS, int PACKS>
+// FULL: the row is exactly THREADS x PACKS packs (no bounds tests).
+template <typename T, int THREADS, int PACKS, bool FULL = false>
 __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, const int64_t pf) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
@@ -98,12 +99,12 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
         uint4 raw[PACKS];
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
-            if (t + k * THREADS < P) raw[k] = ld_stream(xr + (size_t)(t + k * THREADS) * V);
+            if (FULL || t + k * THREADS < P) raw[k] = ld_stream(xr + (size_t)(t + k * THREADS) * V);
         float2 v[PACKS][H];
         float2 mx = f2(-INFINITY);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
-            if (t + k * THREADS < P) {
+            if (FULL || t + k * THREADS < P) {
                 io2::unpack(raw[k], v[k]);
 #pragma unroll
                 for (int h = 0; h < H; ++h)
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
         float dt = 0.f;
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
-            if (t + k * THREADS < P) {
+            if (FULL || t + k * THREADS < P) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     v[k][h] = make_float2(smx_exp<T>(v[k][h].x - sh), smx_exp<T>(v[k][h].y - sh));
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             const int idx = t + k * THREADS;
-            if (idx < P) {
+            if (FULL || idx < P) {
                 float2 o[H];
 #pragma unroll
                 for (int h = 0; h < H; ++h) o[h] = __fmul2_rn(v[k][h], s2);
@@ -178,9 +179,9 @@ __global__ void __launch_bounds__(THREADS) softmax_generic_kernel(const RowArgs 
     }
 }
 
-template <typename T, int THREADS, int PACKS>
+template <typename T, int THREADS, int PACKS, bool FULL = false>
 cudaError_t launch_softmax_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
-    auto kernel = softmax_cta_kernel<T, THREADS, PACKS>;
+    auto kernel = softmax_cta_kernel<T, THREADS, PACKS, FULL>;
     int64_t pf = 0;
     if (p.prefetch > 0) {
         int dev = 0;
@@ -218,6 +219,10 @@ cudaError_t launch_softmax_t(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.kind != PLAN_CTA) return cudaErrorInvalidConfiguration;
 #define NRM_SMX_CASE(TH, PK) \
     if (p.threads == TH && p.packs == PK) return launch_softmax_cta<T, TH, PK>(a, p, s);
+    if (p.threads == 128 && p.packs == 4 && a.N / IO<T>::V == 512)
+        return launch_softmax_cta<T, 128, 4, true>(a, p, s);
+    if (p.threads == 256 && p.packs == 4 && a.N / IO<T>::V == 1024)
+        return launch_softmax_cta<T, 256, 4, true>(a, p, s);
     NRM_SMX_CASE(128, 1) NRM_SMX_CASE(256, 1) NRM_SMX_CASE(128, 4) NRM_SMX_CASE(256, 2)
     NRM_SMX_CASE(256, 4) NRM_SMX_CASE(512, 4) NRM_SMX_CASE(1024, 4)
 #undef NRM_SMX_CASE
