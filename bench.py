@@ -181,6 +181,19 @@ def measured_peak():
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+# BatchNorm calls report their plan with the row-plan codes (include/nrm.h,
+# nrm_last_plan); name them by what they run.
+_BN_PLAN_NAMES = {
+    "bn": {"tma": "cluster", "cta": "stream", "generic": "scalar"},
+    "bn_bwd": {"cta": "stream", "generic": "scalar"},
+    "bn_infer": {"cta": "flat", "generic": "scalar"},
+}
+
+
+def plan_name(op, kind_name):
+    return _BN_PLAN_NAMES.get(op, {}).get(kind_name, kind_name)
+
+
 class Step:
     """One call of the hot path on rotating, pre-filled device buffers."""
 
@@ -222,7 +235,7 @@ class Step:
         self.run(self.sets[0])
         torch.cuda.synchronize()
         kind = nrm.last_plan()[0]
-        self.plan = nrm.PLAN_NAMES.get(kind)
+        self.plan = plan_name(w.op, nrm.PLAN_NAMES.get(kind))
         self.launches_per_step = 1
         if w.op in ("bn", "bn_bwd") and kind in (nrm.PLAN_CTA, nrm.PLAN_GENERIC):
             self.launches_per_step = 2
