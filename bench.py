@@ -184,7 +184,7 @@ def measured_peak():
 # BatchNorm calls report their plan with the row-plan codes (include/nrm.h,
 # nrm_last_plan); name them by what they run.
 _BN_PLAN_NAMES = {
-    "bn": {"tma": "cluster", "cta": "stream", "generic": "scalar"},
+    "bn": {"tma": "cluster", "cta": "stream", "generic": "scalar", "persist": "flow"},
     "bn_bwd": {"cta": "stream", "generic": "scalar"},
     "bn_infer": {"cta": "flat", "generic": "scalar"},
 }
@@ -237,7 +237,7 @@ class Step:
         kind = nrm.last_plan()[0]
         self.plan = plan_name(w.op, nrm.PLAN_NAMES.get(kind))
         self.launches_per_step = 1
-        if w.op in ("bn", "bn_bwd") and kind in (nrm.PLAN_CTA, nrm.PLAN_GENERIC):
+        if w.op in ("bn", "bn_bwd") and kind in (nrm.PLAN_CTA, nrm.PLAN_GENERIC, nrm.PLAN_PERSIST):
             self.launches_per_step = 2
 
     def __call__(self):

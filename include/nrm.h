@@ -197,10 +197,12 @@ int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum,
 
 /*
  * Bytes of device workspace bn_fwd_train needs for this shape (0 on invalid
- * arguments): 8 bytes per chunk of at most 1024 16-byte packs of each (n, c)
- * plane, i.e. batch * C * ceil(ceil(HW / (16 / element size)) / 1024) * 8.
- * The workspace holds partial statistics; its content on entry does not
- * matter and it is scratch on exit.
+ * arguments): 8 bytes per chunk of at most 128 16-byte packs of each (n, c)
+ * plane, P = batch * C * ceil(ceil(HW / (16 / element size)) / 128) chunks,
+ * rounded up to 16 bytes, plus 24 bytes per channel:
+ * roundup16(8 * P) + 24 * C.  The workspace holds partial statistics, folded
+ * per-channel statistics and per-channel control words that each call resets
+ * itself; its content on entry does not matter and it is scratch on exit.
  */
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype);
 
@@ -378,8 +380,14 @@ typedef enum {
  * follows the forced plan too: NRM_PLAN_CTA selects its streaming two-kernel
  * plan (per-plane statistics into the workspace, then a dependent launch that
  * normalizes), NRM_PLAN_TMA one cluster of CTAs per channel (shared memory and
- * distributed shared memory, no workspace), NRM_PLAN_GENERIC the scalar
- * two-kernel plan for any layout; bn_bwd takes NRM_PLAN_GENERIC as its scalar
+ * distributed shared memory, no workspace), NRM_PLAN_PERSIST the one-pass
+ * plan (a reset of the workspace's control words, then one kernel whose
+ * CTAs take statistics items and normalize items in a fixed interleaved
+ * order, x read once from HBM; `stages` sets its L2 prefetch of the chunks
+ * a CTA takes next: 0 = automatic, two rounds of the grid ahead, 1 = off,
+ * s >= 2 = s - 1 rounds ahead, at most 8), NRM_PLAN_GENERIC the scalar two-kernel plan
+ * for any layout; a forced plan the layout does not allow falls back to the
+ * next plan that runs; bn_bwd takes NRM_PLAN_GENERIC as its scalar
  * plan and anything else as its streaming plan where the layout allows it;
  * bn_fwd_infer takes NRM_PLAN_GENERIC as its scalar element-wise kernel.
  * Returns NRM_OK or NRM_ERR_UNSUPPORTED for
@@ -392,8 +400,9 @@ int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
  * thread's most recent successful call (written to the non-NULL pointers).
  * After a BatchNorm call only the plan is set, as an nrm_plan code: NRM_PLAN_TMA
  * for the cluster plan, NRM_PLAN_CTA for the streaming plans (two kernels,
- * or one element-wise kernel for inference), NRM_PLAN_GENERIC for the scalar
- * plans; the other four values are 0.
+ * or one element-wise kernel for inference), NRM_PLAN_PERSIST for the
+ * one-pass plan, NRM_PLAN_GENERIC for the scalar plans; the other four values
+ * are 0.
  */
 void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups);
 

@@ -116,6 +116,7 @@ int bn_plan_from_forced() {
     case PLAN_GENERIC: return BN_PLAN_SCALAR;
     case PLAN_TMA: return BN_PLAN_CLUSTER;
     case PLAN_CTA: return BN_PLAN_STREAM;
+    case PLAN_PERSIST: return BN_PLAN_FLOW;
     default: return BN_PLAN_AUTO;
     }
 }
@@ -594,13 +595,15 @@ int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum, int64_t 
 
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
     if (!dtype_ok(dtype) || batch < 1 || C < 1 || HW < 1) return 0;
-    // one float2 per chunk of at most 1024 packs of a plane (streaming
-    // plans); the scalar plan needs one per plane, never more
+    // 8 bytes per chunk of at most 128 packs of a plane (the one-pass plan's
+    // smallest chunks; the streaming plans use 1024-pack chunks, the scalar
+    // plan one partial per plane, never more), then the one-pass plan's
+    // per-channel statistics and control words
     const int64_t V = 16 / (int64_t)elem_size(dtype);
     const int64_t packs = (HW + V - 1) / V;
-    const int64_t nch = (packs + kBnChunkPacks - 1) / kBnChunkPacks;
-    if ((uint64_t)batch > (uint64_t)INT64_MAX / 8 / (uint64_t)C / (uint64_t)nch) return 0;
-    return (size_t)batch * (size_t)C * (size_t)nch * 8;
+    const int64_t nch = (packs + kBnFlowMinChunkPacks - 1) / kBnFlowMinChunkPacks;
+    if ((uint64_t)batch > (uint64_t)INT64_MAX / 16 / (uint64_t)C / (uint64_t)nch) return 0;
+    return bn_flow_ws_bytes(C, batch * C * nch);
 }
 
 int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
@@ -641,7 +644,11 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
     if ((st = device_info(&dev)) != NRM_OK) return st;
     BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
              eps, momentum, workspace, fault_word(), g_wait_limit.load(std::memory_order_relaxed),
-             bn_plan_from_forced()};
+             bn_plan_from_forced(), workspace_bytes, 0, 0};
+    if (g_force_kind.load(std::memory_order_relaxed) == PLAN_PERSIST) {
+        a.prefetch = g_force_stages.load(std::memory_order_relaxed);
+        a.packs = g_force_packs.load(std::memory_order_relaxed);
+    }
     int used = 0;
     return record_bn(launch_bn_train(a, dtype, dev.sms, stream, &used), used);
 }

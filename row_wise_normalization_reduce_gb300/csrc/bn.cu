@@ -97,21 +97,6 @@ __global__ void __launch_bounds__(BN_THREADS) bn_partial_kernel(const BnArgs a) 
     }
 }
 
-// Writes save_mean/save_rstd and the running statistics of channel c from
-// its shifted mean md (d = x - K), biased variance and rstd.
-__device__ __forceinline__ void bn_write_channel_stats(const BnArgs &a, int64_t c, float K,
-                                                       float md, float var, float rstd) {
-    if (a.save_mean) a.save_mean[c] = K + md;
-    if (a.save_rstd) a.save_rstd[c] = rstd;
-    const float m = a.momentum;
-    if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
-    if (a.running_var) {
-        const float cnt = (float)(a.batch * a.HW);
-        const float unbiased = var * (cnt / (float)(a.batch * a.HW - 1));
-        a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
-    }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
     constexpr int V = IO<T>::V;
@@ -190,8 +175,6 @@ __global__ void __launch_bounds__(BN_THREADS) bn_apply_kernel(const BnArgs a) {
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, const BnChunks u) {
-    using io2 = IO2<T>;
-    constexpr int H = io2::H;
     constexpr int NW = BNS_THREADS / 32;
     __shared__ float s1[2][NW];
     __shared__ float2 s2[2][NW];
@@ -210,39 +193,8 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, c
         for (int k = 0; k < BNS_PACKS; ++k)
             if (tid + k * BNS_THREADS < w.len) v[k] = __ldg(xp + tid + k * BNS_THREADS);
         const float K = bn_elem<T>(a.x, w.c * HW);
-        const float cnt = (float)(w.len * IO<T>::V);
-        const float2 nk = f2(-K);
-        float2 acc = f2(0.f);
-#pragma unroll
-        for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < w.len) {
-                float2 f[H];
-                io2::unpack(v[k], f);
-#pragma unroll
-                for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, __fadd2_rn(f[h], nk));
-            }
-        const float tot = cta_sum_all<NW>(hsum(acc), s1[par]);
-        const float m0 = tot / cnt;
-        const float2 nkm = f2(-m0);
-        float2 e1 = f2(0.f), e2 = f2(0.f);
-#pragma unroll
-        for (int k = 0; k < BNS_PACKS; ++k)
-            if (tid + k * BNS_THREADS < w.len) {
-                float2 f[H];
-                io2::unpack(v[k], f);
-#pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const float2 e = __fadd2_rn(__fadd2_rn(f[h], nk), nkm);
-                    e1 = __fadd2_rn(e1, e);
-                    e2 = __ffma2_rn(e, e, e2);
-                }
-            }
-        const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2[par]);
-        if (tid == 0) {
-            const float cc = E.x / cnt;
-            ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] =
-                make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
-        }
+        const float2 r = bn_unit_partial<T>(v, w.len, K, s1[par], s2[par]);
+        if (tid == 0) ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] = r;
     }
     pdl_launch_dependents();
     // A later group's statistics kernel overlaps the previous group's
@@ -623,10 +575,21 @@ cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int 
             return e;
         }
     }
-    // automatic choice: the streaming plan only for planes of one unit; longer
-    // planes run faster on the scalar plan's per-plane loops (measured at
-    // [64, 64, 112, 112]: 108 us against 150 us)
+    // automatic choice beyond the cluster plan: planes of one unit take the
+    // streaming plan; longer planes the one-pass plan (measured at
+    // [64, 64, 112, 112] binary32: 104 us, against 108 us for the scalar
+    // plan's two passes over x and 150 us for the streaming plan; at
+    // [32, 64, 56, 56] the streaming plan's 18.6 us beats its 33 us)
     const bool one_unit = a.HW / V <= kBnChunkPacks;
+    if (((a.bn_plan == BN_PLAN_AUTO || a.bn_plan == BN_PLAN_NO_STREAM) && !one_unit) ||
+        a.bn_plan == BN_PLAN_FLOW) {
+        bool launched = false;
+        const cudaError_t e = launch_bn_flow(a, bn_dtype<T>(), num_sms, s, &launched);
+        if (launched || e != cudaSuccess) {
+            *used = PLAN_PERSIST;
+            return e;
+        }
+    }
     if (stream_ok && ((a.bn_plan == BN_PLAN_AUTO && one_unit) || a.bn_plan == BN_PLAN_STREAM)) {
         *used = PLAN_CTA;
         return launch_bn_stream<T>(a, num_sms, s);
@@ -774,7 +737,8 @@ extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void
         return NRM_ERR_DEVICE;
     }
     BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
-             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, bn_plan};
+             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, bn_plan,
+             sizeof(g_bn_static_partials)};
     int used = 0;
     return launch_bn_train(a, dtype, sms, stream, &used) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
 }

@@ -26,6 +26,21 @@ __device__ __forceinline__ float hsum(float2 v) { return v.x + v.y; }
 
 __host__ __device__ __forceinline__ bool bn_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Writes save_mean/save_rstd and the running statistics of channel c from
+// its shifted mean md (d = x - K), biased variance and rstd.
+__device__ __forceinline__ void bn_write_channel_stats(const BnArgs &a, int64_t c, float K,
+                                                       float md, float var, float rstd) {
+    if (a.save_mean) a.save_mean[c] = K + md;
+    if (a.save_rstd) a.save_rstd[c] = rstd;
+    const float m = a.momentum;
+    if (a.running_mean) a.running_mean[c] = fmaf(1.f - m, a.running_mean[c], m * (K + md));
+    if (a.running_var) {
+        const float cnt = (float)(a.batch * a.HW);
+        const float unbiased = var * (cnt / (float)(a.batch * a.HW - 1));
+        a.running_var[c] = fmaf(1.f - m, a.running_var[c], m * unbiased);
+    }
+}
+
 // Division of 32-bit unsigned integers by a run-time constant d (1 <= d <
 // 2^31) with a multiply-high, shift and add: the round-up method of
 // Granlund and Montgomery, "Division by Invariant Integers using
@@ -98,6 +113,51 @@ __device__ __forceinline__ BnUnit bn_unit(const BnChunks &u, int64_t idx) {
     return r;
 }
 
+// Exact partial statistics of one unit held in registers by a CTA of
+// BNS_THREADS threads (pack tid + k * BNS_THREADS in v[k], k < PACKS, valid
+// below len):
+// a corrected two-pass on d = x - K, returned as (mean of d, M2) with the
+// same bits in every thread.  Two CTA-wide sums through s1 and s2, which the
+// caller alternates between consecutive units.
+template <typename T, int PACKS = BNS_PACKS>
+__device__ __forceinline__ float2 bn_unit_partial(const uint4 (&v)[PACKS], int len, float K,
+                                                  float *s1, float2 *s2) {
+    using io2 = IO2<T>;
+    constexpr int H = io2::H;
+    constexpr int NW = BNS_THREADS / 32;
+    const int tid = threadIdx.x;
+    const float cnt = (float)(len * IO<T>::V);
+    const float2 nk = f2(-K);
+    float2 acc = f2(0.f);
+#pragma unroll
+    for (int k = 0; k < PACKS; ++k)
+        if (tid + k * BNS_THREADS < len) {
+            float2 f[H];
+            io2::unpack(v[k], f);
+#pragma unroll
+            for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, __fadd2_rn(f[h], nk));
+        }
+    const float tot = cta_sum_all<NW>(hsum(acc), s1);
+    const float m0 = tot / cnt;
+    const float2 nkm = f2(-m0);
+    float2 e1 = f2(0.f), e2 = f2(0.f);
+#pragma unroll
+    for (int k = 0; k < PACKS; ++k)
+        if (tid + k * BNS_THREADS < len) {
+            float2 f[H];
+            io2::unpack(v[k], f);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float2 e = __fadd2_rn(__fadd2_rn(f[h], nk), nkm);
+                e1 = __fadd2_rn(e1, e);
+                e2 = __ffma2_rn(e, e, e2);
+            }
+        }
+    const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2);
+    const float cc = E.x / cnt;
+    return make_float2(m0 + cc, fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f));
+}
+
 // Channels per group so that a group's input bytes stay within `budget`
 // (the second stage then re-reads them from L2).
 inline int64_t bn_group_channels(int64_t C, int64_t bytes_per_channel, int64_t budget) {
@@ -137,6 +197,16 @@ cudaError_t launch_bn_unit_stats(const BnArgs &a, int dtype, int num_sms, cudaSt
                                  BnChunks *u);
 cudaError_t launch_bn_bwd_unit_sums(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
                                     BnChunks *u);
+
+// The one-pass plan (bn_flow.cu) for 16-byte aligned planes of whole packs
+// and a workspace of at least bn_flow_ws_bytes: *launched tells whether it
+// ran (false: the layout or the workspace does not allow it).
+cudaError_t launch_bn_flow(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, bool *launched);
+
+template <typename T> constexpr int bn_dtype();
+template <> constexpr int bn_dtype<float>() { return DT_F32; }
+template <> constexpr int bn_dtype<__half>() { return DT_F16; }
+template <> constexpr int bn_dtype<__nv_bfloat16>() { return DT_BF16; }
 
 // Input bytes per channel group of the streaming BatchNorm plans (api.cpp;
 // nrm_set_bn_group_bytes), 0 for a single group.

@@ -92,30 +92,50 @@ struct BnArgs {
     int64_t batch, C, HW;
     float eps, momentum;
     void *ws;             // two-kernel plans: batch * C float2 partials
-    unsigned *fault;      // device fault word (cluster plan), or NULL
+    unsigned *fault;      // device fault word (cluster and one-pass plans), or NULL
     unsigned wait_limit;  // tries per bounded wait
     int bn_plan;          // BnPlan
+    size_t ws_bytes = 0;  // bytes at ws (the one-pass plan runs only if it fits)
+    int prefetch = 0;     // one-pass plan's L2 prefetch: 0 auto, 1 off, s >= 2: s - 1 rounds ahead
+    int packs = 0;        // one-pass plan's packs per thread: 0 auto, 4 or 8
 };
 
 // BatchNorm plans: automatic, streaming two kernels (registers + dependent
 // launch), one cluster of CTAs per channel (shared memory + DSMEM), and the
 // scalar two-kernel plan (any layout).
 // BN_PLAN_NO_STREAM: automatic choice without the streaming plan (whose
-// per-chunk partials may not fit a fixed partials array).
+// per-chunk partials may not fit a fixed partials array).  BN_PLAN_FLOW: the
+// one-pass plan (bn_flow.cu): statistics and normalization in one kernel,
+// each channel normalized a few channels after its statistics, its second
+// read served by L2.
 enum BnPlan {
     BN_PLAN_AUTO = 0,
     BN_PLAN_STREAM = 1,
     BN_PLAN_CLUSTER = 2,
     BN_PLAN_SCALAR = 3,
-    BN_PLAN_NO_STREAM = 4
+    BN_PLAN_NO_STREAM = 4,
+    BN_PLAN_FLOW = 5
 };
 
 // Packs (16 bytes) per work unit of the streaming BatchNorm plans: a unit is
 // a chunk of at most this many packs of one plane; the workspace holds one
 // float2 per unit.
 constexpr int kBnChunkPacks = 1024;
+
+// Smallest chunk of the one-pass plan (32 lanes x 4 packs): the workspace
+// holds one partial per chunk of this size.
+constexpr int kBnFlowMinChunkPacks = 128;
+
+// Workspace bytes of the one-pass plans for C channels and `units` chunks in
+// all: the per-chunk 8-byte partials (padded to 16 bytes), then 24 bytes per
+// channel (folded statistics and control words).
+inline size_t bn_flow_ws_bytes(int64_t C, int64_t units) {
+    return (((size_t)units * 8 + 15) & ~(size_t)15) + (size_t)C * 24;
+}
+
 // The launchers report the plan they ran through *used as a PlanKind
-// (cluster: PLAN_TMA, streaming: PLAN_CTA, scalar: PLAN_GENERIC).
+// (cluster: PLAN_TMA, streaming: PLAN_CTA, scalar: PLAN_GENERIC, one-pass:
+// PLAN_PERSIST).
 cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_t s, int *used);
 
 // BatchNorm inference forward: y = (x - running_mean) * rsqrt(running_var +

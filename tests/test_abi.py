@@ -91,10 +91,19 @@ def test_aliasing_rules(lib):
     assert st in (OK, DEVICE)
 
 
+def bn_ws_formula(b, c, hw, es):
+    # include/nrm.h: roundup16(8 * P) + 24 * C, P = batch * C * chunks per plane
+    packs = -(-hw // (16 // es))
+    chunks = b * c * -(-packs // 128)
+    return -(-8 * chunks // 16) * 16 + 24 * c
+
+
 def test_bn_validation(lib):
     b, c, hw = 2, 3, 5
     need = lib.bn_fwd_train_workspace_size(b, c, hw, 0)
-    assert need == b * c * 8
+    assert need == bn_ws_formula(b, c, hw, 4) == 120
+    for shape, dt, es in (((2, 3, 5000), 0, 4), ((3, 5, 9000), 2, 2), ((1, 1, 1), 1, 2)):
+        assert lib.bn_fwd_train_workspace_size(*shape, dt) == bn_ws_formula(*shape, es)
     assert lib.bn_fwd_train_workspace_size(0, c, hw, 0) == 0
     assert lib.bn_fwd_train_workspace_size(b, c, hw, 9) == 0
     x, y, ws = A, A * 16, A * 64
@@ -144,7 +153,7 @@ def test_bn_infer_validation(lib):
 def test_bn_bwd_validation(lib):
     b, c, hw = 2, 3, 5
     need = lib.bn_bwd_workspace_size(b, c, hw, 0)
-    assert need == b * c * 8
+    assert need == bn_ws_formula(b, c, hw, 4)
     assert lib.bn_bwd_workspace_size(b, 0, hw, 0) == 0
     dy, x, sm, sr, dx, ws = A, A * 16, A * 32, A * 33, A * 48, A * 64
 
@@ -223,11 +232,11 @@ def _model_overlap(a, lda, wa, b, ldb, wb, rows):
 def test_sync_bn_validation(lib):
     b, c, hw = 2, 3, 5
     x, st, ws, y, parts, dy, dx = A, A * 16, A * 32, A * 48, A * 64, A * 80, A * 96
-    assert lib.bn_fwd_partial_stats(None, st, b, c, hw, 0, ws, 64, None) == NULL
+    assert lib.bn_fwd_partial_stats(None, st, b, c, hw, 0, ws, 256, None) == NULL
     assert lib.bn_fwd_partial_stats(x, st, b, c, hw, 0, ws, 8, None) == WS
-    assert lib.bn_fwd_partial_stats(x, st + 4, b, c, hw, 0, ws, 64, None) == VALUE
-    assert lib.bn_fwd_partial_stats(x, x + 8, b, c, hw, 0, ws, 64, None) == ALIAS
-    assert lib.bn_fwd_partial_stats(x, st, b, c, hw, 0, ws, 64, None) in (OK, DEVICE)
+    assert lib.bn_fwd_partial_stats(x, st + 4, b, c, hw, 0, ws, 256, None) == VALUE
+    assert lib.bn_fwd_partial_stats(x, x + 8, b, c, hw, 0, ws, 256, None) == ALIAS
+    assert lib.bn_fwd_partial_stats(x, st, b, c, hw, 0, ws, 256, None) in (OK, DEVICE)
     args = (None, None, None, None, None, None)
     assert lib.bn_fwd_apply_stats(x, None, None, y, parts, 0, *args[:4], b, c, hw, 1e-5, 0.1, 0,
                                   None) == SHAPE
@@ -237,8 +246,8 @@ def test_sync_bn_validation(lib):
                                   None) == VALUE
     assert lib.bn_fwd_apply_stats(x, None, None, y, parts, 2, *args[:4], b, c, hw, 1e-5, 0.1, 0,
                                   None) in (OK, DEVICE)
-    assert lib.bn_bwd_partial_sums(dy, x, None, st, parts, b, c, hw, 0, ws, 64, None) == NULL
-    assert lib.bn_bwd_partial_sums(dy, x, st, st + 64, parts, b, c, hw, 0, ws, 64,
+    assert lib.bn_bwd_partial_sums(dy, x, None, st, parts, b, c, hw, 0, ws, 256, None) == NULL
+    assert lib.bn_bwd_partial_sums(dy, x, st, st + 64, parts, b, c, hw, 0, ws, 256,
                                    None) in (OK, DEVICE)
     assert lib.bn_bwd_apply_sums(dy, x, None, st, st + 64, parts, 2, b * hw - 1, dx, None, None,
                                  b, c, hw, 0, None) == SHAPE

@@ -22,8 +22,8 @@ def _lib():
     nrm.force_plan(nrm.PLAN_AUTO)
 
 
-TRAIN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC]
-TRAIN_IDS = ["auto", "stream", "cluster", "scalar"]
+TRAIN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC, nrm.PLAN_PERSIST]
+TRAIN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
 TWO_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_GENERIC]
 TWO_IDS = ["auto", "scalar"]
 SHAPES = [(1, 3, 5, 5), (2, 4, 3, 3), (4, 8, 1, 1), (2, 3, 4, 8), (3, 5, 13, 11), (8, 16, 28, 28),
@@ -141,3 +141,66 @@ def test_bn_stream_chunks_and_groups(orc, shape, group_bytes, dtype, op):
     for k in gpu:
         assert (gpu[k] == again[k]).all(), k
     RN.compare(op, inp, gpu, RN.run_oracle(orc, op, inp, 1e-5, 0.1))
+
+
+@pytest.mark.parametrize("packs", [0, 4, 8], ids=["auto_packs", "packs4", "packs8"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 5, 64, 80), (1, 2, 96, 96), (2, 3, 70, 70), (3, 4, 40, 200),
+                                   (1, 1, 64, 64), (2, 1, 200, 200), (4, 40, 32, 32),
+                                   (64, 64, 16, 16), (32, 64, 56, 56)])
+def test_bn_flow_chunks_and_lag(orc, shape, dtype, packs):
+    # the one-pass plan at four and eight packs per thread: several chunks per
+    # plane (the last one shorter where the plane does not divide evenly), a
+    # single channel (every statistics item before any normalize item), more
+    # items than resident CTAs (normalize items interleaved with later
+    # channels' statistics); bitwise repeatable; layouts it cannot take fall
+    # back to another plan
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
+    nrm.force_plan(nrm.PLAN_PERSIST, 0, packs)
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    hw = shape[2] * shape[3]
+    packed = hw % (4 if dtype == "f32" else 8) == 0
+    assert (nrm.last_plan()[0] == nrm.PLAN_PERSIST) == packed
+    again = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    for k in gpu:
+        assert (gpu[k] == again[k]).all(), k
+    RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
+
+
+def test_bn_flow_ignores_workspace_contents(orc):
+    # the control words live in the caller's workspace and are reset by the
+    # call itself: a workspace full of 0xFF bytes gives the same result
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(6, 10, 40, 40))
+    nrm.force_plan(nrm.PLAN_PERSIST)
+    ref = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    x, g, b = inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda()
+    need = nrm.bn_fwd_train_workspace_size(6, 10, 1600)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        y, sm, sr = nrm.bn_fwd_train(x, g, b, None, None, 1e-5, 0.1, workspace=ws)
+        torch.cuda.synchronize()
+        assert nrm.last_plan()[0] == nrm.PLAN_PERSIST
+        assert np.array_equal(y.cpu().numpy(), ref["y"])
+        assert np.array_equal(sm.cpu().numpy(), ref["save_mean"])
+        assert np.array_equal(sr.cpu().numpy(), ref["save_rstd"])
+
+
+def test_bn_flow_wait_give_up_path(orc):
+    # wait limit 0: every normalize item gives up its wait for the channel's
+    # statistics at once; the kernel must raise the fault bit and still end,
+    # and the next call must be correct
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(8, 16, 28, 28))
+    nrm.force_plan(nrm.PLAN_PERSIST)
+    x = inp["x"].cuda()
+    assert nrm.device_fault(clear=True) == 0
+    old = nrm.set_wait_limit(0)
+    try:
+        nrm.bn_fwd_train(x, None, None, None, None, 1e-5, 0.1)
+        bits = nrm.device_fault(clear=True)
+    finally:
+        nrm.set_wait_limit(old)
+    assert nrm.last_plan()[0] == nrm.PLAN_PERSIST
+    assert bits == 1, bits
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
+    assert nrm.device_fault(clear=True) == 0

@@ -248,9 +248,10 @@ def test_guard_bands_untouched(op):
 
 
 # ---- BatchNorm ------------------------------------------------------------
-# automatic / streaming two kernels / cluster per channel / scalar two kernels
-BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC]
-BN_IDS = ["auto", "stream", "cluster", "scalar"]
+# automatic / streaming two kernels / cluster per channel / scalar two kernels /
+# one-pass dataflow kernel
+BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC, nrm.PLAN_PERSIST]
+BN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
 
 
 @pytest.mark.parametrize("plan", BN_PLANS, ids=BN_IDS)
@@ -278,14 +279,16 @@ def test_bn_large_mean_channel(orc, plan):
 def test_bn_plans_agree_and_repeat():
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 8, 28, 28))
     outs = []
-    plans = (nrm.PLAN_CTA, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_TMA, nrm.PLAN_GENERIC)
+    plans = (nrm.PLAN_CTA, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_TMA, nrm.PLAN_GENERIC,
+             nrm.PLAN_PERSIST, nrm.PLAN_PERSIST)
     for plan in plans:
         nrm.force_plan(plan)
         outs.append(RN.run_gpu("bn", inp, 1e-5, 0.1))
     for k in outs[0]:
         assert (outs[0][k] == outs[1][k]).all(), k  # bitwise repeatable
         assert (outs[2][k] == outs[3][k]).all(), k
-        for o in (outs[2], outs[4]):
+        assert (outs[5][k] == outs[6][k]).all(), k
+        for o in (outs[2], outs[4], outs[5]):
             assert np.max(np.abs(outs[0][k].astype(np.float64) - o[k])) <= 2e-5, k
 
 
