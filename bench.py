@@ -532,7 +532,8 @@ class SyncBnStep:
                      for _ in range(self.nsets)]
         c = w.shape[1]
         self.parts = torch.empty(1, c, 3, dtype=torch.float64, device=device)
-        self.ws = torch.empty(w.shape[0] * c * 8, dtype=torch.uint8, device=device)
+        self.ws = torch.empty(nrm.bn_fwd_train_workspace_size(w.shape[0], c, int(np.prod(w.shape[2:]))),
+                              dtype=torch.uint8, device=device)
         self.sm = torch.empty(c, device=device)
         self.sr = torch.empty(c, device=device)
         self.i = 0

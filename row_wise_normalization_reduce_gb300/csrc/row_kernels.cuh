@@ -324,7 +324,15 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
 #if NRM_ROW_PDL
     // launched as a programmatic dependent: wait for the previous grid on the
     // stream (its outputs may be this call's inputs), then let the next one
-    // get its CTAs resident while this grid runs
+    // get its CTAs resident while this grid runs.  A CTA that becomes
+    // resident while the previous grid still runs first asks L2 for its own
+    // row: L2 is where writes become coherent, so data the previous grid
+    // writes afterwards still reaches the loads issued after the wait.
+    if (pf > 0 && threadIdx.x == 0 && blockIdx.x < a.rows) {
+        const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+        prefetch_l2_bulk(X + blockIdx.x * a.ldx, bytes);
+        if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + blockIdx.x * a.ldr, bytes);
+    }
     pdl_wait();
     pdl_launch_dependents();
 #endif

@@ -91,6 +91,13 @@ __global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, c
     const int t = threadIdx.x;
     const int P = (int)(a.N / V);
     const T *X = static_cast<const T *>(a.x);
+    // launched as a programmatic dependent (as the norm kernels): the CTA's
+    // own row is requested from L2 first, then the kernel waits for the
+    // previous grid on the stream and lets the next one become resident
+    if (pf > 0 && t == 0 && blockIdx.x < a.rows)
+        prefetch_l2_bulk(X + blockIdx.x * a.ldx, (uint32_t)(a.N * (int64_t)sizeof(T)));
+    pdl_wait();
+    pdl_launch_dependents();
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
         if (pf > 0 && t == 0 && row + pf < a.rows)
@@ -200,8 +207,17 @@ cudaError_t launch_softmax_cta(const RowArgs &a, const Plan &p, cudaStream_t s) 
         }
         pf = (int64_t)p.prefetch * p.sms * per_sm;
     }
-    kernel<<<(unsigned)p.grid, THREADS, 0, s>>>(a, pf);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, pf);
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 template <typename T>
