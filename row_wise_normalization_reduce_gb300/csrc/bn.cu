@@ -181,6 +181,18 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, c
     const int tid = threadIdx.x;
     const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
     float2 *ws = static_cast<float2 *>(a.ws);
+    if (u.c0 == 0) {
+        // first group, a programmatic dependent of the stream's previous
+        // kernel: request the first unit's chunk from L2, then wait for that
+        // kernel (its outputs may be x, and it may still read the workspace)
+        if (tid == 0 && blockIdx.x < units) {
+            const BnUnit w = bn_unit(u, blockIdx.x);
+            prefetch_l2_bulk(reinterpret_cast<const uint4 *>(static_cast<const T *>(a.x) +
+                                                             (w.n * a.C + w.c) * HW) + w.off,
+                             (uint32_t)w.len * 16u);
+        }
+        pdl_wait();
+    }
     int par = 0;
     for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
         const BnUnit w = bn_unit(u, idx);
@@ -339,6 +351,14 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     // thread 0's bookkeeping: iteration whose planes were last issued into /
     // last received from each buffer (for the drain after a give-up)
     int last_issued0 = -1, last_issued1 = -1, last_done0 = -1, last_done1 = -1;
+    // programmatic dependent launch: the CTA's planes of its first channel are
+    // requested from L2 before the wait for the previous grid (L2 is where
+    // that grid's writes become coherent; the bulk copies come after the wait)
+    if (tid == 0 && np > 0 && first_c < C)
+        for (int j = 0; j < np; ++j)
+            prefetch_l2_bulk(static_cast<const T *>(a.x) + ((n0 + j) * C + first_c) * HW, plane_bytes);
+    pdl_wait();
+    pdl_launch_dependents();
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
@@ -512,11 +532,13 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(BNC_THREADS);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(a.C * cs));
@@ -539,6 +561,7 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     if (k < 1) return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(k * cs));
     *launched = true;
+    cfg.numAttrs = 2;  // the occupancy queries above take the cluster shape alone
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
@@ -553,9 +576,11 @@ cudaError_t launch_bn_stream(const BnArgs &a, int num_sms, cudaStream_t s) {
         u.c0 = c0;
         u.G = (a.C - c0) < G ? (a.C - c0) : G;
         const unsigned grid = bn_grid(a.batch * u.G * u.nch, num_sms);
-        // the first group's statistics follow the stream's earlier work; later
-        // groups read other channels and only overlap the previous group
-        e = launch_pdl(bn_stats_kernel<T>, grid, BNS_THREADS, s, c0 > 0, a, u);
+        // every statistics kernel is a programmatic dependent: the first
+        // group's waits for the stream's earlier work before it touches
+        // memory, later groups read other channels and only overlap the
+        // previous group's normalize kernel
+        e = launch_pdl(bn_stats_kernel<T>, grid, BNS_THREADS, s, true, a, u);
         if (e == cudaSuccess) e = launch_pdl(bn_norm_kernel<T>, grid, BNS_THREADS, s, true, a, u);
     }
     return e;

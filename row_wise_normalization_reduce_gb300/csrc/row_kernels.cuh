@@ -306,6 +306,25 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 #ifndef NRM_LN4_MIN_THREADS
 #define NRM_LN4_MIN_THREADS 896
 #endif
+// Launch with programmatic stream serialization when NRM_ROW_PDL (the
+// kernels then order themselves with griddepcontrol.wait).
+template <typename K, typename... Args>
+inline cudaError_t launch_row(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = NRM_ROW_PDL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int OP, int THREADS, int PACKS>
 constexpr int row_min_blocks() {
     return (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0)                 ? NRM_CTA_MIN_THREADS / THREADS
@@ -368,6 +387,19 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()
     const int P = (int)(a.N / IO<T>::V);
     const T *X = static_cast<const T *>(a.x);
     const T *R = static_cast<const T *>(a.res);
+#if NRM_ROW_PDL
+    // programmatic dependent launch, as row_cta_kernel: the CTA's first two
+    // rows are requested from L2 before the wait for the previous grid
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+        for (int64_t r = blockIdx.x; r < a.rows && r < (int64_t)blockIdx.x + 2 * gridDim.x; r += gridDim.x) {
+            prefetch_l2_bulk(X + r * a.ldx, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + r * a.ldr, bytes);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+#endif
     if (smem_params)
         fill_smem_params<T, (OP == OP_LN ? 2 : 1), THREADS>(a, reinterpret_cast<float *>(sparams));
     __syncthreads();
@@ -427,6 +459,20 @@ __global__ void __launch_bounds__(WARPS * 32) row_wraw_kernel(const RowArgs a, c
     const int warp = threadIdx.x >> 5;
     const int P = (int)(a.N / V);
     const float fN = a.fN, invN = a.invN;
+#if NRM_ROW_PDL
+    // programmatic dependent launch, as row_cta_kernel: each warp's first row
+    // is requested from L2 before the wait for the previous grid
+    {
+        const int64_t r0 = (int64_t)blockIdx.x * WARPS + warp;
+        if (lane == 0 && r0 < a.rows) {
+            const uint32_t bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
+            prefetch_l2_bulk(static_cast<const T *>(a.x) + r0 * a.ldx, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(static_cast<const T *>(a.res) + r0 * a.ldr, bytes);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+#endif
     if (smem_params)
         fill_smem_params<T, (OP == OP_LN ? 2 : 1), WARPS * 32>(a, reinterpret_cast<float *>(sparams));
     __syncthreads();
@@ -721,8 +767,7 @@ cudaError_t launch_persist(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = a.rows < slots ? a.rows : slots;
-    kernel<<<(unsigned)grid, THREADS, smem, s>>>(a, p.smem_params, p.prefetch);
-    return cudaGetLastError();
+    return launch_row(kernel, (unsigned)grid, THREADS, smem, s, a, p.smem_params, p.prefetch);
 }
 
 // Warp-per-row launch: dynamic shared memory = parameters in binary32 (when
@@ -758,8 +803,7 @@ cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const int64_t need = (a.rows + WARPS - 1) / WARPS;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = need < slots ? need : slots;
-    kernel<<<(unsigned)grid, WARPS * 32, smem, s>>>(a, p.smem_params, p.prefetch);
-    return cudaGetLastError();
+    return launch_row(kernel, (unsigned)grid, WARPS * 32, smem, s, a, p.smem_params, p.prefetch);
 }
 
 // CTA-per-row launch: grid = rows (clamped); the L2 prefetch distance is
