@@ -637,13 +637,14 @@ cudaError_t launch_bn_unit_stats(const BnArgs &a, int dtype, int num_sms, cudaSt
     u->c0 = 0;
     u->G = a.C;
     const unsigned grid = bn_grid(a.batch * a.C * u->nch, num_sms);
+    // a programmatic dependent: one group (c0 = 0), so the kernel waits for
+    // the stream's previous kernel before it touches memory
     switch (dtype) {
-    case DT_F32: bn_stats_kernel<float><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
-    case DT_F16: bn_stats_kernel<__half><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
-    case DT_BF16: bn_stats_kernel<__nv_bfloat16><<<grid, BNS_THREADS, 0, s>>>(a, *u); break;
+    case DT_F32: return launch_pdl(bn_stats_kernel<float>, grid, BNS_THREADS, s, true, a, *u);
+    case DT_F16: return launch_pdl(bn_stats_kernel<__half>, grid, BNS_THREADS, s, true, a, *u);
+    case DT_BF16: return launch_pdl(bn_stats_kernel<__nv_bfloat16>, grid, BNS_THREADS, s, true, a, *u);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bn_plane_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s) {

@@ -54,6 +54,9 @@ template <typename T>
 __global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *stats,
                                      int64_t per_channel, int64_t C, int64_t HW, int nch, int cpk,
                                      int q, int V) {
+    // a programmatic dependent of the statistics kernel
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (c >= C) return;
@@ -82,6 +85,8 @@ __global__ void bn_fold_stats_kernel(const float2 *ws, const void *x, double *st
 // over the channel's `per_channel` partials.
 __global__ void bn_fold_sums_kernel(const float2 *ws, const float *rstd, double *sums,
                                     int64_t per_channel, int64_t C) {
+    pdl_wait();  // a programmatic dependent of the stream's previous kernel
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t c = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (c >= C) return;
@@ -233,32 +238,40 @@ __global__ void __launch_bounds__(BSY_THREADS) bn_apply_stats_flat_kernel(const 
                                                                           const uint32_t total,
                                                                           const FastDiv per_plane,
                                                                           const FastDiv channels) {
+    // a programmatic dependent of the stream's previous kernel (the fold, or
+    // the exchange of the parts): wait before reading anything
+    pdl_wait();
+    pdl_launch_dependents();
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     extern __shared__ float4 tab[];  // [C] {mean_hi, mean_lo, rstd, gamma}, then [C] beta
     float *tb = reinterpret_cast<float *>(tab + a.C);
+    // every CTA builds the table; GB300's binary64 rate is low, so the
+    // binary64 work per channel is the fold of the parts alone, and the
+    // variance and rstd are formed in binary32 from the binary64 M2 and count
+    // (division, square root and reciprocal correctly rounded: rstd within a
+    // few ulp of the binary64 value)
     for (int64_t c = threadIdx.x; c < a.C; c += BSY_THREADS) {
-        DStats st{0.0, 0.0, 0.0};
-        for (int64_t r = 0; r < a.nparts; ++r) {
+        const double *q0 = a.parts + 3 * c;
+        DStats st{q0[0], q0[1], q0[2]};
+        for (int64_t r = 1; r < a.nparts; ++r) {
             const double *q = a.parts + 3 * (r * a.C + c);
             st = dcombine(st, DStats{q[0], q[1], q[2]});
         }
-        const double var = st.m2 / st.n;
-        const double rstd = 1.0 / sqrt(var + (double)a.eps);
+        const float rstd = 1.0f / sqrtf((float)st.m2 / (float)st.n + a.eps);
         const float hi = (float)st.mean;
         // the mean as hi + lo: (x - hi) - lo keeps x - mean exact-ish for
         // channels with a large mean
-        tab[c] = make_float4(hi, (float)(st.mean - (double)hi), (float)rstd,
-                             bn_param<T>(a.gamma, c, 1.f));
+        tab[c] = make_float4(hi, (float)(st.mean - (double)hi), rstd, bn_param<T>(a.gamma, c, 1.f));
         tb[c] = bn_param<T>(a.beta, c, 0.f);
         if (blockIdx.x == 0) {
             if (a.save_mean) a.save_mean[c] = hi;
-            if (a.save_rstd) a.save_rstd[c] = (float)rstd;
+            if (a.save_rstd) a.save_rstd[c] = rstd;
             const double m = (double)a.momentum;
             if (a.running_mean)
                 a.running_mean[c] = (float)((1.0 - m) * a.running_mean[c] + m * st.mean);
             if (a.running_var)
-                a.running_var[c] = (float)((1.0 - m) * a.running_var[c] + m * var * st.n / (st.n - 1.0));
+                a.running_var[c] = (float)((1.0 - m) * a.running_var[c] + m * st.m2 / (st.n - 1.0));
         }
     }
     __syncthreads();
@@ -296,6 +309,10 @@ __global__ void __launch_bounds__(BSY_THREADS) bn_apply_sums_flat_kernel(const B
                                                                          const uint32_t total,
                                                                          const FastDiv per_plane,
                                                                          const FastDiv channels) {
+    // a programmatic dependent of the stream's previous kernel (the fold, or
+    // the exchange of the parts): wait before reading anything
+    pdl_wait();
+    pdl_launch_dependents();
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     extern __shared__ float4 tab[];  // [C] {mean, rstd, gamma*rstd, s1/count}, then [C] s2/count
@@ -306,10 +323,11 @@ __global__ void __launch_bounds__(BSY_THREADS) bn_apply_sums_flat_kernel(const B
             s1 += a.parts[2 * (r * a.C + c) + 0];
             s2 += a.parts[2 * (r * a.C + c) + 1];
         }
+        // binary32 divisions of the binary64 sums (GB300's binary64 rate is low)
         const float rstd = a.rstd[c];
-        tab[c] = make_float4(a.mean[c], rstd, bn_param<T>(a.gamma, c, 1.f) * rstd,
-                             (float)(s1 / (double)a.count));
-        tb[c] = (float)(s2 / (double)a.count);
+        const float cnt = (float)a.count;
+        tab[c] = make_float4(a.mean[c], rstd, bn_param<T>(a.gamma, c, 1.f) * rstd, (float)s1 / cnt);
+        tb[c] = (float)s2 / cnt;
         if (blockIdx.x == 0) {
             if (a.dbeta) a.dbeta[c] = (float)s1;
             if (a.dgamma) a.dgamma[c] = (float)s2;
@@ -371,9 +389,19 @@ cudaError_t launch_bn_flat(K kernel, const BnSyncArgs &a, int num_sms, cudaStrea
     const int64_t slots = (int64_t)num_sms * 8;
     const unsigned grid = (unsigned)(need < slots ? need : slots);
     const size_t smem = (size_t)a.C * (sizeof(float4) + sizeof(float));
-    kernel<<<grid, BSY_THREADS, smem, s>>>(a, (uint32_t)total, make_fastdiv((uint32_t)(a.HW / V)),
-                                           make_fastdiv((uint32_t)a.C));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(BSY_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (uint32_t)total,
+                                             make_fastdiv((uint32_t)(a.HW / V)), make_fastdiv((uint32_t)a.C));
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 template <typename T>
@@ -413,18 +441,20 @@ cudaError_t launch_bn_bwd_unit_sums_host(const BnBwdArgs &a, int dtype, int num_
 cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats, int64_t per_channel,
                                  int64_t C, int64_t HW, int nch, int cpk, int q, int V, int dtype,
                                  cudaStream_t s) {
-    const unsigned grid = (unsigned)((C + 7) / 8);  // 8 channels (warps) per CTA
+    // one channel (warp) per CTA, so the channels' binary64 folds run on
+    // different SMs (GB300's binary64 rate per SM is low)
+    if (C < 1 || C > 0x7fffffff) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)C;
     switch (dtype) {
     case DT_F32:
-        bn_fold_stats_kernel<float><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch, cpk, q, V);
-        break;
+        return launch_pdl(bn_fold_stats_kernel<float>, grid, 32, s, true, ws, x, stats, per_channel, C, HW,
+                          nch, cpk, q, V);
     case DT_F16:
-        bn_fold_stats_kernel<__half><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch, cpk, q, V);
-        break;
+        return launch_pdl(bn_fold_stats_kernel<__half>, grid, 32, s, true, ws, x, stats, per_channel, C, HW,
+                          nch, cpk, q, V);
     case DT_BF16:
-        bn_fold_stats_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ws, x, stats, per_channel, C, HW, nch,
-                                                                 cpk, q, V);
-        break;
+        return launch_pdl(bn_fold_stats_kernel<__nv_bfloat16>, grid, 32, s, true, ws, x, stats, per_channel,
+                          C, HW, nch, cpk, q, V);
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -432,8 +462,8 @@ cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats,
 
 cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums,
                                 int64_t per_channel, int64_t C, cudaStream_t s) {
-    bn_fold_sums_kernel<<<(unsigned)((C + 7) / 8), 256, 0, s>>>(ws, rstd, sums, per_channel, C);
-    return cudaGetLastError();
+    if (C < 1 || C > 0x7fffffff) return cudaErrorInvalidValue;
+    return launch_pdl(bn_fold_sums_kernel, (unsigned)C, 32, s, true, ws, rstd, sums, per_channel, C);
 }
 
 cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s) {
