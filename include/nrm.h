@@ -197,8 +197,8 @@ int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum,
 
 /*
  * Bytes of device workspace bn_fwd_train needs for this shape (0 on invalid
- * arguments): 8 bytes per chunk of at most 128 16-byte packs of each (n, c)
- * plane, P = batch * C * ceil(ceil(HW / (16 / element size)) / 128) chunks,
+ * arguments): 8 bytes per chunk of at most 1024 16-byte packs of each (n, c)
+ * plane, P = batch * C * ceil(ceil(HW / (16 / element size)) / 1024) chunks,
  * rounded up to 16 bytes, plus 24 bytes per channel:
  * roundup16(8 * P) + 24 * C.  The workspace holds partial statistics, folded
  * per-channel statistics and per-channel control words that each call resets

@@ -595,13 +595,12 @@ int softmax_fwd(const void *x, void *y, float *row_max, float *row_sum, int64_t 
 
 size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dtype) {
     if (!dtype_ok(dtype) || batch < 1 || C < 1 || HW < 1) return 0;
-    // 8 bytes per chunk of at most 128 packs of a plane (the one-pass plan's
-    // smallest chunks; the streaming plans use 1024-pack chunks, the scalar
-    // plan one partial per plane, never more), then the one-pass plan's
-    // per-channel statistics and control words
+    // 8 bytes per chunk of at most 1024 packs of a plane (the streaming and
+    // one-pass plans; the scalar plan needs one per plane, never more), then
+    // the one-pass plan's per-channel statistics and control words
     const int64_t V = 16 / (int64_t)elem_size(dtype);
     const int64_t packs = (HW + V - 1) / V;
-    const int64_t nch = (packs + kBnFlowMinChunkPacks - 1) / kBnFlowMinChunkPacks;
+    const int64_t nch = (packs + kBnChunkPacks - 1) / kBnChunkPacks;
     if ((uint64_t)batch > (uint64_t)INT64_MAX / 16 / (uint64_t)C / (uint64_t)nch) return 0;
     return bn_flow_ws_bytes(C, batch * C * nch);
 }

@@ -122,10 +122,6 @@ enum BnPlan {
 // float2 per unit.
 constexpr int kBnChunkPacks = 1024;
 
-// Smallest chunk of the one-pass plan (32 lanes x 4 packs): the workspace
-// holds one partial per chunk of this size.
-constexpr int kBnFlowMinChunkPacks = 128;
-
 // Workspace bytes of the one-pass plans for C channels and `units` chunks in
 // all: the per-chunk 8-byte partials (padded to 16 bytes), then 24 bytes per
 // channel (folded statistics and control words).

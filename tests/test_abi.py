@@ -94,7 +94,7 @@ def test_aliasing_rules(lib):
 def bn_ws_formula(b, c, hw, es):
     # include/nrm.h: roundup16(8 * P) + 24 * C, P = batch * C * chunks per plane
     packs = -(-hw // (16 // es))
-    chunks = b * c * -(-packs // 128)
+    chunks = b * c * -(-packs // 1024)
     return -(-8 * chunks // 16) * 16 + 24 * c
 
 
