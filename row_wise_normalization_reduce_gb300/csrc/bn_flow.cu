@@ -51,7 +51,6 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "bn_common.cuh"
 
@@ -335,20 +334,9 @@ cudaError_t launch_bn_flow_t(const BnArgs &a, int num_sms, cudaStream_t s, bool 
     f.divU = make_fastdiv(f.U);
     f.divN = make_fastdiv((uint32_t)u.nch);
     auto kernel = bn_flow_kernel<T, PACKS>;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static std::mutex mu;  // one cache per kernel instance
-    static int cached_per_sm[64] = {};
     int per_sm = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!cached_per_sm[dev]) {
-            const cudaError_t e =
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, BNF_THREADS, 0);
-            if (e != cudaSuccess) return e;
-        }
-        per_sm = cached_per_sm[dev];
-    }
+    const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), BNF_THREADS, 0, &per_sm);
+    if (oe != cudaSuccess) return oe;
     if (per_sm < 1) return cudaSuccess;
     const int64_t cap = (int64_t)per_sm * num_sms;
     const int64_t grid = items < cap ? items : cap;

@@ -65,6 +65,12 @@ struct Plan {
     int prefetch;  // CTA: L2 prefetch distance in waves of resident CTAs (0: off)
 };
 
+// Resident CTAs per SM of `kernel` (a __global__ function) on the current
+// device at `threads` threads and `smem` bytes of dynamic shared memory; the
+// kernel's dynamic shared-memory limit is raised to `smem` when needed.  Asked
+// once per device, kernel, block size and shared-memory size.  occupancy.cpp.
+cudaError_t resident_ctas(const void *kernel, int threads, size_t smem, int *per_sm);
+
 // Address of the current device's fault word (set up once per device), or
 // NULL if it cannot be obtained.  fault.cu.
 unsigned *fault_word();

@@ -31,8 +31,6 @@
 // from sums of x and x^2.
 #pragma once
 
-#include <mutex>
-
 #include "nrm_device.cuh"
 #include "nrm_internal.h"
 
@@ -709,25 +707,9 @@ cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const size_t params = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
     const size_t smem = params + stage * (size_t)p.stages * G;
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static std::mutex mu;  // one cache per kernel instance
-    static size_t cached_smem[64];
-    static int cached_per_sm[64];
     int per_sm = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (cached_smem[dev] != smem) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, GT * G,
-                                                              smem);
-            if (e != cudaSuccess) return e;
-            cached_smem[dev] = smem;
-        }
-        per_sm = cached_per_sm[dev];
-    }
+    const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), GT * G, smem, &per_sm);
+    if (oe != cudaSuccess) return oe;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = a.rows < slots ? a.rows : slots;
@@ -743,27 +725,9 @@ cudaError_t launch_persist(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.sms < 1) return cudaErrorInvalidConfiguration;
     const size_t smem = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static std::mutex mu;  // one cache per kernel instance
-    static size_t cached_smem[64] = {};
-    static int cached_per_sm[64] = {};
-    static bool cached[64] = {};
     int per_sm = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!cached[dev] || cached_smem[dev] != smem) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, THREADS,
-                                                              smem);
-            if (e != cudaSuccess) return e;
-            cached_smem[dev] = smem;
-            cached[dev] = true;
-        }
-        per_sm = cached_per_sm[dev];
-    }
+    const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), THREADS, smem, &per_sm);
+    if (oe != cudaSuccess) return oe;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = a.rows < slots ? a.rows : slots;
@@ -778,27 +742,9 @@ cudaError_t launch_wraw(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.sms < 1) return cudaErrorInvalidConfiguration;
     const size_t smem = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static std::mutex mu;  // one cache per kernel instance
-    static size_t cached_smem[64] = {};
-    static int cached_per_sm[64] = {};
-    static bool cached[64] = {};
     int per_sm = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!cached[dev] || cached_smem[dev] != smem) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel,
-                                                              WARPS * 32, smem);
-            if (e != cudaSuccess) return e;
-            cached_smem[dev] = smem;
-            cached[dev] = true;
-        }
-        per_sm = cached_per_sm[dev];
-    }
+    const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), WARPS * 32, smem, &per_sm);
+    if (oe != cudaSuccess) return oe;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t need = (a.rows + WARPS - 1) / WARPS;
     const int64_t slots = (int64_t)p.sms * per_sm;
@@ -814,20 +760,9 @@ cudaError_t launch_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
     auto kernel = row_cta_kernel<OP, T, THREADS, PACKS, FULL>;
     int64_t pf = 0;
     if (p.prefetch > 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        static std::mutex mu;  // one cache per kernel instance
-        static int cached_per_sm[64] = {};
         int per_sm = 0;
-        {
-            std::lock_guard<std::mutex> lock(mu);
-            if (!cached_per_sm[dev]) {
-                const cudaError_t e =
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, THREADS, 0);
-                if (e != cudaSuccess) return e;
-            }
-            per_sm = cached_per_sm[dev];
-        }
+        const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), THREADS, 0, &per_sm);
+        if (oe != cudaSuccess) return oe;
         pf = (int64_t)p.prefetch * p.sms * per_sm;
     }
 #if NRM_ROW_PDL

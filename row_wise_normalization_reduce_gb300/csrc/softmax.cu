@@ -27,7 +27,6 @@
 // output type.
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "nrm_device.cuh"
 #include "nrm_internal.h"
@@ -191,20 +190,9 @@ cudaError_t launch_softmax_cta(const RowArgs &a, const Plan &p, cudaStream_t s) 
     auto kernel = softmax_cta_kernel<T, THREADS, PACKS, FULL>;
     int64_t pf = 0;
     if (p.prefetch > 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        static std::mutex mu;  // one cache per kernel instance
-        static int cached_per_sm[64] = {};
         int per_sm = 0;
-        {
-            std::lock_guard<std::mutex> lock(mu);
-            if (!cached_per_sm[dev]) {
-                const cudaError_t e =
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_per_sm[dev], kernel, THREADS, 0);
-                if (e != cudaSuccess) return e;
-            }
-            per_sm = cached_per_sm[dev];
-        }
+        const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), THREADS, 0, &per_sm);
+        if (oe != cudaSuccess) return oe;
         pf = (int64_t)p.prefetch * p.sms * per_sm;
     }
     cudaLaunchConfig_t cfg = {};
