@@ -185,7 +185,7 @@ def measured_peak():
 # nrm_last_plan); name them by what they run.
 _BN_PLAN_NAMES = {
     "bn": {"tma": "cluster", "cta": "stream", "generic": "scalar", "persist": "flow"},
-    "bn_bwd": {"cta": "stream", "generic": "scalar"},
+    "bn_bwd": {"cta": "stream", "generic": "scalar", "persist": "flow"},
     "bn_infer": {"cta": "flat", "generic": "scalar"},
 }
 

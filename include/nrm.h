@@ -387,8 +387,9 @@ typedef enum {
  * a CTA takes next: 0 = automatic, two rounds of the grid ahead, 1 = off,
  * s >= 2 = s - 1 rounds ahead, at most 8), NRM_PLAN_GENERIC the scalar two-kernel plan
  * for any layout; a forced plan the layout does not allow falls back to the
- * next plan that runs; bn_bwd takes NRM_PLAN_GENERIC as its scalar
- * plan and anything else as its streaming plan where the layout allows it;
+ * next plan that runs; bn_bwd takes NRM_PLAN_GENERIC as its scalar plan,
+ * NRM_PLAN_PERSIST as its one-pass plan (dy and x read once) and anything
+ * else as its streaming plan where the layout allows it;
  * bn_fwd_infer takes NRM_PLAN_GENERIC as its scalar element-wise kernel.
  * Returns NRM_OK or NRM_ERR_UNSUPPORTED for
  * an unknown plan.  Process-wide; not meant to change while calls run.
@@ -401,8 +402,8 @@ int nrm_force_plan(int plan, int threads, int packs, int stages, int groups);
  * After a BatchNorm call only the plan is set, as an nrm_plan code: NRM_PLAN_TMA
  * for the cluster plan, NRM_PLAN_CTA for the streaming plans (two kernels,
  * or one element-wise kernel for inference), NRM_PLAN_PERSIST for the
- * one-pass plan, NRM_PLAN_GENERIC for the scalar plans; the other four values
- * are 0.
+ * one-pass plans (training forward and backward), NRM_PLAN_GENERIC for the
+ * scalar plans; the other four values are 0.
  */
 void nrm_last_plan(int *plan, int *threads, int *packs, int *stages, int *groups);
 

@@ -716,7 +716,10 @@ int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_m
     DevInfo dev;
     if ((st = device_info(&dev)) != NRM_OK) return st;
     BnBwdArgs a{dy, x, gamma, save_mean, save_rstd, dx, dgamma, dbeta, batch, C, HW, workspace,
-                bn_plan_from_forced()};
+                bn_plan_from_forced(), fault_word(), g_wait_limit.load(std::memory_order_relaxed),
+                workspace_bytes, 0};
+    if (g_force_kind.load(std::memory_order_relaxed) == PLAN_PERSIST)
+        a.prefetch = g_force_stages.load(std::memory_order_relaxed);
     int used = 0;
     return record_bn(launch_bn_bwd(a, dtype, dev.sms, stream, &used), used);
 }

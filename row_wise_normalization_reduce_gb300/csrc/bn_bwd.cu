@@ -227,6 +227,17 @@ cudaError_t launch_bn_bwd_t(const BnBwdArgs &a, int num_sms, cudaStream_t s, int
     const bool stream_ok = a.bn_plan != BN_PLAN_SCALAR && a.HW % V == 0 &&
                            a.HW / V < kBnMaxPlanePacks && bn_aligned16(a.dy) &&
                            bn_aligned16(a.x) && bn_aligned16(a.dx);
+    // planes longer than one unit: the one-pass plan first (dy and x read
+    // from HBM once; the streaming plan reads them twice once they exceed L2)
+    const bool one_unit = a.HW / V <= kBnChunkPacks;
+    if (stream_ok && ((a.bn_plan == BN_PLAN_AUTO && !one_unit) || a.bn_plan == BN_PLAN_FLOW)) {
+        bool launched = false;
+        const cudaError_t e = launch_bn_bwd_flow(a, bn_dtype<T>(), num_sms, s, &launched);
+        if (launched || e != cudaSuccess) {
+            *used = PLAN_PERSIST;
+            return e;
+        }
+    }
     *used = stream_ok ? PLAN_CTA : PLAN_GENERIC;
     if (stream_ok) {
         BnChunks u = bn_chunks(a.HW / V);

@@ -170,8 +170,16 @@ struct BnBwdArgs {
     float *dbeta;
     int64_t batch, C, HW;
     void *ws;
-    int bn_plan;          // BN_PLAN_AUTO / STREAM / SCALAR
+    int bn_plan;          // BN_PLAN_AUTO / STREAM / SCALAR / FLOW
+    unsigned *fault = nullptr;  // device fault word (one-pass plan), or NULL
+    unsigned wait_limit = 0;    // tries per bounded wait
+    size_t ws_bytes = 0;        // bytes at ws (the one-pass plan runs only if it fits)
+    int prefetch = 0;           // one-pass plan's L2 prefetch, as BnArgs::prefetch
 };
+// The one-pass backward (bn_flow_bwd.cu) for 16-byte aligned planes of whole
+// packs; *launched tells whether it ran.
+cudaError_t launch_bn_bwd_flow(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
+                               bool *launched);
 cudaError_t launch_bn_bwd(const BnBwdArgs &a, int dtype, int num_sms, cudaStream_t s,
                           int *used);
 

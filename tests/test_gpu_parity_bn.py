@@ -204,3 +204,43 @@ def test_bn_flow_wait_give_up_path(orc):
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
     RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
     assert nrm.device_fault(clear=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 5, 64, 80), (1, 2, 96, 96), (2, 3, 70, 70), (3, 4, 40, 200),
+                                   (1, 1, 64, 64), (2, 1, 200, 200), (4, 40, 32, 32),
+                                   (64, 64, 16, 16), (16, 8, 56, 56)])
+def test_bn_bwd_flow_chunks_and_lag(orc, shape, dtype):
+    # the one-pass backward: several chunks per plane, a single channel, more
+    # items than resident CTAs; bitwise repeatable; layouts it cannot take
+    # fall back to another plan
+    inp = W.make_inputs(W.BN_BWD_F32_32x64x56x56, shape=shape, dtype=dtype)
+    nrm.force_plan(nrm.PLAN_PERSIST)
+    gpu = RN.run_gpu("bn_bwd", inp, 1e-5)
+    hw = shape[2] * shape[3]
+    packed = hw % (4 if dtype == "f32" else 8) == 0
+    assert (nrm.last_plan()[0] == nrm.PLAN_PERSIST) == packed
+    again = RN.run_gpu("bn_bwd", inp, 1e-5)
+    for k in gpu:
+        assert (gpu[k] == again[k]).all(), k
+    RN.compare("bn_bwd", inp, gpu, RN.run_oracle(orc, "bn_bwd", inp, 1e-5))
+
+
+def test_bn_bwd_flow_wait_give_up_path(orc):
+    # wait limit 0: every wait of the one-pass backward gives up at once; the
+    # kernel raises the fault bit and ends, and the next call is correct
+    inp = W.make_inputs(W.BN_BWD_F32_32x64x56x56, shape=(8, 16, 40, 40))
+    nrm.force_plan(nrm.PLAN_PERSIST)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    assert nrm.device_fault(clear=True) == 0
+    old = nrm.set_wait_limit(0)
+    try:
+        nrm.bn_bwd(d["dy"], d["x"], d["save_mean"], d["save_rstd"], d["gamma"])
+        bits = nrm.device_fault(clear=True)
+    finally:
+        nrm.set_wait_limit(old)
+    assert nrm.last_plan()[0] == nrm.PLAN_PERSIST
+    assert bits == 1, bits
+    gpu = RN.run_gpu("bn_bwd", inp, 1e-5)
+    RN.compare("bn_bwd", inp, gpu, RN.run_oracle(orc, "bn_bwd", inp, 1e-5))
+    assert nrm.device_fault(clear=True) == 0
