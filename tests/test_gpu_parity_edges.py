@@ -188,6 +188,24 @@ def test_absent_parameters(orc, op):
     _check(orc, op, inp)
 
 
+@pytest.mark.parametrize("plan", [(nrm.PLAN_AUTO,), (nrm.PLAN_CTA, 128, 4), (nrm.PLAN_CTA, 256, 2),
+                                  (nrm.PLAN_PERSIST,), (nrm.PLAN_WARP,), (nrm.PLAN_GENERIC, 256)],
+                         ids=["auto", "cta128x4", "cta256x2", "persist", "warp", "generic"])
+@pytest.mark.parametrize("n", [1024, 2048, 4096])
+def test_ln_small_spread_large_mean_f32(orc, n, plan):
+    # binary32 rows with mean 1000 and spread 1e-3: the statistics must not
+    # lose the spread to the mean's rounding (an error of one binary32 ulp of
+    # 1000 in the mean would move y by 0.06)
+    inp = W.generic_rows("ln", "f32", 16, n, seed=n + 5, scale=1e-3, shift=1000.0)
+    nrm.force_plan(*plan)
+    try:
+        gpu = RN.run_gpu("ln", inp, 1e-12)
+    except nrm.NrmError:
+        pytest.skip("plan does not take this row length")
+    RN.compare("ln", inp, gpu, RN.run_oracle(orc, "ln", inp, 1e-12))
+    nrm.force_plan(nrm.PLAN_AUTO)
+
+
 @pytest.mark.parametrize("dt", DTYPES)
 def test_constant_rows_give_beta_exactly(dt):
     n = 4096
