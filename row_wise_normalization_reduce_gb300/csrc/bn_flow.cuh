@@ -55,7 +55,11 @@ constexpr unsigned kOpen = 0xffffffffu;
 constexpr uint32_t kNone = 0xffffffffu;
 // L2 bytes the lag may keep in flight (the inputs of L channels, their
 // outputs on the way out as well): a fraction of GB300's 126 MB L2.
-constexpr int64_t kFlowL2Budget = (int64_t)40 << 20;
+// NRM_FLOW_L2_MB overrides it for experiments.
+#ifndef NRM_FLOW_L2_MB
+#define NRM_FLOW_L2_MB 40
+#endif
+constexpr int64_t kFlowL2Budget = (int64_t)NRM_FLOW_L2_MB << 20;
 
 struct FlowPlan {
     BnChunks u;           // chunk layout over all channels
