@@ -182,8 +182,10 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         else if (P <= 1024)
             kind = PLAN_CTA;
         else if (P <= 2048) {
+            // LayerNorm: 4 packs per thread (512 x 4 at 16384 bf16: 13.98 us
+            // against 15.64 us for 1024 x 2); the RMS operators keep 2
             kind = PLAN_PERSIST;
-            fpacks = 2;
+            fpacks = op == OP_LN ? 4 : 2;
         } else if (tma_ok) {
             kind = PLAN_TMA;
             fpacks = 4;

@@ -289,12 +289,18 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 //  * at most 2 packs per thread: 1280 threads per SM (five 256-thread CTAs,
 //    at most 51 registers) kept the most row loads in flight; 1024 and 1536
 //    were slower;
-//  * LayerNorm with 4 packs per thread: 896 threads (seven 128-thread CTAs,
-//    at most 73 registers): 12.3 us at 4096 x 4096 bf16 against 13.4 us
-//    uncapped (92 registers, five CTAs) and 12.9 / 12.7 us at six / eight;
-//  * anything else is left uncapped (caps made it spill or run slower).
-// NRM_CTA_MIN_THREADS / NRM_LN4_MIN_THREADS override the two caps for
-// experiments.
+//  * LayerNorm with 4 packs per thread in CTAs of at most 256 threads: 896
+//    threads (seven 128-thread CTAs, at most 73 registers): 12.3 us at
+//    4096 x 4096 bf16 against 13.4 us uncapped (92 registers, five CTAs) and
+//    12.9 / 12.7 us at six / eight; the exact-row instance (no bounds tests,
+//    no spills at 64 registers) 1024 threads: eight CTAs, 10.17-10.19 us
+//    against 10.39-10.40 us at seven (with the row requested before the
+//    dependent-launch wait);
+//  * anything else is left uncapped (caps made it spill or run slower; the
+//    persistent 512 x 4 LayerNorm at 16384 bf16 runs 13.98 us uncapped at 96
+//    registers, one CTA per SM, and 15.9 us capped to two CTAs).
+// NRM_CTA_MIN_THREADS / NRM_LN4_MIN_THREADS / NRM_LN4_FULL_MIN_THREADS
+// override the caps for experiments.
 #ifndef NRM_CTA_MIN_THREADS
 #define NRM_CTA_MIN_THREADS 1280
 #endif
@@ -303,6 +309,9 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 #endif
 #ifndef NRM_LN4_MIN_THREADS
 #define NRM_LN4_MIN_THREADS 896
+#endif
+#ifndef NRM_LN4_FULL_MIN_THREADS
+#define NRM_LN4_FULL_MIN_THREADS 1024
 #endif
 // Launch with programmatic stream serialization when NRM_ROW_PDL (the
 // kernels then order themselves with griddepcontrol.wait).
@@ -323,15 +332,18 @@ inline cudaError_t launch_row(K kernel, unsigned grid, unsigned threads, size_t 
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
-template <int OP, int THREADS, int PACKS>
+template <int OP, int THREADS, int PACKS, bool FULL = false>
 constexpr int row_min_blocks() {
-    return (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0)                 ? NRM_CTA_MIN_THREADS / THREADS
-           : (OP == OP_LN && PACKS == 4 && NRM_LN4_MIN_THREADS / THREADS > 0) ? NRM_LN4_MIN_THREADS / THREADS
-                                                                              : 1;
+    return (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0) ? NRM_CTA_MIN_THREADS / THREADS
+           : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && FULL && NRM_LN4_FULL_MIN_THREADS / THREADS > 0)
+               ? NRM_LN4_FULL_MIN_THREADS / THREADS
+           : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && NRM_LN4_MIN_THREADS / THREADS > 0)
+               ? NRM_LN4_MIN_THREADS / THREADS
+               : 1;
 }
 
 template <int OP, typename T, int THREADS, int PACKS, bool FULL = false>
-__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS>()))
+__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS, FULL>()))
     row_cta_kernel(const RowArgs a, const int64_t pf) {
     constexpr int NW = THREADS / 32;
     __shared__ float s1[2][NW];
@@ -830,7 +842,7 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.threads == TH && p.packs == PK) return launch_persist<OP, T, TH, PK>(a, p, s);
         NRM_PERSIST_CASE(128, 4) NRM_PERSIST_CASE(256, 1) NRM_PERSIST_CASE(256, 2)
         NRM_PERSIST_CASE(256, 4) NRM_PERSIST_CASE(512, 1) NRM_PERSIST_CASE(512, 2)
-        NRM_PERSIST_CASE(1024, 2)
+        NRM_PERSIST_CASE(512, 4) NRM_PERSIST_CASE(1024, 2)
 #undef NRM_PERSIST_CASE
         return cudaErrorInvalidConfiguration;
     } else if (p.kind == PLAN_TMA) {
