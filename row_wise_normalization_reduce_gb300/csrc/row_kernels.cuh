@@ -288,7 +288,9 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 // (CTAs x THREADS)), measured on GB300 with cold L2:
 //  * at most 2 packs per thread: 1280 threads per SM (five 256-thread CTAs,
 //    at most 51 registers) kept the most row loads in flight; 1024 and 1536
-//    were slower;
+//    were slower (add+RMSNorm 4096 x 4096 bf16: 19.17 us against 19.90 and
+//    19.27); plain RMSNorm 1024 threads (2048 x 4096 fp16: 5.92 us against
+//    6.18 at 1280 and 6.15 at 1536);
 //  * LayerNorm with 4 packs per thread in CTAs of at most 256 threads: 896
 //    threads (seven 128-thread CTAs, at most 73 registers): 12.3 us at
 //    4096 x 4096 bf16 against 13.4 us uncapped (92 registers, five CTAs) and
@@ -299,8 +301,8 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 //  * anything else is left uncapped (caps made it spill or run slower; the
 //    persistent 512 x 4 LayerNorm at 16384 bf16 runs 13.98 us uncapped at 96
 //    registers, one CTA per SM, and 15.9 us capped to two CTAs).
-// NRM_CTA_MIN_THREADS / NRM_LN4_MIN_THREADS / NRM_LN4_FULL_MIN_THREADS
-// override the caps for experiments.
+// NRM_CTA_MIN_THREADS / NRM_RMS_MIN_THREADS / NRM_LN4_MIN_THREADS /
+// NRM_LN4_FULL_MIN_THREADS override the caps for experiments.
 #ifndef NRM_CTA_MIN_THREADS
 #define NRM_CTA_MIN_THREADS 1280
 #endif
@@ -312,6 +314,9 @@ __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, co
 #endif
 #ifndef NRM_LN4_FULL_MIN_THREADS
 #define NRM_LN4_FULL_MIN_THREADS 1024
+#endif
+#ifndef NRM_RMS_MIN_THREADS
+#define NRM_RMS_MIN_THREADS 1024
 #endif
 // Launch with programmatic stream serialization when NRM_ROW_PDL (the
 // kernels then order themselves with griddepcontrol.wait).
@@ -334,7 +339,8 @@ inline cudaError_t launch_row(K kernel, unsigned grid, unsigned threads, size_t 
 
 template <int OP, int THREADS, int PACKS, bool FULL = false>
 constexpr int row_min_blocks() {
-    return (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0) ? NRM_CTA_MIN_THREADS / THREADS
+    return (OP == OP_RMS && PACKS <= 2 && NRM_RMS_MIN_THREADS / THREADS > 0) ? NRM_RMS_MIN_THREADS / THREADS
+           : (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0) ? NRM_CTA_MIN_THREADS / THREADS
            : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && FULL && NRM_LN4_FULL_MIN_THREADS / THREADS > 0)
                ? NRM_LN4_FULL_MIN_THREADS / THREADS
            : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && NRM_LN4_MIN_THREADS / THREADS > 0)
