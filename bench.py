@@ -20,7 +20,6 @@ from __future__ import annotations
 import argparse
 import ctypes
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -149,13 +148,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # ncu traffic record (profiles/ncu_traffic.json), valid only for unchanged kernels
 # ---------------------------------------------------------------------------
+# The sources the row kernels (and their plan choice) are built from: a
+# traffic record stays valid while none of them changes.
+ROW_KERNEL_SOURCES = ("api.cpp", "nrm_device.cuh", "nrm_internal.h", "row_kernels.cuh",
+                      "row_pipe.cuh", "rows_add_rms.cu", "rows_ln.cu", "rows_rms.cu")
+
+
 def csrc_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_normalization_reduce_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if f.endswith((".cu", ".cuh", ".cpp", ".h")):
-            h.update(os.path.basename(f).encode())
-            h.update(open(f, "rb").read())
+    for name in ROW_KERNEL_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 

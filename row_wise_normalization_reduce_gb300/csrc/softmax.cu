@@ -80,8 +80,16 @@ __device__ __forceinline__ MaxSum cta_merge_all(MaxSum v, float2 *slot) {
 // CTA plan
 // ---------------------------------------------------------------------------
 // FULL: the row is exactly THREADS x PACKS packs (no bounds tests).
+// Resident 128-thread CTAs per SM the CTA plan is compiled for
+// (NRM_SMX128_MIN_BLOCKS, at most 48 registers at ten): bf16 4096 x 4096 on
+// GB300 11.81 us at ten against 12.23 us uncapped (52 registers, nine CTAs)
+// and 12.45 us at twelve (spills).
+#ifndef NRM_SMX128_MIN_BLOCKS
+#define NRM_SMX128_MIN_BLOCKS 10
+#endif
 template <typename T, int THREADS, int PACKS, bool FULL = false>
-__global__ void __launch_bounds__(THREADS) softmax_cta_kernel(const RowArgs a, const int64_t pf) {
+__global__ void __launch_bounds__(THREADS, (THREADS == 128 ? NRM_SMX128_MIN_BLOCKS : 1))
+    softmax_cta_kernel(const RowArgs a, const int64_t pf) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
