@@ -25,13 +25,19 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+@pytest.mark.parametrize("shape", [(16, 24, 28, 28), (32, 4, 112, 112)],
+                         ids=["cluster_plan", "one_pass_plan"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(shape):
+    # (32, 4, 112, 112): planes too large for a cluster's shared memory, so
+    # both entry points take the one-pass plan, whose control words live in
+    # the library's fixed array for the no-allocation entry point
     import row_wise_normalization_reduce_gb300 as nrm
     from row_wise_normalization_reduce_gb300 import workloads as W
 
     nrm.build()
     lib = nrm.lib()
-    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 24, 28, 28))
+    nrm.force_plan(nrm.PLAN_AUTO)
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape)
     dev = torch.device("cuda", 0)
     x = inp["x"].to(dev)
     g = inp["gamma"].to(dev)
@@ -49,6 +55,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         y, sm, sr = nrm.bn_fwd_train(x, g, b, rm_ref, rv_ref, eps, mom)
         torch.cuda.synchronize()
         refs.append((y.clone(), sm.clone(), sr.clone(), rm_ref.clone(), rv_ref.clone()))
+    want_plan = nrm.PLAN_TMA if shape[2] * shape[3] < 100 * 100 else nrm.PLAN_PERSIST
+    assert nrm.last_plan()[0] == want_plan
 
     # no-allocation entry point through the C ABI: every buffer passed in
     rm = inp["running_mean"].to(dev)
