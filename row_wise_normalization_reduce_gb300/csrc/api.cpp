@@ -157,10 +157,8 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     int fgroups = g_force_groups.load(std::memory_order_relaxed);
 
     // Shared-memory stage of the bulk-copy pipeline: one row of x (and one of
-    // the residual for add+RMS).  Stages are sized to about 96 KB per CTA so
-    // that two or more CTAs fit on an SM.
+    // the residual for add+RMS).
     const int64_t stage_bytes = a.N * (int64_t)elem_size(dtype) * (a.res ? 2 : 1);
-    const int64_t kStageBudget = 96 * 1024;
     // parameters widened to binary32 in shared memory when they fit in 64 KB
     const int64_t param_bytes = a.N * 4 * (op == OP_LN ? 2 : 1);
     const bool smem_params = param_bytes <= 64 * 1024;
