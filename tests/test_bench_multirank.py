@@ -28,7 +28,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_job_value_gloo():
     port = 29500 + (os.getpid() % 1000)
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)

@@ -68,7 +68,7 @@ def _worker(rank, world, port, out):
 
 def test_sync_bn_exchange_gloo():
     port = 29600 + (os.getpid() % 1000)
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
