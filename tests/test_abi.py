@@ -311,3 +311,23 @@ def test_strided_validation(lib):
                               None) == ALIAS
     assert lib.add_rms_fwd_ld(x, 8, y, 16, None, y, 16, y + 4096, 8, None, 3, 8, 1e-6, 0,
                               None) in (OK, DEVICE)
+
+
+def test_header_compiles_as_c(tmp_path):
+    # include/nrm.h is a C interface: it must compile as strict C11 (and C++)
+    # with every warning an error
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = next((p for p in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda")
+                     if p and os.path.exists(os.path.join(p, "include", "cuda_runtime_api.h"))), None)
+    if not gcc or not cuda_inc:
+        pytest.skip("gcc or the CUDA headers not found")
+    src = tmp_path / "use_nrm.c"
+    src.write_text('#include "nrm.h"\n'
+                   "int main(void) { return bn_fwd_train_workspace_size(1, 1, 2, NRM_F32) == 0; }\n")
+    inc = ["-I" + os.path.join(ROOT, "include"), "-I" + os.path.join(cuda_inc, "include")]
+    for lang in (["-x", "c", "-std=c11", "-pedantic"], ["-x", "c++", "-std=c++17"]):
+        r = subprocess.run([gcc, *lang, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", *inc, str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
