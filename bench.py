@@ -69,7 +69,7 @@ def algorithmic_bytes(w: W.Workload, stats: bool = True) -> int:
 
 
 # ---------------------------------------------------------------------------
-# clocks (NVML through ctypes; nvidia-smi as a fallback)
+# clocks (NVML through ctypes; reported as unavailable when NVML cannot be loaded)
 # ---------------------------------------------------------------------------
 REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
            0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
@@ -151,13 +151,14 @@ class ClockSampler:
 # The sources the row kernels (and their plan choice) are built from: a
 # traffic record stays valid while none of them changes.
 ROW_KERNEL_SOURCES = ("api.cpp", "nrm_device.cuh", "nrm_internal.h", "row_kernels.cuh",
-                      "row_pipe.cuh", "rows_add_rms.cu", "rows_ln.cu", "rows_rms.cu")
+                      "row_pipe.cuh")  # and every rows_*.cu instance file
 
 
 def csrc_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_normalization_reduce_gb300", "csrc")
-    for name in ROW_KERNEL_SOURCES:
+    inst = sorted(f for f in os.listdir(csrc) if f.startswith("rows_") and f.endswith(".cu"))
+    for name in ROW_KERNEL_SOURCES + tuple(inst):
         h.update(name.encode())
         h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
@@ -201,13 +202,14 @@ def plan_name(op, kind_name):
 class Step:
     """One call of the hot path on rotating, pre-filled device buffers."""
 
-    def __init__(self, w: W.Workload, device, l2_bytes: int):
+    def __init__(self, w: W.Workload, device, l2_bytes: int, hot: bool = False):
         import row_wise_normalization_reduce_gb300 as nrm
         self.nrm = nrm
         self.w = w
         inp = W.make_inputs(w)
         per_set = algorithmic_bytes(w)
-        self.nsets = max(2, int(np.ceil(3 * l2_bytes / per_set)) + 1)
+        # cold: rotating input sets totalling > 3x L2; hot: one set, reused
+        self.nsets = 1 if hot else max(2, int(np.ceil(3 * l2_bytes / per_set)) + 1)
         dev = lambda t: t.to(device)  # noqa: E731
         self.params = {k: dev(v) for k, v in inp.items() if k not in ("x", "residual", "dy")}
         self.sets = []
@@ -311,6 +313,133 @@ def time_graphs(step: Step, k: int, warmup: int, stream, chunk=1000, dist=None):
     if dist is not None:
         dist.barrier()
     return ev0.elapsed_time(ev1) / 1e3, t0, t1
+
+
+# ---------------------------------------------------------------------------
+# per-call timings of one workload (the isolated-call protocol with an L2
+# scrub before each call, hot back-to-back calls, and a drained variant of the
+# graph replay)
+# ---------------------------------------------------------------------------
+def _cudart():
+    """The CUDA runtime torch already loaded (for cudaMemsetAsync), or None."""
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            rt.cudaMemsetAsync.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t,
+                                           ctypes.c_void_p]
+            rt.cudaMemsetAsync.restype = ctypes.c_int
+            return rt
+        except (OSError, AttributeError):
+            continue
+    return None
+
+
+class Scrub:
+    """Evicts L2 between calls.  write(): cudaMemsetAsync of 4x L2 bytes on
+    the stream (the call then starts with L2 full of dirty lines it must
+    write back as it evicts them); read(): a reduction that reads 4x L2 bytes
+    (L2 is left holding clean lines only, as after a flush and invalidate)."""
+
+    def __init__(self, device, l2_bytes, stream):
+        self.nbytes = 4 * l2_bytes
+        self.buf = torch.empty(self.nbytes // 4, dtype=torch.float32, device=device)
+        self.buf.zero_()
+        self.out = torch.empty((), dtype=torch.float32, device=device)
+        self.stream = stream
+        self.rt = _cudart()
+        self.how = "cudaMemsetAsync" if self.rt is not None else "torch fill (no cudart handle)"
+
+    def write(self):
+        if self.rt is not None:
+            st = self.rt.cudaMemsetAsync(ctypes.c_void_p(self.buf.data_ptr()), 0, self.nbytes,
+                                         ctypes.c_void_p(self.stream.cuda_stream))
+            if st != 0:
+                raise RuntimeError(f"cudaMemsetAsync failed ({st})")
+        else:
+            self.buf.fill_(0.0)
+
+    def read(self):
+        torch.sum(self.buf, dim=0, out=self.out)
+
+
+def time_isolated(step, stream, scrub, warm=50, timed=50, reps=5):
+    """Section 8(d)'s isolated-call protocol: before every call the L2 is
+    scrubbed (outside the events); CUDA events bracket the call alone.
+    Median over `timed` calls, median of `reps` repeats; seconds."""
+    meds = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(timed)]
+            # a head start for the GPU (a bounded spin kernel of about 30 ms):
+            # every call below is queued before the GPU reaches it, so no
+            # host launch gap falls between an event pair
+            torch.cuda._sleep(60_000_000)
+            for i in range(warm + timed):
+                scrub()
+                if i >= warm:
+                    evs[i - warm][0].record(stream)
+                step()
+                if i >= warm:
+                    evs[i - warm][1].record(stream)
+            torch.cuda.synchronize()
+            meds.append(statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3)
+    return statistics.median(meds)
+
+
+def time_drained(step, stream, scrub, k=200, reps=5):
+    """The graph replay with the write-back of every call inside the timed
+    region: L2 is emptied of dirty lines before ev0 (a read scrub), and a read
+    scrub after the k calls, before ev1, writes back what the last calls left
+    in L2; the time of the same read scrub on a clean L2 is subtracted.
+    Median of `reps`; seconds per call."""
+    g = capture(step, k, stream)
+    out = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            scrub.read()
+            e[0].record(stream)
+            scrub.read()          # on a clean L2: the scrub's own time
+            e[1].record(stream)
+            scrub.read()
+            e[2].record(stream)
+            g.replay()
+            scrub.read()          # writes back the calls' last dirty lines
+            e[3].record(stream)
+            torch.cuda.synchronize()
+            out.append((e[2].elapsed_time(e[3]) - e[0].elapsed_time(e[1])) / 1e3 / k)
+    return statistics.median(out)
+
+
+def target_line(w: W.Workload, device, stream, l2, peak):
+    """Every timing of one target workload (graph replay cold and hot,
+    isolated calls after a write or a read scrub, drained replay)."""
+    b = algorithmic_bytes(w)
+    cold = Step(w, device, l2)
+    t_graph, _, _ = time_graphs(cold, 2000, 20, stream)
+    t_graph /= 2000
+    scrub = Scrub(device, l2, stream)
+    t_iso_w = time_isolated(cold, stream, scrub.write)
+    t_iso_r = time_isolated(cold, stream, scrub.read)
+    t_drain = time_drained(cold, stream, scrub)
+    plan = cold.plan
+    del cold
+    torch.cuda.empty_cache()
+    hot = Step(w, device, l2, hot=True)
+    t_hot, _, _ = time_graphs(hot, 2000, 20, stream)
+    t_hot /= 2000
+    del hot, scrub
+    torch.cuda.empty_cache()
+
+    def entry(t):
+        return {"us": round(t * 1e6, 3), "frac": round(b / t / 1e9 / peak, 4),
+                "frac8": round(b / t / 1e9 / 8000.0, 4)}
+
+    return {"bytes": b, "plan": plan,
+            "graph_cold": entry(t_graph), "graph_hot": entry(t_hot),
+            "isolated_cold_memset": entry(t_iso_w), "isolated_cold_clean": entry(t_iso_r),
+            "graph_cold_drained": entry(t_drain)}
 
 
 def time_e2e(w: W.Workload, device, steps: int):
@@ -455,6 +584,13 @@ def base_line(args, w, world):
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded torch.Generator)"}
 
 
+def workload_config(w: W.Workload, world: int) -> dict:
+    """The workload as both arms name it (identical dicts)."""
+    return {"workload": w.name, "shape": list(w.shape), "dtype": w.dtype, "eps": w.eps,
+            "parallelism": f"replicas x{world} (rows are independent)",
+            "l2": "cold: rotating input sets totalling more than 3x L2, used round-robin"}
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -471,8 +607,7 @@ def run_reference(args, w, rank, world):
     line = base_line(args, w, world)
     line.update({
         "impl": "reference", "value": gbs, "ms_per_step": sec * 1e3,
-        "config": {"workload": w.name, "shape": list(w.shape), "dtype": w.dtype,
-                   "sample_rows": rows, "l2": "n/a (CPU)"},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} of {w.shape[0]} rows per step, fp64 oracle, "
                                    f"rows split over {threads} threads"},
@@ -576,10 +711,11 @@ def secondary(args, device, stream, l2):
         sec, _, _ = time_graphs(st, k, 20, stream)
         per = sec / k
         peak, _ = measured_peak()
-        out.append({"workload": name, "us_per_call": per * 1e6, "gbs": b / per / 1e9,
-                    "frac_of_measured_peak": b / per / 1e9 / peak,
-                    "frac_of_8tbs": b / per / 1e9 / 8000.0, "bytes": b,
-                    "launches_per_call": st.launches_per_step, "plan": st.plan})
+        # compact keys: us per call, fraction of the measured peak and of 8 TB/s
+        out.append({"w": name, "us": round(per * 1e6, 3),
+                    "frac": round(b / per / 1e9 / peak, 4),
+                    "frac8": round(b / per / 1e9 / 8000.0, 4), "plan": st.plan,
+                    "launches": st.launches_per_step})
         del st
         torch.cuda.empty_cache()
     return out
@@ -595,6 +731,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the per-call timings of the two 4096x4096 bf16 targets")
     ap.add_argument("--plan", default="auto",
                     help="row-operator plan: auto, generic:T, warp:T:P, cta:T:P or "
                          "tma:T:P:STAGES:GROUPS (for measurements and profiling)")
@@ -655,6 +793,23 @@ def main():
     if rank == 0 and not args.no_secondary:
         sec_lines = secondary(args, device, stream, l2)
 
+    targets = None
+    if rank == 0 and not args.no_targets:
+        peak, _ = measured_peak()
+        tsampler = ClockSampler(local, period_s=0.02)
+        tsampler.start()
+        targets = {t.name: target_line(t, device, stream, l2, peak)
+                   for t in (W.ADD_RMS_BF16_4096x4096, W.LN_BF16_4096x4096)}
+        tsampler.stop()
+        ts = tsampler.summary()
+        targets["clocks"] = {"sm_mhz": ts["sm_mhz"], "reasons": ts["reasons"]}
+        targets["how"] = ("graph_*: K calls replayed from a CUDA graph, per call (cold: rotating "
+                          "sets > 3x L2; hot: one set); isolated_*: events around one call after "
+                          "a 4x L2 scrub, median of 50, median of 5 repeats (memset: the scrub "
+                          "writes, so the call first writes back dirty lines; clean: the scrub "
+                          "reads); drained: graph replay plus the write-back of the last calls' "
+                          "dirty lines; frac of the measured peak, frac8 of 8 TB/s")
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not w.op.startswith("bn"):
         rows = w.shape[0]
@@ -668,11 +823,10 @@ def main():
         line = base_line(args, w, world)
         line.update({
             "value": value, "ms_per_step": per_step * 1e3, "us_per_call": per_step * 1e6,
-            "config": {"workload": w.name, "shape": list(w.shape), "dtype": w.dtype,
-                       "eps": w.eps, "parallelism": f"replicas x{world} (rows are independent)",
-                       "l2": f"cold: {step.nsets} rotating input sets "
-                             f"({step.nsets * nbytes / 1e6:.0f} MB) > L2 ({l2 / 1e6:.0f} MB)",
-                       "timing": "CUDA graphs replaying exactly K calls between CUDA events"},
+            "config": workload_config(w, world),
+            "timing": (f"CUDA graphs replaying exactly K calls between CUDA events; "
+                       f"{step.nsets} rotating input sets ({step.nsets * nbytes / 1e6:.0f} MB) "
+                       f"> L2 ({l2 / 1e6:.0f} MB)"),
             "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s",
                          "frac": kernel_gbs / peak, "peak_source": peak_src,
                          "frac_of_nominal_8tbs": kernel_gbs / 8000.0,
@@ -687,6 +841,8 @@ def main():
             line["cpu_baseline"] = cpu
         if sec_lines is not None:
             line["secondary"] = sec_lines
+        if targets is not None:
+            line["targets"] = targets  # last, so the end of the line carries both targets
         emit(line)
     if dist is not None:
         dist.destroy_process_group()

@@ -364,8 +364,13 @@ typedef enum {
                                with bulk asynchronous copies */
     NRM_PLAN_PERSIST = 5,   /* persistent CTAs; the next row is loaded into
                                registers while the current one is reduced */
-    NRM_PLAN_WRAW = 6       /* warp per row, the whole row's packs in registers,
+    NRM_PLAN_WRAW = 6,      /* warp per row, the whole row's packs in registers,
                                shuffle-only reductions */
+    NRM_PLAN_CLUSTER = 7    /* one row split over the CTAs of a thread-block
+                               cluster (`groups` = CTAs per cluster: 2, 4 or
+                               8, dividing the row's 16-byte packs); each CTA
+                               holds a contiguous slice in registers and the
+                               row sums meet in distributed shared memory */
 } nrm_plan;
 
 /*
@@ -380,7 +385,10 @@ typedef enum {
  * follows the forced plan too: NRM_PLAN_CTA selects its streaming two-kernel
  * plan (per-plane statistics into the workspace, then a dependent launch that
  * normalizes), NRM_PLAN_TMA one cluster of CTAs per channel (shared memory and
- * distributed shared memory, no workspace), NRM_PLAN_PERSIST the one-pass
+ * distributed shared memory, no workspace; as measurement hooks, `stages`
+ * of 2, 4 or 8 sets the CTAs per cluster and a non-zero `threads` caps the
+ * number of clusters, each then taking several channels in turn),
+ * NRM_PLAN_PERSIST the one-pass
  * plan (a reset of the workspace's control words, then one kernel whose
  * CTAs take statistics items and normalize items in a fixed interleaved
  * order, x read once from HBM; `stages` sets its L2 prefetch of the chunks

@@ -8,7 +8,7 @@ package is the thin Python binding over that library.
 """
 from ._binding import (  # noqa: F401
     LIB_PATH, NRM_BF16, NRM_F16, NRM_F32, PLAN_AUTO, PLAN_CTA, PLAN_GENERIC, PLAN_NAMES,
-    PLAN_PERSIST, PLAN_TMA, PLAN_WRAW, PLAN_WARP, NrmError, add_rms_fwd, bn_bwd,
+    PLAN_CLUSTER, PLAN_PERSIST, PLAN_TMA, PLAN_WRAW, PLAN_WARP, NrmError, add_rms_fwd, bn_bwd,
     bn_bwd_workspace_size, bn_fwd_infer, bn_fwd_train, bn_fwd_train_noalloc,
     bn_fwd_train_workspace_size, device_fault, force_plan, last_plan, lib, ln_fwd, rms_fwd,
     set_bn_group_bytes, set_pointer_checks, set_wait_limit, softmax_fwd, status_string,

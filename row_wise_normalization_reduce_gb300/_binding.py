@@ -16,8 +16,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libnrm.so")
 
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
-PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA, PLAN_TMA, PLAN_PERSIST, PLAN_WRAW = range(7)
-PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta", 4: "tma", 5: "persist", 6: "wraw"}
+PLAN_AUTO, PLAN_GENERIC, PLAN_WARP, PLAN_CTA, PLAN_TMA, PLAN_PERSIST, PLAN_WRAW, PLAN_CLUSTER = range(8)
+PLAN_NAMES = {0: "auto", 1: "generic", 2: "warp", 3: "cta", 4: "tma", 5: "persist", 6: "wraw",
+              7: "cluster"}
 
 _DT = {torch.float32: NRM_F32, torch.float16: NRM_F16, torch.bfloat16: NRM_BF16}
 
@@ -277,11 +278,10 @@ def bn_fwd_train_workspace_size(batch, c, hw, dtype=torch.float32) -> int:
     return lib().bn_fwd_train_workspace_size(batch, c, hw, _DT[dtype])
 
 
-def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, eps=1e-5,
-                 momentum=0.1, *, out=None, save_mean=None, save_rstd=None, workspace=None,
-                 stream=None):
-    """BatchNorm2d training forward over NCHW x.  Returns (y, save_mean, save_rstd);
-    running_mean / running_var (binary32) are updated in place when given."""
+def _bn_train_tensors(x, gamma, beta, running_mean, running_var, out, save_mean, save_rstd):
+    """Checks shared by both training-forward entry points; allocates the
+    outputs that are None.  Returns (batch, c, hw, gamma, beta, y, save_mean,
+    save_rstd)."""
     _cuda(x, "x")
     if x.dim() < 2:
         raise ValueError("x must be [batch, C, ...]")
@@ -289,14 +289,29 @@ def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, 
     hw = x.numel() // (batch * c) if batch * c else 0
     gamma = _param(gamma, c, x.dtype, x.device, "gamma")
     beta = _param(beta, c, x.dtype, x.device, "beta")
-    for t, name in ((running_mean, "running_mean"), (running_var, "running_var")):
+    for t, name in ((running_mean, "running_mean"), (running_var, "running_var"),
+                    (save_mean, "save_mean"), (save_rstd, "save_rstd")):
         if t is not None:
             _cuda(t, name)
-            if t.dtype != torch.float32 or t.numel() != c:
-                raise ValueError(f"{name} must be [{c}] float32")
+            if t.dtype != torch.float32 or t.numel() != c or t.device != x.device:
+                raise ValueError(f"{name} must be [{c}] float32 on {x.device}")
+    if out is not None:
+        _cuda(out, "out")
+        if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+            raise ValueError("out must be like x")
     y = torch.empty_like(x) if out is None else out
     save_mean = torch.empty(c, device=x.device, dtype=torch.float32) if save_mean is None else save_mean
     save_rstd = torch.empty(c, device=x.device, dtype=torch.float32) if save_rstd is None else save_rstd
+    return batch, c, hw, gamma, beta, y, save_mean, save_rstd
+
+
+def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, eps=1e-5,
+                 momentum=0.1, *, out=None, save_mean=None, save_rstd=None, workspace=None,
+                 stream=None):
+    """BatchNorm2d training forward over NCHW x.  Returns (y, save_mean, save_rstd);
+    running_mean / running_var (binary32) are updated in place when given."""
+    batch, c, hw, gamma, beta, y, save_mean, save_rstd = _bn_train_tensors(
+        x, gamma, beta, running_mean, running_var, out, save_mean, save_rstd)
     need = lib().bn_fwd_train_workspace_size(batch, c, hw, _dtype_code(x))
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=x.device, dtype=torch.uint8)
@@ -313,19 +328,20 @@ def bn_fwd_train(x, gamma=None, beta=None, running_mean=None, running_var=None, 
 def bn_fwd_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_var=None,
                          eps=1e-5, momentum=0.1, *, out, save_mean, save_rstd, stream=None):
     """bn_fwd_train for callers that cannot allocate device memory at call time:
-    every output is passed in, and the library keeps the partial statistics in
-    a fixed array of its own (batch * C <= 65536).  Returns (y, save_mean,
-    save_rstd)."""
-    _cuda(x, "x")
-    batch, c = x.shape[0], x.shape[1]
-    hw = x.numel() // (batch * c) if batch * c else 0
+    every output is passed in (same checks as bn_fwd_train), and the library
+    keeps the partial statistics in a fixed array of its own (batch * C <=
+    65536).  Returns (y, save_mean, save_rstd)."""
+    if out is None or save_mean is None or save_rstd is None:
+        raise ValueError("bn_fwd_train_noalloc allocates nothing: pass out, save_mean and save_rstd")
+    batch, c, hw, gamma, beta, y, save_mean, save_rstd = _bn_train_tensors(
+        x, gamma, beta, running_mean, running_var, out, save_mean, save_rstd)
     with torch.cuda.device(x.device):
         st = lib().bn_fwd_train_noalloc(
-            _ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(save_mean), _ptr(save_rstd),
+            _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(save_mean), _ptr(save_rstd),
             _ptr(running_mean), _ptr(running_var), batch, c, hw, eps, momentum, _dtype_code(x),
             stream if stream is not None else _stream(x.device))
     _check(st, "bn_fwd_train_noalloc")
-    return out, save_mean, save_rstd
+    return y, save_mean, save_rstd
 
 
 def softmax_fwd(x, *, out=None, row_max=None, row_sum=None, want_stats=False, stream=None):

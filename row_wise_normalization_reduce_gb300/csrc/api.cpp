@@ -271,6 +271,22 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
         p.stages = fstages;
         break;
     }
+    case PLAN_CLUSTER: {
+        // one row over a cluster of CS CTAs (p.groups), each a contiguous
+        // slice of S = P / CS packs held as THREADS x PACKS
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        const int cs = fgroups ? fgroups : (P >= 2048 ? 4 : 2);
+        if ((cs != 2 && cs != 4 && cs != 8) || P % cs) return NRM_ERR_UNSUPPORTED;
+        const int64_t S = P / cs;
+        int packs = fpacks, threads = fthreads ? fthreads : 128;
+        if (!packs) packs = S <= 128 ? 1 : S <= 256 ? 2 : 4;
+        if ((int64_t)threads * packs < S) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.groups = cs;
+        p.grid = (a.rows < kMaxGrid / cs ? a.rows : kMaxGrid / cs) * cs;
+        break;
+    }
     case PLAN_TMA: {
         // Row groups of GT threads x PACKS packs (4 preferred), as many groups
         // per CTA as fit in 1024 threads and the shared memory with 3 (else 2)
@@ -363,6 +379,20 @@ int choose_softmax_plan(const RowArgs &a, int dtype, const DevInfo &dev, Plan *p
         p.packs = packs;
         p.prefetch = fstages == 0 ? 1 : fstages - 1;
         p.stages = fstages;
+    } else if (kind == PLAN_CLUSTER) {
+        // one row over a cluster of CS CTAs (p.groups), as the norms' plan
+        if (!vec_ok) return NRM_ERR_UNSUPPORTED;
+        const int fgroups = g_force_groups.load(std::memory_order_relaxed);
+        const int cs = fgroups ? fgroups : 4;
+        if ((cs != 2 && cs != 4 && cs != 8) || P % cs) return NRM_ERR_UNSUPPORTED;
+        const int64_t S = P / cs;
+        if (!threads) threads = 128;
+        if (!packs) packs = S <= 128 ? 1 : S <= 256 ? 2 : 4;
+        if ((int64_t)threads * packs < S) return NRM_ERR_UNSUPPORTED;
+        p.threads = threads;
+        p.packs = packs;
+        p.groups = cs;
+        p.grid = (a.rows < kMaxGrid / cs ? a.rows : kMaxGrid / cs) * cs;
     } else {
         return NRM_ERR_UNSUPPORTED;
     }
@@ -605,29 +635,39 @@ size_t bn_fwd_train_workspace_size(int64_t batch, int64_t C, int64_t HW, int dty
     return bn_flow_ws_bytes(C, batch * C * nch);
 }
 
-int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
-                 float *save_rstd, float *running_mean, float *running_var, int64_t batch,
-                 int64_t C, int64_t HW, float eps, float momentum, int dtype, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The BatchNorm training forward behind both entry points: bn_fwd_train
+// (caller workspace) and bn_fwd_train_noalloc (fixed == true: the library's
+// fixed partials array, bn_fixed_workspace in bn.cu).  Same validation, plan
+// choice, wait limit and plan record for both.
+int bn_train_call(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
+                  float *save_rstd, float *running_mean, float *running_var, int64_t batch,
+                  int64_t C, int64_t HW, float eps, float momentum, int dtype, void *workspace,
+                  size_t workspace_bytes, bool fixed, cudaStream_t stream) {
     if (!dtype_ok(dtype)) return NRM_ERR_DTYPE;
     if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
     const size_t es = elem_size(dtype);
     if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / es)
         return NRM_ERR_SHAPE;
     if (batch * HW < 2) return NRM_ERR_SHAPE;
+    if (fixed && batch * C > kBnFixedPlanes) return NRM_ERR_TOO_LARGE;
     if (!eps_ok(eps) || !(momentum >= 0.f && momentum <= 1.f)) return NRM_ERR_VALUE;
     if (!x || !y) return NRM_ERR_NULL;
     int st;
     if ((st = check_elem_alignment({x, gamma, beta, y}, es)) != NRM_OK) return st;
     if ((st = check_elem_alignment({save_mean, save_rstd, running_mean, running_var}, 4)) != NRM_OK)
         return st;
-    const size_t need = bn_fwd_train_workspace_size(batch, C, HW, dtype);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return NRM_ERR_WORKSPACE;
+    const size_t need = fixed ? 0 : bn_fwd_train_workspace_size(batch, C, HW, dtype);
+    if (!fixed && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return NRM_ERR_WORKSPACE;
     const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es;
     const Span sx = span(x, tb), sy = span(y, tb), sg = span(gamma, C * es), sb = span(beta, C * es),
                ssm = span(save_mean, C * 4), ssr = span(save_rstd, C * 4),
                srm = span(running_mean, C * 4), srv = span(running_var, C * 4),
-               sws = span(workspace, need);
+               sws = span(fixed ? nullptr : workspace, need);
     const Span outs[] = {sy, ssm, ssr, srm, srv, sws};
     const Span ins[] = {sx, sg, sb};
     for (const Span &o : outs)
@@ -637,19 +677,58 @@ int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, fl
         for (int j = i + 1; j < 6; ++j)
             if (overlap(outs[i], outs[j])) return NRM_ERR_ALIAS;
     if ((st = check_pointers({x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var,
-                              workspace})) != NRM_OK)
+                              fixed ? nullptr : workspace})) != NRM_OK)
         return st;
     DevInfo dev;
     if ((st = device_info(&dev)) != NRM_OK) return st;
+    if (fixed && (st = bn_fixed_workspace(&workspace, &workspace_bytes)) != NRM_OK) return st;
+    int bn_plan = bn_plan_from_forced();
+    if (fixed) {
+        // the streaming plan keeps one partial per chunk of at most
+        // kBnChunkPacks packs; when those do not fit the fixed array, the
+        // other plans (per-plane partials, or none) still do
+        const int64_t V = 16 / (int64_t)es;
+        const int64_t nch = ((HW + V - 1) / V + kBnChunkPacks - 1) / kBnChunkPacks;
+        if (batch * C * nch > kBnFixedPlanes &&
+            (bn_plan == BN_PLAN_AUTO || bn_plan == BN_PLAN_STREAM))
+            bn_plan = BN_PLAN_NO_STREAM;
+    }
     BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
              eps, momentum, workspace, fault_word(), g_wait_limit.load(std::memory_order_relaxed),
-             bn_plan_from_forced(), workspace_bytes, 0, 0};
+             bn_plan, workspace_bytes, 0, 0};
     if (g_force_kind.load(std::memory_order_relaxed) == PLAN_PERSIST) {
         a.prefetch = g_force_stages.load(std::memory_order_relaxed);
         a.packs = g_force_packs.load(std::memory_order_relaxed);
     }
+    if (g_force_kind.load(std::memory_order_relaxed) == PLAN_TMA) {
+        a.cluster_size = g_force_stages.load(std::memory_order_relaxed);
+        a.max_clusters = g_force_threads.load(std::memory_order_relaxed);
+    }
     int used = 0;
     return record_bn(launch_bn_train(a, dtype, dev.sms, stream, &used), used);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bn_fwd_train(const void *x, const void *gamma, const void *beta, void *y, float *save_mean,
+                 float *save_rstd, float *running_mean, float *running_var, int64_t batch,
+                 int64_t C, int64_t HW, float eps, float momentum, int dtype, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+    return bn_train_call(x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch,
+                         C, HW, eps, momentum, dtype, workspace, workspace_bytes, false, stream);
+}
+
+// No page has this entry point: bn_fwd_train for callers that cannot allocate
+// device memory when they call (the header says who and why).  The partials
+// live in the library's fixed array (bn.cu).
+int bn_fwd_train_noalloc(const void *x, const void *gamma, const void *beta, void *y,
+                         float *save_mean, float *save_rstd, float *running_mean,
+                         float *running_var, int64_t batch, int64_t C, int64_t HW, float eps,
+                         float momentum, int dtype, cudaStream_t stream) {
+    return bn_train_call(x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch,
+                         C, HW, eps, momentum, dtype, nullptr, 0, true, stream);
 }
 
 int bn_fwd_infer(const void *x, const void *gamma, const void *beta, void *y,
@@ -903,7 +982,7 @@ const char *nrm_status_string(int status) {
 }
 
 int nrm_force_plan(int plan, int threads, int packs, int stages, int groups) {
-    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_WRAW || threads < 0 || packs < 0 || stages < 0 ||
+    if (plan < NRM_PLAN_AUTO || plan > NRM_PLAN_CLUSTER || threads < 0 || packs < 0 || stages < 0 ||
         stages > kMaxStages || groups < 0 || groups > 15)
         return NRM_ERR_UNSUPPORTED;
     g_force_kind.store(plan);

@@ -289,31 +289,39 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a, co
 // The cs CTAs split the batch: CTA rank r owns planes n in [r*ppc,
 // min((r+1)*ppc, batch)) of the channel.  Each CTA has two shared-memory
 // buffers: while channel i is reduced and written from one buffer, the planes
-// of channel i+1 stream into the other (one bulk asynchronous copy per
-// plane), so x is read from HBM once and loads overlap the stores.
+// of channel i+1 stream into the other (one bulk asynchronous copy per plane,
+// each completing on its own mbarrier), so x is read from HBM once and loads
+// overlap the stores.
 //
-// Per channel a CTA computes the statistics of its planes with a shifted,
-// corrected two-pass over shared memory (shift K = x[0, c, 0], so channels
-// with a large mean lose nothing to cancellation), publishes (count, mean,
-// M2), and after a cluster barrier every CTA folds the cs partials over
-// distributed shared memory in rank order (all agree bit for bit), then
-// normalizes its planes and writes y.  Rank 0 writes save_mean/save_rstd and
-// the running statistics.  The barrier that protects the partials is split:
-// each CTA arrives right after its fold and waits only before it writes the
-// next channel's partial (or exits), so it overlaps the stores of y.  The
-// bulk-copy waits are bounded; on a give-up the CTA raises a fault bit, keeps
-// taking part in every barrier, and drains its copies before exiting.
+// Statistics in one pass, plane by plane as the copies land: thread t keeps
+// (count, sum e, sum e^2) of e = x - K_t over its packs, K_t its own first
+// value (a per-thread shift: a far-off K_t only affects that thread's few
+// values, whose sums stay small).  From these each thread forms its mean
+// relative to the channel shift K = x[0, c, 0] and its M2; the CTA merges
+// them exactly with two CTA-wide sums (the mean, then M2_t + n_t (m_t -
+// m)^2, a sum of non-negative terms), publishes (count, mean, M2), and after
+// a cluster barrier every CTA folds the cs partials over distributed shared
+// memory in rank order (all agree bit for bit).  Then it normalizes its
+// planes, y = ((x - K) - md) * (rstd * gamma) + beta, and writes y.  Rank 0
+// writes save_mean/save_rstd and the running statistics.  The barrier that
+// protects the partials is split: each CTA arrives right after its fold and
+// waits only before it writes the next channel's partial (or exits), so it
+// overlaps the stores of y.  Every bulk-copy wait is bounded; on a give-up
+// the thread raises a fault bit, the CTA stops issuing copies, keeps taking
+// part in every barrier, and drains its copies in flight before exiting.
 // ---------------------------------------------------------------------------
 constexpr int BNC_THREADS = 512;
+constexpr int kBnMaxPpc = 16;  // planes per CTA (one mbarrier each per buffer)
 
 template <typename T>
-__device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uint64_t *bar,
+__device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uint64_t *bars,
                                                 int64_t c, int64_t n0, int np, int q,
                                                 uint32_t plane_bytes) {
-    mbar_arrive_expect_tx(bar, plane_bytes * (uint32_t)np);
-    for (int j = 0; j < np; ++j)
+    for (int j = 0; j < np; ++j) {
+        mbar_arrive_expect_tx(&bars[j], plane_bytes);
         bulk_g2s(buf + (size_t)j * q, static_cast<const T *>(a.x) + ((n0 + j) * a.C + c) * a.HW,
-                 plane_bytes, bar);
+                 plane_bytes, &bars[j]);
+    }
 }
 
 // Four 512-thread CTAs per SM (at most 32 registers): with fewer, the 8-CTA
@@ -323,14 +331,15 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     namespace cg = cooperative_groups;
     using io2 = IO2<T>;
     constexpr int H = io2::H;
+    constexpr int V = IO<T>::V;
     constexpr int NW = BNC_THREADS / 32;
     extern __shared__ __align__(16) uint4 sx[];  // two buffers of ppc planes
-    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ __align__(8) uint64_t bar[2][kBnMaxPpc];
     __shared__ float s1[2][NW];
-    __shared__ float2 s2[2][NW];
-    __shared__ float part[2][3];  // count, mean, M2 of this CTA's planes (shifted)
+    __shared__ float s2[2][NW];
+    __shared__ float part[2][3];  // count, mean, M2 of this CTA's planes (shifted by K)
     __shared__ float stat[2][3];  // combined shifted mean, rstd, biased variance
-    __shared__ int s_ok[2];
+    __shared__ int s_fail;        // some wait of this CTA gave up
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
@@ -342,15 +351,16 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     const int64_t n0 = (int64_t)rank * ppc;
     const int64_t left = a.batch - n0;
     const int np = (int)(left <= 0 ? 0 : left < ppc ? left : ppc);
-    const int q = (int)(HW / IO<T>::V);  // 16-byte packs per plane
+    const int q = (int)(HW / V);  // 16-byte packs per plane
+    const int tp = np * q;        // packs of this CTA's planes
     const uint32_t plane_bytes = (uint32_t)(HW * (int64_t)sizeof(T));
     const size_t buf_packs = (size_t)ppc * q;
     const float cnt = (float)np * (float)HW;
     const float ctot = (float)(a.batch * HW);
 
-    // thread 0's bookkeeping: iteration whose planes were last issued into /
-    // last received from each buffer (for the drain after a give-up)
-    int last_issued0 = -1, last_issued1 = -1, last_done0 = -1, last_done1 = -1;
+    // thread 0's bookkeeping: iteration whose planes were last issued into
+    // each buffer (for the drain after a give-up)
+    int last_issued0 = -1, last_issued1 = -1;
     // programmatic dependent launch: the CTA's planes of its first channel are
     // requested from L2 before the wait for the previous grid (L2 is where
     // that grid's writes become coherent; the bulk copies come after the wait)
@@ -360,13 +370,16 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        s_fail = 0;
+        for (int j = 0; j < np; ++j) {
+            mbar_init(&bar[0][j], 1);
+            mbar_init(&bar[1][j], 1);
+        }
         fence_mbar_init();
         for (int b = 0; b < 2; ++b) {
             const int64_t c = first_c + b * K_clusters;
             if (np > 0 && c < C) {
-                bn_issue_planes<T>(a, sx + b * buf_packs, &bar[b], c, n0, np, q, plane_bytes);
+                bn_issue_planes<T>(a, sx + b * buf_packs, bar[b], c, n0, np, q, plane_bytes);
                 if (b == 0) last_issued0 = 0;
                 else last_issued1 = 1;
             }
@@ -374,62 +387,58 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     }
     __syncthreads();
 
-    bool gave_up = false;  // identical in every thread (read from s_ok)
     int i = 0;
     for (int64_t c = first_c; c < C; c += K_clusters, ++i) {
         const int b = i & 1;
         const uint4 *buf = sx + b * buf_packs;
+        const uint32_t par = (uint32_t)((i >> 1) & 1);
+        const float K = bn_elem<T>(a.x, c * HW);  // x[0, c, 0]
         // second half of the previous channel's barrier: every peer has folded
         // that channel's partials before any partial is written again
         if (i > 0) cluster_wait();
-        // one thread waits on the copies; the CTA barrier releases the rest
-        if (tid == 0) {
-            // after a give-up nothing more is issued: do not wait again
-            const bool got = np == 0 ||
-                             (!gave_up && mbar_wait_bounded(&bar[b], (uint32_t)((i >> 1) & 1), a.wait_limit));
-            if (!got && np > 0 && !gave_up) atomicOr(a.fault, FAULT_WAIT);
-            if (got && np > 0) {
-                if (b == 0) last_done0 = i;
-                else last_done1 = i;
-            }
-            s_ok[b] = got;
-        }
-        __syncthreads();
-        gave_up = gave_up || !s_ok[b];
-        const float K = bn_elem<T>(a.x, c * HW);  // x[0, c, 0]
 
-        // pass 1: sum of d = x - K over this CTA's planes
-        const float2 nk = f2(-K);
-        float2 acc = f2(0.f);
-        for (int j = 0; j < np; ++j)
-            for (int k = tid; k < q; k += BNC_THREADS) {
-                float2 f[H];
-                io2::unpack(buf[(size_t)j * q + k], f);
-#pragma unroll
-                for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, __fadd2_rn(f[h], nk));
+        // one pass, plane by plane as the copies land (flat pack index idx of
+        // the buffer; thread t owns idx = t, t + THREADS, ...)
+        float tn = 0.f, tK = 0.f;
+        bool have = false;
+        float2 a1 = f2(0.f), a2 = f2(0.f);
+        int idx = tid;
+        for (int j = 0; j < np; ++j) {
+            const int end = (j + 1) * q;
+            if (idx >= end) continue;
+            if (!mbar_wait_bounded(&bar[b][j], par, a.wait_limit)) {
+                s_fail = 1;  // read by thread 0 after the next __syncthreads
+                atomicOr(a.fault, FAULT_WAIT);
             }
-        const float tot = cta_sum_all<NW>(hsum(acc), s1[b]);
-        const float m0 = np ? tot / cnt : 0.f;
-        // pass 2: e = d - m0, corrected
-        const float2 nkm = f2(-m0);
-        float2 e1 = f2(0.f), e2 = f2(0.f);
-        for (int j = 0; j < np; ++j)
-            for (int k = tid; k < q; k += BNC_THREADS) {
+            for (; idx < end; idx += BNC_THREADS) {
                 float2 f[H];
-                io2::unpack(buf[(size_t)j * q + k], f);
+                io2::unpack(buf[idx], f);
+                if (!have) {
+                    tK = f[0].x;
+                    have = true;
+                }
+                const float2 nk = f2(-tK);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    const float2 e = __fadd2_rn(__fadd2_rn(f[h], nk), nkm);
-                    e1 = __fadd2_rn(e1, e);
-                    e2 = __ffma2_rn(e, e, e2);
+                    const float2 e = __fadd2_rn(f[h], nk);
+                    a1 = __fadd2_rn(a1, e);
+                    a2 = __ffma2_rn(e, e, a2);
                 }
+                tn += (float)V;
             }
-        const float2 E = cta_sum_all<NW>(make_float2(hsum(e1), hsum(e2)), s2[b]);
+        }
+        // the thread's mean relative to K and its M2, merged over the CTA
+        const float S1 = hsum(a1), S2 = hsum(a2);
+        const float mt = tn > 0.f ? S1 / tn : 0.f;
+        const float m2t = tn > 0.f ? fmaxf(fmaf(-S1, mt, S2), 0.f) : 0.f;
+        const float mdt = tn > 0.f ? (tK - K) + mt : 0.f;
+        const float md_r = np ? cta_sum_all<NW>(tn * mdt, s1[b]) / cnt : 0.f;
+        const float dm = mdt - md_r;
+        const float m2_r = cta_sum_all<NW>(fmaf(tn * dm, dm, m2t), s2[b]);
         if (tid == 0) {
-            const float cc = np ? E.x / cnt : 0.f;
             part[b][0] = cnt;
-            part[b][1] = m0 + cc;
-            part[b][2] = fmaxf(fmaf(-cnt * cc, cc, E.y), 0.f);
+            part[b][1] = md_r;
+            part[b][2] = m2_r;
         }
         cluster.sync();  // every partial of this channel is written
 
@@ -463,44 +472,49 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         const float md = stat[b][0], rstd = stat[b][1];
         if (rank == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[b][2], rstd);
 
-        // normalize from shared memory: y = ((x - K) - md) * rstd * gamma + beta
+        // normalize from shared memory: y = ((x - K) - md) * (rstd * gamma) + beta
         const float g = bn_param<T>(a.gamma, c, 1.f);
         const float bb = bn_param<T>(a.beta, c, 0.f);
-        const float2 nmd = f2(-md), r2 = f2(rstd), g2 = f2(g), b2 = f2(bb);
-        for (int j = 0; j < np; ++j) {
-            uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + ((n0 + j) * C + c) * HW);
-            for (int k = tid; k < q; k += BNC_THREADS) {
+        const float2 nk = f2(-K), nmd = f2(-md), A2 = f2(rstd * g), b2 = f2(bb);
+        idx = tid;
+        for (int j = 0; j < np && idx < tp; ++j) {
+            const int end = (j + 1) * q;
+            uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + ((n0 + j) * C + c) * HW) -
+                        (size_t)j * q;
+            for (; idx < end; idx += BNC_THREADS) {
                 float2 f[H], o[H];
-                io2::unpack(buf[(size_t)j * q + k], f);
+                io2::unpack(buf[idx], f);
 #pragma unroll
                 for (int h = 0; h < H; ++h)
-                    o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), r2), g2, b2);
-                __stcs(yp + k, io2::pack(o));
+                    o[h] = __ffma2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), A2, b2);
+                __stcs(yp + idx, io2::pack(o));
             }
         }
-        __syncthreads();  // every thread is done with this buffer
+        __syncthreads();  // every thread is done with this buffer; s_fail is visible
         const int64_t next = c + 2 * K_clusters;
-        if (tid == 0 && np > 0 && next < C && !gave_up) {
+        if (tid == 0 && np > 0 && next < C && !s_fail) {
             fence_proxy_async_smem();
-            bn_issue_planes<T>(a, sx + b * buf_packs, &bar[b], next, n0, np, q, plane_bytes);
+            bn_issue_planes<T>(a, sx + b * buf_packs, bar[b], next, n0, np, q, plane_bytes);
             if (b == 0) last_issued0 = i + 2;
             else last_issued1 = i + 2;
         }
     }
     if (i > 0) cluster_wait();  // peers are done reading this CTA's last partials
-    if (tid == 0 && gave_up) {
-        // wait (bounded) for copies issued but never received
-        if (last_issued0 > last_done0 &&
-            !mbar_wait_bounded(&bar[0], (uint32_t)((last_issued0 >> 1) & 1), 1u << 22))
-            atomicOr(a.fault, FAULT_DRAIN);
-        if (last_issued1 > last_done1 &&
-            !mbar_wait_bounded(&bar[1], (uint32_t)((last_issued1 >> 1) & 1), 1u << 22))
-            atomicOr(a.fault, FAULT_DRAIN);
+    if (tid == 0 && s_fail) {
+        // wait (bounded) for the copies of every plane's last issued phase; a
+        // phase that already completed returns at once
+        for (int b = 0; b < 2; ++b) {
+            const int li = b == 0 ? last_issued0 : last_issued1;
+            if (li < 0) continue;
+            for (int j = 0; j < np; ++j)
+                if (!mbar_wait_bounded(&bar[b][j], (uint32_t)((li >> 1) & 1), 1u << 22))
+                    atomicOr(a.fault, FAULT_DRAIN);
+        }
     }
 }
 
 // Plan choice (measured on GB300 at [32, 64, 56, 56] binary32: cluster
-// 16.0 us, streaming 17.9 us, scalar 24.3 us).  One cluster of up to 8 CTAs
+// 11.8 us, streaming 17.3 us, one-pass 32.4 us, scalar 24.3 us).  One cluster of up to 8 CTAs
 // per channel when the channel's planes fit the clusters' shared memory and
 // every channel's cluster can be resident at once (one buffer); when there
 // are more channels than resident clusters, each cluster pipelines its
@@ -510,11 +524,16 @@ template <typename T>
 cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     *launched = false;
     auto kernel = bn_cluster_kernel<T>;
-    int cs = 8;
+    // clusters of 4 CTAs when a CTA's two buffers fit (measured at
+    // [32, 64, 56, 56]: binary32 11.8 us against 12.5 us with 8, bfloat16
+    // 10.3 against 10.9), else 8; a forced size (2, 4 or 8) wins
+    int cs = a.cluster_size;
+    if (cs != 2 && cs != 4 && cs != 8)
+        cs = 2 * (size_t)((a.batch + 3) / 4) * (size_t)a.HW * sizeof(T) <= (size_t)200 * 1024 ? 4 : 8;
     while (cs > 1 && cs > a.batch) cs >>= 1;
     const int64_t ppc = (a.batch + cs - 1) / cs;
     const size_t buf = (size_t)ppc * (size_t)a.HW * sizeof(T);
-    if (2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
+    if (ppc > kBnMaxPpc || 2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
     static std::mutex mu;  // one per instance
     static int attr_done[64];
     int dev = 0;
@@ -550,13 +569,14 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
         return cudaSuccess;
     }
     int64_t k = a.C;
-    if (clusters < a.C) {
+    if (clusters < a.C || (a.max_clusters > 0 && a.max_clusters < a.C)) {
         cfg.dynamicSmemBytes = 2 * buf;
         if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
             cudaGetLastError();
             return cudaSuccess;
         }
         k = clusters;
+        if (a.max_clusters > 0 && a.max_clusters < k) k = a.max_clusters;
     }
     if (k < 1) return cudaSuccess;
     cfg.gridDim = dim3((unsigned)(k * cs));
@@ -670,101 +690,50 @@ cudaError_t launch_bn_train(const BnArgs &a, int dtype, int num_sms, cudaStream_
 }  // namespace nrm
 
 // ---------------------------------------------------------------------------
-// bn_fwd_train_noalloc: the same plans as bn_fwd_train; the plans that keep
-// per-plane partial statistics in global memory (the streaming and scalar
-// two-kernel plans) keep them in a fixed array of this library instead of a
-// workspace the caller allocates.  It is for callers that cannot allocate device memory
-// when they call -- for example a runtime that reserves its whole device
-// memory budget at start-up and forbids later allocations, or a component
-// that is handed device pointers by another part of the program and has no
-// allocator of its own.
+// The fixed partials array of bn_fwd_train_noalloc (entry point in api.cpp):
+// the same plans as bn_fwd_train; the plans that keep partial statistics in
+// global memory (streaming, scalar and one-pass) keep them here instead of
+// in a workspace the caller allocates.  It is for callers that cannot
+// allocate device memory when they call -- for example a runtime that
+// reserves its whole device memory budget at start-up and forbids later
+// allocations, or a component that is handed device pointers by another part
+// of the program and has no allocator of its own.
 //
 // The array is a file-scope __device__ variable: every GPU that loads this
-// library holds it (kBnStaticPlanes float2 = 512 KB) until the process exits.
+// library holds it (kBnFixedPlanes float2 = 512 KB) until the process exits.
 // Its name in host code is only a host-side stand-in, so the device address
 // is taken with cudaGetSymbolAddress, once per device, with that device
 // current, on the first call made on that device.  All calls on a device
 // share the array: calls that overlap on the GPU (different streams without
 // ordering) race on it.  Every partial a call reads it first writes in the
-// same call, so nothing needs clearing between calls.
+// same call, and the one-pass plan's reset kernel clears its control words,
+// so nothing needs clearing between calls.
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int64_t kBnStaticPlanes = 65536;  // largest batch * C accepted
-__device__ __align__(256) float2 g_bn_static_partials[kBnStaticPlanes];
+__device__ __align__(256) float2 g_bn_fixed_partials[nrm::kBnFixedPlanes];
 
 constexpr int kMaxDevices = 64;
-float2 *g_bn_static_ptr[kMaxDevices];
-std::once_flag g_bn_static_once[kMaxDevices];
-
-bool spans_overlap(const void *a, size_t na, const void *b, size_t nb) {
-    if (!a || !b || !na || !nb) return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + nb && b0 < a0 + na;
-}
+void *g_bn_fixed_ptr[kMaxDevices];
+std::once_flag g_bn_fixed_once[kMaxDevices];
 
 }  // namespace
 
-extern "C" int bn_fwd_train_noalloc(const void *x, const void *gamma, const void *beta, void *y,
-                                    float *save_mean, float *save_rstd, float *running_mean,
-                                    float *running_var, int64_t batch, int64_t C, int64_t HW,
-                                    float eps, float momentum, int dtype, cudaStream_t stream) {
-    using namespace nrm;
-    if (dtype != NRM_F32 && dtype != NRM_F16 && dtype != NRM_BF16) return NRM_ERR_DTYPE;
-    if (batch < 1 || C < 1 || HW < 1) return NRM_ERR_SHAPE;
-    if ((uint64_t)batch > (uint64_t)INT64_MAX / (uint64_t)C / (uint64_t)HW / 4) return NRM_ERR_SHAPE;
-    if (batch * HW < 2) return NRM_ERR_SHAPE;
-    if (batch * C > kBnStaticPlanes) return NRM_ERR_TOO_LARGE;
-    // the streaming plan keeps one partial per chunk of at most kBnChunkPacks
-    // packs; when those do not fit, the per-plane plans still do
-    const int64_t V = dtype == NRM_F32 ? 4 : 8;
-    const int64_t nch = ((HW + V - 1) / V + kBnChunkPacks - 1) / kBnChunkPacks;
-    const int bn_plan = batch * C * nch > kBnStaticPlanes ? BN_PLAN_NO_STREAM : BN_PLAN_AUTO;
-    if (!std::isfinite(eps) || eps < 0.f || !(momentum >= 0.f && momentum <= 1.f))
-        return NRM_ERR_VALUE;
-    if (!x || !y) return NRM_ERR_NULL;
-    const size_t es = dtype == NRM_F32 ? 4 : 2;
-    const void *data[] = {x, gamma, beta, y};
-    for (const void *p : data)
-        if (p && (reinterpret_cast<uintptr_t>(p) & (es - 1))) return NRM_ERR_VALUE;
-    const void *stats[] = {save_mean, save_rstd, running_mean, running_var};
-    for (const void *p : stats)
-        if (p && (reinterpret_cast<uintptr_t>(p) & 3)) return NRM_ERR_VALUE;
-    const size_t tb = (size_t)batch * (size_t)C * (size_t)HW * es, cb = (size_t)C * 4;
-    const size_t pb = (size_t)C * es;
-    const void *ins[] = {x, gamma, beta};
-    const size_t in_n[] = {tb, pb, pb};
-    const void *outs[] = {y, save_mean, save_rstd, running_mean, running_var};
-    const size_t out_n[] = {tb, cb, cb, cb, cb};
-    for (int o = 0; o < 5; ++o) {
-        for (int i = 0; i < 3; ++i)
-            if (spans_overlap(outs[o], out_n[o], ins[i], in_n[i])) return NRM_ERR_ALIAS;
-        for (int o2 = o + 1; o2 < 5; ++o2)
-            if (spans_overlap(outs[o], out_n[o], outs[o2], out_n[o2])) return NRM_ERR_ALIAS;
-    }
-
+int nrm::bn_fixed_workspace(void **ws, size_t *bytes) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return NRM_ERR_DEVICE;
     }
-    std::call_once(g_bn_static_once[dev], [dev]() {
+    std::call_once(g_bn_fixed_once[dev], [dev]() {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bn_static_partials) == cudaSuccess)
-            g_bn_static_ptr[dev] = static_cast<float2 *>(p);
+        if (cudaGetSymbolAddress(&p, g_bn_fixed_partials) == cudaSuccess)
+            g_bn_fixed_ptr[dev] = p;
         else
             cudaGetLastError();
     });
-    if (!g_bn_static_ptr[dev]) return NRM_ERR_DEVICE;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms < 1) {
-        cudaGetLastError();
-        return NRM_ERR_DEVICE;
-    }
-    BnArgs a{x, gamma, beta, y, save_mean, save_rstd, running_mean, running_var, batch, C, HW,
-             eps, momentum, g_bn_static_ptr[dev], fault_word(), 1u << 20, bn_plan,
-             sizeof(g_bn_static_partials)};
-    int used = 0;
-    return launch_bn_train(a, dtype, sms, stream, &used) == cudaSuccess ? NRM_OK : NRM_ERR_LAUNCH;
+    if (!g_bn_fixed_ptr[dev]) return NRM_ERR_DEVICE;
+    *ws = g_bn_fixed_ptr[dev];
+    *bytes = sizeof(g_bn_fixed_partials);
+    return NRM_OK;
 }

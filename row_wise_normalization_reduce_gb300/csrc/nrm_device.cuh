@@ -396,6 +396,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Rank of this CTA in its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Loads from CTA `rank`'s shared memory at the address of `p` in this CTA
+// (distributed shared memory of the cluster).
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(p, rank)) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 ld_dsmem(const float2 *p, uint32_t rank) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "r"(dsmem_addr(p, rank))
+                 : "memory");
+    return v;
+}
+
 // Cluster barrier in two halves: arrive (release: this thread's earlier
 // memory accesses, including reads of peers' shared memory, are done) and
 // wait (acquire).

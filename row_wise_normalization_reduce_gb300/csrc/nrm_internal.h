@@ -17,7 +17,8 @@ enum PlanKind {
     PLAN_CTA = 3,
     PLAN_TMA = 4,
     PLAN_PERSIST = 5,
-    PLAN_WRAW = 6
+    PLAN_WRAW = 6,
+    PLAN_CLUSTER = 7
 };
 
 // Bits of the device fault word (see fault.cu).
@@ -78,9 +79,23 @@ unsigned *fault_word();
 // Launch a row operator with a fully specified plan.  Returns a cudaError_t
 // from the launch (cudaSuccess or the launch error), or
 // cudaErrorInvalidConfiguration when the template set has no such plan.
-cudaError_t launch_ln(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
-cudaError_t launch_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
-cudaError_t launch_add_rms(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
+// One instance per operator and storage type (rows_<op>_<type>.cu).
+#define NRM_ROW_LAUNCHERS(op)                                                          \
+    cudaError_t launch_##op##_f32(const RowArgs &a, const Plan &p, cudaStream_t s);    \
+    cudaError_t launch_##op##_f16(const RowArgs &a, const Plan &p, cudaStream_t s);    \
+    cudaError_t launch_##op##_bf16(const RowArgs &a, const Plan &p, cudaStream_t s);   \
+    inline cudaError_t launch_##op(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s) { \
+        switch (dtype) {                                                               \
+        case DT_F32: return launch_##op##_f32(a, p, s);                                \
+        case DT_F16: return launch_##op##_f16(a, p, s);                                \
+        case DT_BF16: return launch_##op##_bf16(a, p, s);                              \
+        default: return cudaErrorInvalidValue;                                         \
+        }                                                                              \
+    }
+NRM_ROW_LAUNCHERS(ln)
+NRM_ROW_LAUNCHERS(rms)
+NRM_ROW_LAUNCHERS(add_rms)
+#undef NRM_ROW_LAUNCHERS
 // Row softmax (softmax.cu): PLAN_CTA (row in registers) or PLAN_GENERIC.
 cudaError_t launch_softmax(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s);
 
@@ -104,6 +119,9 @@ struct BnArgs {
     size_t ws_bytes = 0;  // bytes at ws (the one-pass plan runs only if it fits)
     int prefetch = 0;     // one-pass plan's L2 prefetch: 0 auto, 1 off, s >= 2: s - 1 rounds ahead
     int packs = 0;        // one-pass plan's packs per thread: 0 auto, 4 or 8
+    int cluster_size = 0; // cluster plan: CTAs per cluster (0: 8), a measurement hook
+    int max_clusters = 0; // cluster plan: at most this many clusters (0: one per channel
+                          // when they all fit at once), a measurement hook
 };
 
 // BatchNorm plans: automatic, streaming two kernels (registers + dependent
@@ -127,6 +145,14 @@ enum BnPlan {
 // a chunk of at most this many packs of one plane; the workspace holds one
 // float2 per unit.
 constexpr int kBnChunkPacks = 1024;
+
+// Capacity of the library's fixed partials array used by
+// bn_fwd_train_noalloc: batch * C planes (one float2 each, 512 KB).
+constexpr int64_t kBnFixedPlanes = 65536;
+
+// The current device's address and size of that array (bn.cu), looked up
+// once per device with the device current; an NRM status.
+int bn_fixed_workspace(void **ws, size_t *bytes);
 
 // Workspace bytes of the one-pass plans for C channels and `units` chunks in
 // all: the per-chunk 8-byte partials (padded to 16 bytes), then 24 bytes per

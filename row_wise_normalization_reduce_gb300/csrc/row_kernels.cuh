@@ -156,7 +156,7 @@ template <int OP, typename T, int PACKS, int STRIDE, class Red, class Prm, class
 __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row, const int t,
                                             Red &red, const uint4 (&rx)[PACKS],
                                             const uint4 (&rr)[PACKS], const Prm &prm,
-                                            const Hook &after_sync) {
+                                            const Hook &after_sync, const bool lead = true) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
@@ -220,7 +220,7 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
         c = E.x * invN;
         const float var = fmaxf(fmaf(-c, c, E.y * invN), 0.f);
         rstd = rsqrtf(var + a.eps);
-        if (t == 0) {
+        if (t == 0 && lead) {
             if (a.mean) a.mean[row] = m0 + c;
             if (a.rstd) a.rstd[row] = rstd;
         }
@@ -232,7 +232,7 @@ __device__ __forceinline__ void row_compute(const RowArgs &a, const int64_t row,
             for (int h = 0; h < H; ++h) ss = __ffma2_rn(v[k][h], v[k][h], ss);
         rstd = rsqrtf(fmaf(red.sum(ss.x + ss.y), invN, a.eps));
         after_sync();
-        if (t == 0 && a.rstd) a.rstd[row] = rstd;
+        if (t == 0 && lead && a.rstd) a.rstd[row] = rstd;
     }
 
     // ---- S7/S8: parameters, normalize, round once, store ----
@@ -277,10 +277,11 @@ template <int OP, typename T, int PACKS, int STRIDE, class Red, class Src, class
           bool FULL = false>
 __device__ __forceinline__ void row_body(const RowArgs &a, const int64_t row, const int t,
                                          Red &red, const Src &src, const Prm &prm,
-                                         const Hook &after_sync) {
+                                         const Hook &after_sync, const bool lead = true) {
     uint4 rx[PACKS], rr[PACKS];
     row_load<OP, PACKS, STRIDE, Src, FULL>(src, t, (int)(a.N / IO<T>::V), rx, rr);
-    row_compute<OP, T, PACKS, STRIDE, Red, Prm, Hook, FULL>(a, row, t, red, rx, rr, prm, after_sync);
+    row_compute<OP, T, PACKS, STRIDE, Red, Prm, Hook, FULL>(a, row, t, red, rx, rr, prm, after_sync,
+                                                           lead);
 }
 
 // Resident CTAs per SM the CTA and persistent kernels are compiled for
@@ -341,7 +342,8 @@ template <int OP, int THREADS, int PACKS, bool FULL = false>
 constexpr int row_min_blocks() {
     return (OP == OP_RMS && PACKS <= 2 && NRM_RMS_MIN_THREADS / THREADS > 0) ? NRM_RMS_MIN_THREADS / THREADS
            : (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0) ? NRM_CTA_MIN_THREADS / THREADS
-           : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && FULL && NRM_LN4_FULL_MIN_THREADS / THREADS > 0)
+           : (OP != OP_ADD_RMS && PACKS == 4 && THREADS <= 256 && FULL &&
+              NRM_LN4_FULL_MIN_THREADS / THREADS > 0)
                ? NRM_LN4_FULL_MIN_THREADS / THREADS
            : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && NRM_LN4_MIN_THREADS / THREADS > 0)
                ? NRM_LN4_MIN_THREADS / THREADS
@@ -384,6 +386,111 @@ __global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS, F
         row_body<OP, T, PACKS, THREADS, CtaRed<NW>, GlobalSrc<T>, GlobalParams<T>, NoHook, FULL>(
             a, row, threadIdx.x, red, src, prm, NoHook{});
     }
+}
+
+// ---------------------------------------------------------------------------
+// Cluster split: one row over the CS CTAs of a thread-block cluster (the
+// LayerNorm walkthrough, lpnh.cn/news/2756757, §1.1 and §4.1, splits a row
+// that outgrows one block across several; here the blocks are a cluster and
+// their partial sums meet in distributed shared memory).  CTA rank r holds
+// the contiguous slice [r S, (r+1) S) of the row's P = CS S packs in
+// registers (x still read from HBM once); each row-wide sum is a CTA sum,
+// published in the CTA's shared memory, a cluster barrier, and a read of the
+// CS partials in rank order (lane k of every warp reads rank k's partial,
+// then shuffles), so every thread of the cluster gets the same bits.  It
+// serves rows too long for one CTA's registers and grids with too few rows
+// to fill the SMs.
+// ---------------------------------------------------------------------------
+// Sum of the CS CTAs' published partials, rank order, same bits in every lane.
+template <int CS>
+__device__ __forceinline__ float cluster_gather_sum(const float *slot) {
+    const int lane = threadIdx.x & 31;
+    const float mine = lane < CS ? ld_dsmem(slot, (uint32_t)lane) : 0.f;
+    float r = __shfl_sync(0xffffffffu, mine, 0);
+#pragma unroll
+    for (int k = 1; k < CS; ++k) r += __shfl_sync(0xffffffffu, mine, k);
+    return r;
+}
+
+template <int NW, int CS> struct ClusterRed {
+    float *s1;    // CTA-level exchange slots (CtaRed's)
+    float2 *s2;
+    float *c1;    // this CTA's published partials: c1[0]; c2[0], c2[1]
+    float *c2;
+    __device__ __forceinline__ float sum(float v) {
+        const float t = cta_sum_all<NW>(v, s1);
+        if (threadIdx.x == 0) c1[0] = t;
+        cluster_arrive();
+        cluster_wait();
+        return cluster_gather_sum<CS>(c1);
+    }
+    __device__ __forceinline__ float2 sum2(float2 v) {
+        const float2 t = cta_sum_all<NW>(v, s2);
+        if (threadIdx.x == 0) {
+            c2[0] = t.x;
+            c2[1] = t.y;
+        }
+        cluster_arrive();
+        cluster_wait();
+        return make_float2(cluster_gather_sum<CS>(c2), cluster_gather_sum<CS>(c2 + 1));
+    }
+};
+
+// Persistent clusters: cluster k handles rows k, k + G/CS, ... (G/CS = the
+// clusters that fit at once), asking L2 for its next row while it reduces
+// the current one.  A partial slot of one parity is rewritten two rows
+// later, after at least one more cluster barrier, which every peer reaches
+// only once its reads of that slot are done; a last cluster barrier keeps
+// every CTA resident until its peers have read its partials.
+template <int OP, typename T, int THREADS, int PACKS, int CS, bool FULL>
+__global__ void __launch_bounds__(THREADS, (row_min_blocks<OP, THREADS, PACKS, FULL>()))
+    row_cluster_kernel(const RowArgs a) {
+    constexpr int NW = THREADS / 32;
+    constexpr int V = IO<T>::V;
+    __shared__ float s1[2][NW];
+    __shared__ float2 s2[2][NW];
+    __shared__ float c1[2][1];
+    __shared__ float c2[2][2];
+    const int rank = (int)cluster_rank();
+    const int64_t ncl = gridDim.x / CS;
+    const int S = (int)(a.N / V) / CS;          // packs per CTA slice
+    const int64_t off = (int64_t)rank * S * V;  // first element of this CTA's slice
+    RowArgs b = a;
+    b.N = (int64_t)S * V;  // the slice (a.fN, a.invN stay those of the row)
+    b.y = static_cast<T *>(a.y) + off;
+    if (OP == OP_ADD_RMS) b.res_out = static_cast<T *>(a.res_out) + off;
+    const T *X = static_cast<const T *>(a.x) + off;
+    const T *R = OP == OP_ADD_RMS ? static_cast<const T *>(a.res) + off : nullptr;
+    const T *P0 = a.p0 ? static_cast<const T *>(a.p0) + off : nullptr;
+    const T *P1 = a.p1 ? static_cast<const T *>(a.p1) + off : nullptr;
+    const int64_t first = blockIdx.x / CS;
+#if NRM_ROW_PDL
+    // as row_cta_kernel: the CTA's slice of its first row is requested from
+    // L2 before the wait for the previous grid
+    if (threadIdx.x == 0 && first < a.rows) {
+        const uint32_t bytes = (uint32_t)S * 16u;
+        prefetch_l2_bulk(X + first * a.ldx, bytes);
+        if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + first * a.ldr, bytes);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+#endif
+    int parity = 0;
+    for (int64_t row = first; row < a.rows; row += ncl, parity ^= 1) {
+        // the cluster's next row is requested from L2 while this one is reduced
+        if (threadIdx.x == 0 && row + ncl < a.rows) {
+            const uint32_t bytes = (uint32_t)S * 16u;
+            prefetch_l2_bulk(X + (row + ncl) * a.ldx, bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(R + (row + ncl) * a.ldr, bytes);
+        }
+        ClusterRed<NW, CS> red{&s1[parity][0], &s2[parity][0], &c1[parity][0], &c2[parity][0]};
+        const GlobalSrc<T> src{X + row * a.ldx, OP == OP_ADD_RMS ? R + row * a.ldr : nullptr};
+        const GlobalParams<T> prm{P0, P1};
+        row_body<OP, T, PACKS, THREADS, ClusterRed<NW, CS>, GlobalSrc<T>, GlobalParams<T>, NoHook,
+                 FULL>(b, row, threadIdx.x, red, src, prm, NoHook{}, rank == 0);
+    }
+    cluster_arrive();
+    cluster_wait();
 }
 
 // Persistent register pipeline: CTA b handles rows b, b + G, ... (G =
@@ -801,6 +908,34 @@ cudaError_t launch_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
 #endif
 }
 
+// Cluster-split launch: as many clusters of CS CTAs as are resident at once
+// (at most one per row); needs P divisible by CS (checked by the plan choice).
+template <int OP, typename T, int THREADS, int PACKS, int CS, bool FULL>
+cudaError_t launch_cluster(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    auto kernel = row_cluster_kernel<OP, T, THREADS, PACKS, CS, FULL>;
+    int per_sm = 0;
+    const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), THREADS, 0, &per_sm);
+    if (oe != cudaSuccess) return oe;
+    const int64_t resident = (int64_t)p.sms * (per_sm > 0 ? per_sm : 1) / CS;
+    cudaLaunchConfig_t cfg = {};
+    int64_t clusters = a.rows < resident ? a.rows : resident;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3((unsigned)(clusters * CS));
+    cfg.blockDim = dim3(THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = NRM_ROW_PDL ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int OP, typename T>
 cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
     const dim3 grid((unsigned)p.grid);
@@ -827,7 +962,8 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
 // (LayerNorm 4096x4096 bf16 12.2 -> 11.4 us; RMSNorm measured 2 % slower
 // that way, so it keeps the tested form)
 #define NRM_CTA_FULL_CASE(TH, PK)                                                  \
-    if (OP != OP_RMS && p.threads == TH && p.packs == PK && a.N / IO<T>::V == TH * PK) \
+    if ((OP != OP_RMS || (PK == 4 && TH == 128)) && p.threads == TH && p.packs == PK && \
+        a.N / IO<T>::V == TH * PK)                                                  \
         return launch_cta<OP, T, TH, PK, true>(a, p, s);
         NRM_CTA_FULL_CASE(128, 4) NRM_CTA_FULL_CASE(256, 2) NRM_CTA_FULL_CASE(256, 4)
 #undef NRM_CTA_FULL_CASE
@@ -835,6 +971,20 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
         NRM_CTA_CASE(128, 4) NRM_CTA_CASE(256, 4) NRM_CTA_CASE(512, 4) NRM_CTA_CASE(1024, 4)
 #undef NRM_CTA_CASE
+        return cudaErrorInvalidConfiguration;
+    } else if (p.kind == PLAN_CLUSTER) {
+        // p.groups = CTAs per cluster; the slice is exactly THREADS x PACKS
+        // packs (FULL, no bounds tests) or fits it
+#define NRM_CLUSTER_CASE(TH, PK, CS)                                               \
+    if (p.threads == TH && p.packs == PK && p.groups == CS) {                      \
+        if (a.N / IO<T>::V == (int64_t)TH * PK * CS)                              \
+            return launch_cluster<OP, T, TH, PK, CS, true>(a, p, s);              \
+        return launch_cluster<OP, T, TH, PK, CS, false>(a, p, s);                 \
+    }
+        NRM_CLUSTER_CASE(128, 1, 2) NRM_CLUSTER_CASE(128, 1, 4) NRM_CLUSTER_CASE(128, 2, 2)
+        NRM_CLUSTER_CASE(128, 2, 4) NRM_CLUSTER_CASE(128, 4, 2) NRM_CLUSTER_CASE(128, 4, 4)
+        NRM_CLUSTER_CASE(128, 4, 8) NRM_CLUSTER_CASE(256, 4, 2)
+#undef NRM_CLUSTER_CASE
         return cudaErrorInvalidConfiguration;
     } else if (p.kind == PLAN_WRAW) {
 #define NRM_WRAW_CASE(PK, WP)                                                      \
@@ -866,16 +1016,6 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         return cudaErrorInvalidConfiguration;
     }
     return cudaGetLastError();
-}
-
-template <int OP>
-cudaError_t launch_row_dtype(const RowArgs &a, const Plan &p, int dtype, cudaStream_t s) {
-    switch (dtype) {
-    case DT_F32: return launch_row<OP, float>(a, p, s);
-    case DT_F16: return launch_row<OP, __half>(a, p, s);
-    case DT_BF16: return launch_row<OP, __nv_bfloat16>(a, p, s);
-    default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace nrm

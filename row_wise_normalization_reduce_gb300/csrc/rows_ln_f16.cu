@@ -1,0 +1,12 @@
+// rows_ln_f16.cu -- the row kernels of one operator (LayerNorm) for one
+// storage type (binary16): one translation unit per pair, so they compile in
+// parallel.
+#include "row_kernels.cuh"
+
+namespace nrm {
+
+cudaError_t launch_ln_f16(const RowArgs &a, const Plan &p, cudaStream_t s) {
+    return launch_row<OP_LN, __half>(a, p, s);
+}
+
+}  // namespace nrm

@@ -15,6 +15,13 @@
 // y_i = e_i * (exp(m_t - m) / d), one multiply per element.  Rows of the next
 // wave are prefetched into L2 as in the norm kernels.
 //
+// Cluster plan: the same with one row split over the CS CTAs of a
+// thread-block cluster, CTA rank r holding the contiguous slice [r S, (r+1) S)
+// of the row's packs; after its CTA-wide merge each CTA publishes its
+// (max, sum) pair in shared memory, and after a cluster barrier every warp
+// reads the CS pairs over distributed shared memory and merges them in rank
+// order (same bits everywhere).  For rows too few to fill the SMs.
+//
 // Generic plan (any N, any alignment): one CTA per row streams the row once
 // with the per-element online update to get (m, d), merges, then reads the
 // row again to write y.
@@ -41,6 +48,29 @@ struct MaxSum {
 
 template <typename T> __device__ __forceinline__ float smx_exp(float x) { return __expf(x); }
 template <> __device__ __forceinline__ float smx_exp<float>(float x) { return expf(x); }
+
+// Maximum of three values in one instruction (sm_100+ three-input max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// The CTA plan's exponentials of a pair, e = exp(d) for d = x - m_t <= 0.
+// Binary32 outputs: expf.  16-bit outputs: exp(d) = 2^(d log2 e), the
+// product formed pairwise and PTX's ex2.approx (an error of a few binary32
+// ulp, like __expf; with the rounding of d log2 e, below 1e-5 relative for
+// |d| < 100, far inside the 1-ulp tolerance of binary16 and bfloat16).
+template <typename T> __device__ __forceinline__ float2 smx_exp_pair(float2 d) {
+    const float2 t = __fmul2_rn(d, f2(1.44269504088896341f));
+    float2 r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r.x) : "f"(t.x));
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r.y) : "f"(t.y));
+    return r;
+}
+template <> __device__ __forceinline__ float2 smx_exp_pair<float>(float2 d) {
+    return make_float2(expf(d.x), expf(d.y));
+}
 
 // Merge of two (max, sum) pairs (the rescaling rule above).  A side with no
 // elements (m = -inf, d = 0) leaves the other unchanged; the merge is
@@ -80,74 +110,94 @@ __device__ __forceinline__ MaxSum cta_merge_all(MaxSum v, float2 *slot) {
 // CTA plan
 // ---------------------------------------------------------------------------
 // FULL: the row is exactly THREADS x PACKS packs (no bounds tests).
-// Resident 128-thread CTAs per SM the CTA plan is compiled for
+// Resident 128-thread CTAs per SM the exact-row CTA plan is compiled for
 // (NRM_SMX128_MIN_BLOCKS, at most 48 registers at ten): bf16 4096 x 4096 on
 // GB300 11.81 us at ten against 12.23 us uncapped (52 registers, nine CTAs)
-// and 12.45 us at twelve (spills).
+// and 12.45 us at twelve (spills).  The bounds-tested and cluster instances
+// take eight (64 registers; at ten the 16-bit ones spill).
 #ifndef NRM_SMX128_MIN_BLOCKS
 #define NRM_SMX128_MIN_BLOCKS 10
 #endif
-template <typename T, int THREADS, int PACKS, bool FULL = false>
-__global__ void __launch_bounds__(THREADS, (THREADS == 128 ? NRM_SMX128_MIN_BLOCKS : 1))
+// CS > 1: the cluster plan (launched with clusters of CS CTAs; P divisible
+// by CS).
+template <typename T, int THREADS, int PACKS, int CS, bool FULL = false>
+__global__ void __launch_bounds__(THREADS, (THREADS == 128 ? (CS == 1 && FULL ? NRM_SMX128_MIN_BLOCKS : 8) : 1))
     softmax_cta_kernel(const RowArgs a, const int64_t pf) {
     using io2 = IO2<T>;
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
     constexpr int NW = THREADS / 32;
     __shared__ float2 slot[2][NW];
+    __shared__ float2 pub[2];  // cluster plan: this CTA's (max, sum) of the row
     const int t = threadIdx.x;
-    const int P = (int)(a.N / V);
-    const T *X = static_cast<const T *>(a.x);
+    const int rank = CS > 1 ? (int)cluster_rank() : 0;
+    const int P = (int)(a.N / V) / CS;  // packs of this CTA's slice of the row
+    const int64_t off = (int64_t)rank * P * V;
+    const T *X = static_cast<const T *>(a.x) + off;
+    const int64_t first = blockIdx.x / CS, step = gridDim.x / CS;
+    const uint32_t slice_bytes = (uint32_t)P * 16u;
     // launched as a programmatic dependent (as the norm kernels): the CTA's
     // own row is requested from L2 first, then the kernel waits for the
     // previous grid on the stream and lets the next one become resident
-    if (pf > 0 && t == 0 && blockIdx.x < a.rows)
-        prefetch_l2_bulk(X + blockIdx.x * a.ldx, (uint32_t)(a.N * (int64_t)sizeof(T)));
+    if ((pf > 0 || CS > 1) && t == 0 && first < a.rows) prefetch_l2_bulk(X + first * a.ldx, slice_bytes);
     pdl_wait();
     pdl_launch_dependents();
     int parity = 0;
-    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, parity ^= 1) {
-        if (pf > 0 && t == 0 && row + pf < a.rows)
-            prefetch_l2_bulk(X + (row + pf) * a.ldx, (uint32_t)(a.N * (int64_t)sizeof(T)));
+    for (int64_t row = first; row < a.rows; row += step, parity ^= 1) {
+        if (pf > 0 && t == 0 && row + pf < a.rows) prefetch_l2_bulk(X + (row + pf) * a.ldx, slice_bytes);
         const T *xr = X + row * a.ldx;
         uint4 raw[PACKS];
 #pragma unroll
         for (int k = 0; k < PACKS; ++k)
             if (FULL || t + k * THREADS < P) raw[k] = ld_stream(xr + (size_t)(t + k * THREADS) * V);
         float2 v[PACKS][H];
-        float2 mx = f2(-INFINITY);
+        float mt = -INFINITY;
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             if (FULL || t + k * THREADS < P) {
                 io2::unpack(raw[k], v[k]);
 #pragma unroll
-                for (int h = 0; h < H; ++h)
-                    mx = make_float2(fmaxf(mx.x, v[k][h].x), fmaxf(mx.y, v[k][h].y));
+                for (int h = 0; h < H; ++h) mt = fmax3(mt, v[k][h].x, v[k][h].y);
             }
         }
         // e = exp(x - m_t); a thread whose values are all -inf (masked) holds
         // e = 0 and m_t = -inf, which the merge treats as empty
-        const float mt = fmaxf(mx.x, mx.y);
-        const float sh = mt == -INFINITY ? 0.f : mt;
-        float dt = 0.f;
+        const float2 nsh = f2(mt == -INFINITY ? 0.f : -mt);
+        float2 acc = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             if (FULL || t + k * THREADS < P) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    v[k][h] = make_float2(smx_exp<T>(v[k][h].x - sh), smx_exp<T>(v[k][h].y - sh));
-                    dt += v[k][h].x + v[k][h].y;
+                    v[k][h] = smx_exp_pair<T>(__fadd2_rn(v[k][h], nsh));
+                    acc = __fadd2_rn(acc, v[k][h]);
                 }
             }
         }
-        const MaxSum r = cta_merge_all<T, NW>(MaxSum{mt, dt}, slot[parity]);
-        if (t == 0) {
+        const float dt = acc.x + acc.y;
+        MaxSum r = cta_merge_all<T, NW>(MaxSum{mt, dt}, slot[parity]);
+        if constexpr (CS > 1) {
+            // a slot of one parity is rewritten two rows later, after another
+            // cluster barrier that every peer reaches only once it has read it
+            if (t == 0) pub[parity] = make_float2(r.m, r.d);
+            cluster_arrive();
+            cluster_wait();
+            const int lane = t & 31;
+            const float2 mine = lane < CS ? ld_dsmem(&pub[parity], (uint32_t)lane)
+                                          : make_float2(-INFINITY, 0.f);
+            r = MaxSum{__shfl_sync(0xffffffffu, mine.x, 0), __shfl_sync(0xffffffffu, mine.y, 0)};
+#pragma unroll
+            for (int k = 1; k < CS; ++k)
+                r = ms_merge<T>(r, MaxSum{__shfl_sync(0xffffffffu, mine.x, k),
+                                          __shfl_sync(0xffffffffu, mine.y, k)});
+        }
+        if (t == 0 && rank == 0) {
             if (a.mean) a.mean[row] = r.m;  // row max
             if (a.rstd) a.rstd[row] = r.d;  // row sum of exp(x - max)
         }
         const float s = (mt == -INFINITY ? 0.f : smx_exp<T>(mt - r.m)) / r.d;
         const float2 s2 = f2(s);
-        T *Y = static_cast<T *>(a.y) + row * a.ldy;
+        T *Y = static_cast<T *>(a.y) + off + row * a.ldy;
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             const int idx = t + k * THREADS;
@@ -158,6 +208,11 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 128 ? NRM_SMX128_MIN_BLOC
                 st_stream(Y + (size_t)idx * V, io2::pack(o));
             }
         }
+    }
+    if constexpr (CS > 1) {
+        // stay resident until every peer has read this CTA's pairs
+        cluster_arrive();
+        cluster_wait();
     }
 }
 
@@ -193,25 +248,29 @@ __global__ void __launch_bounds__(THREADS) softmax_generic_kernel(const RowArgs 
     }
 }
 
-template <typename T, int THREADS, int PACKS, bool FULL = false>
+template <typename T, int THREADS, int PACKS, bool FULL = false, int CS = 1>
 cudaError_t launch_softmax_cta(const RowArgs &a, const Plan &p, cudaStream_t s) {
-    auto kernel = softmax_cta_kernel<T, THREADS, PACKS, FULL>;
+    auto kernel = softmax_cta_kernel<T, THREADS, PACKS, CS, FULL>;
     int64_t pf = 0;
-    if (p.prefetch > 0) {
+    if (CS == 1 && p.prefetch > 0) {
         int per_sm = 0;
         const cudaError_t oe = resident_ctas(reinterpret_cast<const void *>(kernel), THREADS, 0, &per_sm);
         if (oe != cudaSuccess) return oe;
         pf = (int64_t)p.prefetch * p.sms * per_sm;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.gridDim = dim3((unsigned)p.grid);  // rows x CS (clamped)
     cfg.blockDim = dim3(THREADS);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = CS > 1 ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, pf);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
@@ -227,6 +286,18 @@ cudaError_t launch_softmax_t(const RowArgs &a, const Plan &p, cudaStream_t s) {
         default: return cudaErrorInvalidConfiguration;
         }
         return cudaGetLastError();
+    }
+    if (p.kind == PLAN_CLUSTER) {
+#define NRM_SMXC_CASE(TH, PK, CS)                                                   \
+    if (p.threads == TH && p.packs == PK && p.groups == CS) {                       \
+        if (a.N / IO<T>::V == (int64_t)TH * PK * CS)                               \
+            return launch_softmax_cta<T, TH, PK, true, CS>(a, p, s);               \
+        return launch_softmax_cta<T, TH, PK, false, CS>(a, p, s);                  \
+    }
+        NRM_SMXC_CASE(128, 1, 4) NRM_SMXC_CASE(128, 1, 8) NRM_SMXC_CASE(128, 2, 2)
+        NRM_SMXC_CASE(128, 2, 4) NRM_SMXC_CASE(128, 4, 2) NRM_SMXC_CASE(128, 4, 4)
+#undef NRM_SMXC_CASE
+        return cudaErrorInvalidConfiguration;
     }
     if (p.kind != PLAN_CTA) return cudaErrorInvalidConfiguration;
 #define NRM_SMX_CASE(TH, PK) \

@@ -88,6 +88,38 @@ def test_forced_plans(orc, op, dt, plan):
     assert got[0] == plan[0]
 
 
+# cluster split (threads, packs per thread, CTAs per cluster): every compiled
+# instance
+CLUSTER_SHAPES = [(128, 1, 2), (128, 1, 4), (128, 2, 2), (128, 2, 4), (128, 4, 2), (128, 4, 4),
+                  (128, 4, 8), (256, 4, 2)]
+
+
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", CLUSTER_SHAPES, ids=lambda c: f"{c[0]}x{c[1]}c{c[2]}")
+@pytest.mark.parametrize("fill", ["full", "ragged"])
+def test_cluster_split_plans(orc, op, dt, shape, fill):
+    # one row over a cluster of CTAs: every slice exactly THREADS x PACKS packs
+    # (no bounds tests) or 37 packs short of it (bounds tests in every CTA)
+    threads, packs, cs = shape
+    v = 4 if dt == "f32" else 8
+    s = threads * packs - (0 if fill == "full" else min(37, threads * packs - 1))
+    inp = W.generic_rows(op, dt, 45, s * cs * v, seed=cs * 100 + s, scale=1.7, shift=-0.6)
+    nrm.force_plan(nrm.PLAN_CLUSTER, threads, packs, 0, cs)
+    _check(orc, op, inp)
+    assert nrm.last_plan() == (nrm.PLAN_CLUSTER, threads, packs, 0, cs)
+
+
+def test_cluster_split_refuses_rows_it_cannot_split():
+    # 1000 binary32 values are 250 packs: not a multiple of 4 or 8 CTAs
+    x = torch.randn(4, 1000, device="cuda")
+    for cs in (4, 8):
+        nrm.force_plan(nrm.PLAN_CLUSTER, 128, 2, 0, cs)
+        with pytest.raises(nrm.NrmError) as e:
+            nrm.ln_fwd(x)
+        assert e.value.status == 6
+
+
 @pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
 @pytest.mark.parametrize("dt,threads,packs,groups", [("bf16", 128, 4, 4), ("f32", 256, 4, 2),
                                                      ("f16", 256, 2, 1), ("bf16", 128, 4, 8)])
@@ -189,8 +221,10 @@ def test_absent_parameters(orc, op):
 
 
 @pytest.mark.parametrize("plan", [(nrm.PLAN_AUTO,), (nrm.PLAN_CTA, 128, 4), (nrm.PLAN_CTA, 256, 2),
-                                  (nrm.PLAN_PERSIST,), (nrm.PLAN_WARP,), (nrm.PLAN_GENERIC, 256)],
-                         ids=["auto", "cta128x4", "cta256x2", "persist", "warp", "generic"])
+                                  (nrm.PLAN_PERSIST,), (nrm.PLAN_WARP,), (nrm.PLAN_GENERIC, 256),
+                                  (nrm.PLAN_CLUSTER, 128, 2, 0, 2), (nrm.PLAN_CLUSTER, 128, 1, 0, 4)],
+                         ids=["auto", "cta128x4", "cta256x2", "persist", "warp", "generic",
+                              "cluster128x2c2", "cluster128x1c4"])
 @pytest.mark.parametrize("n", [1024, 2048, 4096])
 def test_ln_small_spread_large_mean_f32(orc, n, plan):
     # binary32 rows with mean 1000 and spread 1e-3: the statistics must not
@@ -213,7 +247,8 @@ def test_constant_rows_give_beta_exactly(dt):
     for i, c in enumerate([0.0, 1.0, 1000.0, -7.5, 3.25, 0.125, -1000.0, 42.0]):
         inp["x"][i] = c
     d = {k: v.cuda() for k, v in inp.items()}
-    for plan in [(nrm.PLAN_AUTO, 0, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_CTA, 1024, 1)]:
+    for plan in [(nrm.PLAN_AUTO, 0, 0), (nrm.PLAN_GENERIC, 256, 0), (nrm.PLAN_CTA, 1024, 1),
+                 (nrm.PLAN_CLUSTER, 128, 4, 0, 2), (nrm.PLAN_CLUSTER, 128, 2, 0, 4)]:
         nrm.force_plan(*plan)
         y, mean, _ = nrm.ln_fwd(d["x"], d["gamma"], d["beta"], 1e-5)
         torch.cuda.synchronize()
@@ -298,15 +333,19 @@ def test_bn_plans_agree_and_repeat():
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 8, 28, 28))
     outs = []
     plans = (nrm.PLAN_CTA, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_TMA, nrm.PLAN_GENERIC,
-             nrm.PLAN_PERSIST, nrm.PLAN_PERSIST)
-    for plan in plans:
-        nrm.force_plan(plan)
+             nrm.PLAN_PERSIST, nrm.PLAN_PERSIST, nrm.PLAN_TMA, nrm.PLAN_TMA)
+    for i, plan in enumerate(plans):
+        # the last two: the cluster plan with clusters of 8 CTAs (the first
+        # two cluster runs take the automatic size)
+        nrm.force_plan(plan, 0, 0, 8 if i >= 7 else 0, 0)
         outs.append(RN.run_gpu("bn", inp, 1e-5, 0.1))
+        assert nrm.last_plan()[0] == plan
     for k in outs[0]:
         assert (outs[0][k] == outs[1][k]).all(), k  # bitwise repeatable
         assert (outs[2][k] == outs[3][k]).all(), k
         assert (outs[5][k] == outs[6][k]).all(), k
-        for o in (outs[2], outs[4], outs[5]):
+        assert (outs[7][k] == outs[8][k]).all(), k
+        for o in (outs[2], outs[4], outs[5], outs[7]):
             assert np.max(np.abs(outs[0][k].astype(np.float64) - o[k])) <= 2e-5, k
 
 

@@ -3,7 +3,15 @@ against the CPU oracle: every element of every output, except on the
 BatchNorm workloads of the page's (64, 64, 112, 112) shape, where the GPU runs
 the full tensor and every element of three channels (first, middle, last) is
 checked against the oracle run on those channels alone (BatchNorm channels
-are independent)."""
+are independent).
+
+With NRM_PARITY_REPORT set to a file name, each workload appends one JSON line
+with its measured errors: the largest error, the largest ulp distance and how
+many 16-bit elements passed on the cancellation bound rather than within 1 ulp
+(n_cancel_floor)."""
+import json
+import os
+
 import pytest
 import torch
 
@@ -36,6 +44,11 @@ def test_workload_full_size(orc, w):
     ref = RN.run_oracle(orc, w.op, inp, w.eps, w.momentum)
     rep = RN.compare(w.op, inp, gpu, ref)
     print(w.name, rep)
+    path = os.environ.get("NRM_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"workload": w.name, "checked_elements": int(inp["x"].numel()),
+                                "errors": rep}, default=float) + "\n")
 
 
 def test_add_rms_inplace_residual(orc):
