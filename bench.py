@@ -202,6 +202,8 @@ def plan_name(op, kind_name):
 class Step:
     """One call of the hot path on rotating, pre-filled device buffers."""
 
+    max_sets = 0  # cap on the rotating input sets (profiling runs), 0: none
+
     def __init__(self, w: W.Workload, device, l2_bytes: int, hot: bool = False):
         import row_wise_normalization_reduce_gb300 as nrm
         self.nrm = nrm
@@ -210,6 +212,8 @@ class Step:
         per_set = algorithmic_bytes(w)
         # cold: rotating input sets totalling > 3x L2; hot: one set, reused
         self.nsets = 1 if hot else max(2, int(np.ceil(3 * l2_bytes / per_set)) + 1)
+        if Step.max_sets:
+            self.nsets = min(self.nsets, Step.max_sets)
         dev = lambda t: t.to(device)  # noqa: E731
         self.params = {k: dev(v) for k, v in inp.items() if k not in ("x", "residual", "dy")}
         self.sets = []
@@ -532,6 +536,27 @@ def oracle_time(w: W.Workload, rows_sample: int, reps: int, threads: int):
     rows = x.shape[0]
     res = to_np(inp["residual"][:rows_sample].contiguous()) if w.op == "add_rms" else None
     prm = {k: to_np(v) for k, v in inp.items() if k not in ("x", "residual")}
+    if w.op == "bn":
+        # BatchNorm: channels are independent, so they are split over the
+        # threads (each thread's channels copied out before the timed region)
+        chans = np.array_split(np.arange(x.shape[1]), threads)
+        parts = [(np.ascontiguousarray(x[:, c]), c) for c in chans if len(c)]
+        f64 = lambda v: v.astype(np.float64)  # noqa: E731
+
+        def work_bn(part):
+            xc, c = part
+            orc.batchnorm_train(dt, xc, prm["gamma"][c], prm["beta"][c],
+                                f64(prm["running_mean"][c]), f64(prm["running_var"][c]),
+                                eps=w.eps, momentum=w.momentum)
+
+        with cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work_bn, parts))  # warm-up
+            times = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                list(ex.map(work_bn, parts))
+                times.append(time.perf_counter() - t0)
+        return statistics.median(times), algorithmic_bytes(w) * rows / w.shape[0]
     chunks = np.array_split(np.arange(rows), threads)
 
     def work(idx):
@@ -721,6 +746,35 @@ def secondary(args, device, stream, l2):
     return out
 
 
+def baseline_table(device, stream, l2):
+    """One JSON line per workload of the measured table: graph replay cold and
+    hot, isolated calls after a memset or read scrub, and the oracle on one
+    and on all host cores (the full workload, median of 3)."""
+    peak, _ = measured_peak()
+    cores = os.cpu_count() or 1
+    for w in (W.LN_F32_64x1024, W.RMS_F16_2048x4096, W.ADD_RMS_BF16_4096x4096,
+              W.LN_BF16_1024x16384, W.LN_BF16_4096x4096, W.BN_F32_32x64x56x56):
+        b = algorithmic_bytes(w)
+        cold = Step(w, device, l2)
+        t_cold = time_graphs(cold, 2000, 20, stream)[0] / 2000
+        scrub = Scrub(device, l2, stream)
+        t_iso_w = time_isolated(cold, stream, scrub.write)
+        t_iso_r = time_isolated(cold, stream, scrub.read)
+        plan = cold.plan
+        del cold
+        hot = Step(w, device, l2, hot=True)
+        t_hot = time_graphs(hot, 2000, 20, stream)[0] / 2000
+        del hot, scrub
+        torch.cuda.empty_cache()
+        c1, _ = oracle_time(w, w.shape[0], 3, 1)
+        cn, _ = oracle_time(w, w.shape[0], 3, cores)
+        emit({"w": w.name, "bytes": b, "plan": plan, "graph_cold_us": t_cold * 1e6,
+              "graph_hot_us": t_hot * 1e6, "isolated_memset_us": t_iso_w * 1e6,
+              "isolated_clean_us": t_iso_r * 1e6, "gbs_graph_cold": b / t_cold / 1e9,
+              "frac_measured": b / t_cold / 1e9 / peak, "frac_8tbs": b / t_cold / 8e12,
+              "oracle_1core_ms": c1 * 1e3, "oracle_allcore_ms": cn * 1e3, "cores": cores})
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -731,6 +785,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="at most this many rotating input sets (for small profiling runs; "
+                         "the default keeps them above 3x L2)")
+    ap.add_argument("--baseline-table", action="store_true",
+                    help="print the measured table of the six workloads (per-call timings, "
+                         "oracle on one and on all cores) instead of the bench line")
     ap.add_argument("--no-targets", action="store_true",
                     help="skip the per-call timings of the two 4096x4096 bf16 targets")
     ap.add_argument("--plan", default="auto",
@@ -739,6 +799,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    Step.max_sets = max(0, args.sets)
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -765,6 +826,9 @@ def main():
         nrm.force_plan(code, *[int(v) for v in nums])
     stream = torch.cuda.Stream(device)
     l2 = l2_size(local)
+    if args.baseline_table:
+        baseline_table(device, stream, l2)
+        return
 
     step = Step(w, device, l2)
     sampler = ClockSampler(local)

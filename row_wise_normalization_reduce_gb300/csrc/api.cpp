@@ -221,10 +221,12 @@ int choose_plan(Op op, const RowArgs &a, int dtype, const DevInfo &dev, Plan *pl
     case PLAN_CTA: {
         if (!vec_ok) return NRM_ERR_UNSUPPORTED;
         int packs = fpacks, threads = fthreads;
-        // 256 x 2 for 512 packs; LayerNorm: 128 x 4 (measured 12.3 us against
-        // 14.0 us for 256 x 2 at 4096 x 4096 bf16: half the per-element share
-        // of its two row-wide sums)
-        if (!packs) packs = P <= 256 ? 1 : (op == OP_LN && P <= 512) ? 4 : P <= 1024 ? 2 : 4;
+        // 128 x 4 for 512 packs for LayerNorm (measured 12.3 us against 14.0 us
+        // for 256 x 2 at 4096 x 4096 bf16: half the per-element share of its
+        // two row-wide sums) and RMSNorm (2048 x 4096 fp16: 5.65 us against
+        // 5.94 us: twice the bytes in flight per thread); add+RMSNorm, with
+        // two inputs in flight, keeps 256 x 2
+        if (!packs) packs = P <= 256 ? 1 : (op != OP_ADD_RMS && P <= 512) ? 4 : P <= 1024 ? 2 : 4;
         if (!threads) {
             threads = round_up_pow2((P + packs - 1) / packs);
             if (threads < 128) threads = 128;

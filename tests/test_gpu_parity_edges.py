@@ -256,9 +256,14 @@ def test_constant_rows_give_beta_exactly(dt):
         assert torch.equal(mean.cpu(), inp["x"][:, 0].float())
 
 
-def test_zero_residual_equals_rms():
+@pytest.mark.parametrize("plan", [(nrm.PLAN_CTA, 256, 2), (nrm.PLAN_CTA, 128, 4)],
+                         ids=["cta256x2", "cta128x4"])
+def test_zero_residual_equals_rms(plan):
+    # on the same plan (same reduction order) a zero residual gives RMSNorm's
+    # bits exactly
     inp = W.generic_rows("rms", "bf16", 64, 4096, seed=4)
     d = {k: v.cuda() for k, v in inp.items()}
+    nrm.force_plan(*plan)
     y1, r1 = nrm.rms_fwd(d["x"], d["w"], 1e-6, want_stats=True)
     ro, y2, r2 = nrm.add_rms_fwd(d["x"], torch.zeros_like(d["x"]), d["w"], 1e-6, want_stats=True)
     assert torch.equal(ro, d["x"])
@@ -305,6 +310,26 @@ def test_guard_bands_untouched(op):
 # one-pass dataflow kernel
 BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC, nrm.PLAN_PERSIST]
 BN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
+
+
+@pytest.mark.parametrize("cs", [2, 4, 8])
+@pytest.mark.parametrize("shape", [(1, 1, 8, 8), (3, 5, 13, 12), (9, 6, 20, 20), (64, 3, 8, 8),
+                                   (32, 4, 56, 56), (5, 2, 1, 4)])
+def test_bn_cluster_sizes(orc, shape, cs):
+    # the cluster plan at every cluster size; ranks beyond the batch hold no
+    # planes
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape)
+    nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    # the cluster plan takes at most 16 planes per CTA and two buffers of
+    # at most 200 KB; otherwise another plan runs
+    batch, hw = shape[0], shape[2] * shape[3]
+    while cs > 1 and cs > batch:
+        cs //= 2
+    ppc = -(-batch // cs)
+    fits = ppc <= 16 and 2 * ppc * hw * 4 <= 200 * 1024
+    assert (nrm.last_plan()[0] == nrm.PLAN_TMA) == fits
+    RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
 
 
 @pytest.mark.parametrize("plan", BN_PLANS, ids=BN_IDS)
