@@ -56,16 +56,25 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
-// The CTA plan's exponentials of a pair, e = exp(d) for d = x - m_t <= 0.
-// Binary32 outputs: expf.  16-bit outputs: exp(d) = 2^(d log2 e), the
-// product formed pairwise and PTX's ex2.approx (an error of a few binary32
+// The CTA plan's exponentials of a pair, for d = x - m_t <= 0, scaled by
+// kSmxScale<T>.  Binary32 outputs: expf(d), unscaled.  16-bit outputs:
+// 2^16 exp(d) = 2^(d log2 e + 16), the exponent formed pairwise with one
+// fused multiply-add and PTX's ex2.approx.ftz (an error of a few binary32
 // ulp, like __expf; with the rounding of d log2 e, below 1e-5 relative for
-// |d| < 100, far inside the 1-ulp tolerance of binary16 and bfloat16).
+// |d| < 100, far inside the 1-ulp tolerance of binary16 and bfloat16).  The
+// 2^16 scale keeps every exponential whose output can be a nonzero
+// bfloat16 (down to its smallest subnormal, 2^-133) a normal binary32, so
+// the flush to zero of the fast instruction only drops values that round to
+// zero anyway; the sums carry the same exact power-of-two scale, which the
+// output's 1/d removes and the reported row sum divides out.
+template <typename T> struct SmxScale { static constexpr float v = 65536.0f; };
+template <> struct SmxScale<float> { static constexpr float v = 1.0f; };
+
 template <typename T> __device__ __forceinline__ float2 smx_exp_pair(float2 d) {
-    const float2 t = __fmul2_rn(d, f2(1.44269504088896341f));
+    const float2 t = __ffma2_rn(d, f2(1.44269504088896341f), f2(16.0f));
     float2 r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r.x) : "f"(t.x));
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r.y) : "f"(t.y));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(t.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(t.y));
     return r;
 }
 template <> __device__ __forceinline__ float2 smx_exp_pair<float>(float2 d) {
@@ -192,8 +201,8 @@ __global__ void __launch_bounds__(THREADS, (THREADS == 128 ? (CS == 1 && FULL ? 
                                           __shfl_sync(0xffffffffu, mine.y, k)});
         }
         if (t == 0 && rank == 0) {
-            if (a.mean) a.mean[row] = r.m;  // row max
-            if (a.rstd) a.rstd[row] = r.d;  // row sum of exp(x - max)
+            if (a.mean) a.mean[row] = r.m;                      // row max
+            if (a.rstd) a.rstd[row] = r.d / SmxScale<T>::v;     // row sum of exp(x - max)
         }
         const float s = (mt == -INFINITY ? 0.f : smx_exp<T>(mt - r.m)) / r.d;
         const float2 s2 = f2(s);

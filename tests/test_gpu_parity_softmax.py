@@ -68,6 +68,22 @@ def test_softmax_masked_large_and_constant(orc, dtype, plan):
     assert np.all(RN.B.bits_to_f64(RN.B.dt_code(inp["x"].dtype), gpu["y"][5, 1:]) == 0.0)
 
 
+@pytest.mark.parametrize("plan", [(nrm.PLAN_AUTO,), (nrm.PLAN_GENERIC,), (nrm.PLAN_CLUSTER, 128, 2, 0, 4)],
+                         ids=["auto", "generic", "cluster"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_softmax_wide_logits_reach_subnormal_outputs(orc, dtype, plan):
+    # logits spread over hundreds: many outputs fall below the smallest
+    # normal (bfloat16 keeps subnormals down to 2^-133), which the fast
+    # exponential path must neither flush early nor mis-round
+    inp = _inputs(dtype, 24, 4096, seed=77, scale=45.0, shift=-5.0)
+    nrm.force_plan(*plan)
+    gpu = RN.run_gpu("softmax", inp, 0.0)
+    RN.compare("softmax", inp, gpu, RN.run_oracle(orc, "softmax", inp, 0.0))
+    y = RN.B.bits_to_f64(RN.B.dt_code(inp["x"].dtype), gpu["y"])
+    if dtype == "bf16":  # the test does reach bfloat16 subnormal outputs
+        assert np.any((y > 0) & (y < 2.0 ** -126))
+
+
 def test_softmax_empty_and_repeatable():
     nrm.force_plan(nrm.PLAN_AUTO)
     x = torch.empty(0, 128, device="cuda")
