@@ -342,7 +342,7 @@ template <int OP, int THREADS, int PACKS, bool FULL = false>
 constexpr int row_min_blocks() {
     return (OP == OP_RMS && PACKS <= 2 && NRM_RMS_MIN_THREADS / THREADS > 0) ? NRM_RMS_MIN_THREADS / THREADS
            : (PACKS <= 2 && NRM_CTA_MIN_THREADS / THREADS > 0) ? NRM_CTA_MIN_THREADS / THREADS
-           : (OP != OP_ADD_RMS && PACKS == 4 && THREADS <= 256 && FULL &&
+           : (OP != OP_ADD_RMS && PACKS == 4 && THREADS <= 512 && FULL &&
               NRM_LN4_FULL_MIN_THREADS / THREADS > 0)
                ? NRM_LN4_FULL_MIN_THREADS / THREADS
            : (OP == OP_LN && PACKS == 4 && THREADS <= 256 && NRM_LN4_MIN_THREADS / THREADS > 0)
@@ -966,6 +966,7 @@ cudaError_t launch_row(const RowArgs &a, const Plan &p, cudaStream_t s) {
         a.N / IO<T>::V == TH * PK)                                                  \
         return launch_cta<OP, T, TH, PK, true>(a, p, s);
         NRM_CTA_FULL_CASE(128, 4) NRM_CTA_FULL_CASE(256, 2) NRM_CTA_FULL_CASE(256, 4)
+        NRM_CTA_FULL_CASE(512, 4)
 #undef NRM_CTA_FULL_CASE
         NRM_CTA_CASE(128, 1) NRM_CTA_CASE(256, 1) NRM_CTA_CASE(512, 1) NRM_CTA_CASE(1024, 1)
         NRM_CTA_CASE(128, 2) NRM_CTA_CASE(256, 2) NRM_CTA_CASE(512, 2) NRM_CTA_CASE(1024, 2)
