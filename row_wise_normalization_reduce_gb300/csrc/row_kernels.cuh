@@ -125,19 +125,74 @@ template <typename T> struct SmemParams {
     __device__ __forceinline__ void p1_pack(int idx, float2 *f) const { load(1, idx, f); }
 };
 
-// Widen parameters into the SmemParams layout (absent gamma/w = 1, beta = 0).
+// Widen parameters into the SmemParams layout (absent gamma/w = 1, beta = 0),
+// one 16-byte pack per thread and step (the plans that use it need 16-byte
+// aligned parameters and N a multiple of the pack width).
 template <typename T, int NPARAM, int THREADS>
 __device__ __forceinline__ void fill_smem_params(const RowArgs &a, float *sp) {
-    constexpr int V = IO<T>::V, Q = V / 4;
+    constexpr int V = IO<T>::V, Q = V / 4, H = IO2<T>::H;
     const int P = (int)(a.N / V);
     const T *src[2] = {static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
     const float dflt[2] = {1.f, 0.f};
-    for (int i = threadIdx.x; i < (int)a.N; i += THREADS) {
-        const int idx = i / V, j = i % V, h = j / 4, l = j % 4;
+    float4 *q = reinterpret_cast<float4 *>(sp);
+    for (int idx = threadIdx.x; idx < P; idx += THREADS) {
+#pragma unroll
+        for (int p = 0; p < NPARAM; ++p) {
+            float2 f[H];
+            if (src[p]) IO2<T>::unpack(ld_param(src[p] + (size_t)idx * V), f);
+            else
+#pragma unroll
+                for (int h = 0; h < H; ++h) f[h] = f2(dflt[p]);
+#pragma unroll
+            for (int h = 0; h < Q; ++h)
+                q[((size_t)p * Q + h) * P + idx] =
+                    make_float4(f[2 * h].x, f[2 * h].y, f[2 * h + 1].x, f[2 * h + 1].y);
+        }
+    }
+}
+
+// Parameters kept in shared memory in their storage type: the raw 16-byte
+// packs of gamma (w) at [0, P) and beta at [P, 2P), copied once per CTA and
+// unpacked per use (half the shared memory of SmemParams at 16-bit types).
+// An absent parameter is never read: 1 (gamma, w) or 0 (beta).
+template <typename T> struct SmemRawParams {
+    const uint4 *q;
+    int P;
+    bool has0, has1;
+    __device__ __forceinline__ void p0_pack(int idx, float2 *f) const {
+        if (has0) IO2<T>::unpack(q[idx], f);
+        else
+#pragma unroll
+            for (int h = 0; h < IO2<T>::H; ++h) f[h] = f2(1.f);
+    }
+    __device__ __forceinline__ void p1_pack(int idx, float2 *f) const {
+        if (has1) IO2<T>::unpack(q[P + idx], f);
+        else
+#pragma unroll
+            for (int h = 0; h < IO2<T>::H; ++h) f[h] = f2(0.f);
+    }
+};
+
+// Copy the present parameters into the SmemRawParams layout.
+template <typename T, int NPARAM, int THREADS>
+__device__ __forceinline__ void fill_smem_raw_params(const RowArgs &a, uint4 *q) {
+    constexpr int V = IO<T>::V;
+    const int P = (int)(a.N / V);
+    const T *src[2] = {static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
+    for (int idx = threadIdx.x; idx < P; idx += THREADS)
 #pragma unroll
         for (int p = 0; p < NPARAM; ++p)
-            sp[(((size_t)p * Q + h) * P + idx) * 4 + l] = src[p] ? IO<T>::to_f(src[p][i]) : dflt[p];
-    }
+            if (src[p]) q[(size_t)p * P + idx] = ld_param(src[p] + (size_t)idx * V);
+}
+
+// Where a plan keeps its parameters (Plan::smem_params).
+enum ParamsIn { PARAMS_GLOBAL = 0, PARAMS_SMEM_F32 = 1, PARAMS_SMEM_RAW = 2 };
+
+// Dynamic shared-memory bytes of the parameters for a ParamsIn mode.
+template <int OP, typename T>
+inline size_t params_smem_bytes(int mode, int64_t N) {
+    const size_t n = (size_t)N * (OP == OP_LN ? 2 : 1);
+    return mode == PARAMS_SMEM_F32 ? n * sizeof(float) : mode == PARAMS_SMEM_RAW ? n * sizeof(T) : 0;
 }
 
 struct NoHook {
@@ -829,7 +884,7 @@ cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (p.stages < 2 || p.stages > kMaxStages || !a.fault || p.sms < 1)
         return cudaErrorInvalidConfiguration;
     const size_t stage = (size_t)a.N * sizeof(T) * (OP == OP_ADD_RMS ? 2 : 1);
-    const size_t params = p.smem_params ? (size_t)a.N * sizeof(float) * (OP == OP_LN ? 2 : 1) : 0;
+    const size_t params = params_smem_bytes<OP, T>(p.smem_params, a.N);
     const size_t smem = params + stage * (size_t)p.stages * G;
     if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
     int per_sm = 0;
@@ -838,8 +893,7 @@ cudaError_t launch_pipe(const RowArgs &a, const Plan &p, cudaStream_t s) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)p.sms * per_sm;
     const int64_t grid = a.rows < slots ? a.rows : slots;
-    kernel<<<(unsigned)grid, GT * G, smem, s>>>(a, p.stages, p.smem_params);
-    return cudaGetLastError();
+    return launch_row(kernel, (unsigned)grid, GT * G, smem, s, a, p.stages, p.smem_params);
 }
 
 // Persistent launch: dynamic shared memory = parameters in

@@ -10,14 +10,14 @@
 // contiguous, balanced range of rows (its count differs from any other CTA's
 // by at most one) that its groups share dynamically.
 //
-// Per row a group: waits for its stage, copies the raw 16-byte packs into
-// registers (16 registers for 32 bf16 values), releases the stage at the
-// first group barrier (the leader starts the next copy into it), and makes
-// two (LayerNorm) or one (RMS ops) group-wide sums, unpacking the packs again
-// for each pass: unpacking is one integer operation per element, cheaper
-// than the registers to hold the values in binary32.  Parameters are read
-// from shared memory already widened to binary32 (SmemParams) when they fit,
-// else from global memory through L1.
+// Per row a group: waits for its stage, copies the row's packs into
+// registers (widened to binary32 once when a thread holds at most 4 packs,
+// else unpacked again for each pass), releases the stage at the first group
+// barrier (the leader starts the next copy into it), and makes two
+// (LayerNorm) or one (RMS ops) group-wide sums.  Parameters are read from
+// shared memory: widened to binary32 (SmemParams) when several groups share
+// them and they fit, else as raw packs (SmemRawParams) when those fit beside
+// the stages; else from global memory through L1.
 //
 // Termination and failure are decided together at the first group barrier
 // (bar.red.or): a leader that finds the range exhausted publishes row -1 for
@@ -34,9 +34,8 @@
 template <int OP, typename T>
 __device__ __forceinline__ void pipe_claim(const RowArgs &a, unsigned long long *next_row,
                                            int64_t r1, long long *slot_row, uint64_t *full,
-                                           unsigned char *ring, int stages, uint32_t stage_bytes,
-                                           uint32_t row_bytes, int64_t li) {
-    const int s = (int)(li % stages);
+                                           unsigned char *ring, uint32_t stage_bytes,
+                                           uint32_t row_bytes, const int s) {
     const long long r = (long long)atomicAdd(next_row, 1ULL);
     if (r < r1) {
         slot_row[s] = r;
@@ -61,6 +60,11 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
     constexpr int V = IO<T>::V;
     constexpr int H = io2::H;
     constexpr int NWG = GT / 32;
+    // rows of up to 4 packs per thread are widened to binary32 once and kept
+    // in registers (unpacking them for each pass cost 50 % more instructions
+    // at 16384 bf16); 8 packs per thread would not fit, so they are unpacked
+    // again for each pass
+    constexpr bool kWide = PACKS <= 4;
     static_assert(GT % 32 == 0 && (NWG & (NWG - 1)) == 0 && NWG >= 1 && NWG <= 32, "group size");
     static_assert(G >= 1 && G <= 15 && GT * G <= 1024, "groups per CTA");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -84,40 +88,67 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
     const uint32_t row_bytes = (uint32_t)(a.N * (int64_t)sizeof(T));
     const uint32_t stage_bytes = row_bytes * (OP == OP_ADD_RMS ? 2u : 1u);
     const int nparams = (OP == OP_LN) ? 2 : 1;
-    const size_t params_bytes = smem_params ? (size_t)nparams * (size_t)a.N * sizeof(float) : 0;
+    const size_t params_bytes = smem_params == PARAMS_SMEM_F32 ? (size_t)nparams * (size_t)a.N * sizeof(float)
+                                : smem_params == PARAMS_SMEM_RAW ? (size_t)nparams * (size_t)a.N * sizeof(T)
+                                                                 : 0;
     unsigned char *ring = smem + params_bytes + (size_t)g * stages * stage_bytes;
 
+#if NRM_ROW_PDL
+    // programmatic dependent launch, as the other row kernels: the first rows
+    // of the CTA's range are requested from L2 before the wait for the
+    // previous grid (whose writes still reach the bulk copies issued after it)
+    if (threadIdx.x == 0) {
+        for (int64_t r = r0; r < r1 && r < r0 + (int64_t)G * stages; ++r) {
+            prefetch_l2_bulk(static_cast<const T *>(a.x) + r * a.ldx, row_bytes);
+            if (OP == OP_ADD_RMS) prefetch_l2_bulk(static_cast<const T *>(a.res) + r * a.ldr, row_bytes);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+#endif
     if (threadIdx.x == 0) next_row = (unsigned long long)r0;
     __syncthreads();
     int64_t issued = 0;  // leader: local row indices claimed so far
+    int claim_s = 0;     // leader: the stage of the next claim (issued % stages)
     if (t == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&full[g][s], 1);
         fence_mbar_init();
         for (; issued < stages; ++issued)
-            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stages, stage_bytes,
-                              row_bytes, issued);
+            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stage_bytes, row_bytes,
+                              (int)issued);
     }
-    if (smem_params) fill_smem_params<T, (OP == OP_LN ? 2 : 1), GT * G>(a, reinterpret_cast<float *>(smem));
+    if (smem_params == PARAMS_SMEM_F32)
+        fill_smem_params<T, (OP == OP_LN ? 2 : 1), GT * G>(a, reinterpret_cast<float *>(smem));
+    else if (smem_params == PARAMS_SMEM_RAW)
+        fill_smem_raw_params<T, (OP == OP_LN ? 2 : 1), GT * G>(a, reinterpret_cast<uint4 *>(smem));
     __syncthreads();
 
     const float fN = a.fN;
     const float invN = a.invN;
     const SmemParams<T> sprm{reinterpret_cast<const float4 *>(smem), P};
+    const SmemRawParams<T> rprm{reinterpret_cast<const uint4 *>(smem), P, a.p0 != nullptr,
+                                a.p1 != nullptr};
     const GlobalParams<T> gprm{static_cast<const T *>(a.p0), static_cast<const T *>(a.p1)};
 
+    // row li of the group sits in stage s, whose phase parity is ph (kept
+    // incrementally: a 64-bit division per row cost more than the row's
+    // arithmetic)
     int64_t li = 0;
+    int s = 0;
+    uint32_t ph = 0;
     bool gave_up = false;
-    for (;; ++li) {
-        const int s = (int)(li % stages);
+    for (;; ++li, s = s + 1 == stages ? 0 : s + 1, ph ^= (s == 0)) {
         const int par = (int)(li & 1);
-        const bool ok = mbar_wait_bounded(&full[g][s], (uint32_t)((li / stages) & 1), a.wait_limit);
+        const bool ok = mbar_wait_bounded(&full[g][s], ph, a.wait_limit);
         if (!ok) atomicOr(a.fault, FAULT_WAIT);
         const int64_t row = slot_row[g][s];
         const bool valid = ok && row >= 0;
         const uint4 *st = reinterpret_cast<const uint4 *>(ring + (size_t)s * stage_bytes);
 
-        // raw packs of the row (add+RMS: the rounded residual-stream packs)
+        // the row's raw packs (add+RMS: the rounded residual-stream packs,
+        // also stored as residual_out); with kWide also widened once
         uint4 raw[PACKS];
+        float2 v[kWide ? PACKS : 1][H];
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             const int idx = t + k * GT;
@@ -134,16 +165,29 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
                     if (valid)
                         st_stream(static_cast<T *>(a.res_out) + row * a.ldro + (size_t)idx * V, raw[k]);
                 }
+                if constexpr (kWide) io2::unpack(raw[k], v[k]);
+            } else if constexpr (kWide) {
+#pragma unroll
+                for (int h = 0; h < H; ++h) v[k][h] = f2(0.f);  // contributes nothing
             }
         }
+        // the values of pack k (kWide: the registers; else unpacked again)
+        auto vals = [&](int k, float2 *f) {
+            if constexpr (kWide) {
+#pragma unroll
+                for (int h = 0; h < H; ++h) f[h] = v[k][h];
+            } else {
+                io2::unpack(raw[k], f);
+            }
+        };
 
         // pass 1: sum (LayerNorm) or sum of squares (RMS ops)
         float2 acc = f2(0.f);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
-            if (t + k * GT < P) {
+            if (kWide || t + k * GT < P) {
                 float2 f[H];
-                io2::unpack(raw[k], f);
+                vals(k, f);
 #pragma unroll
                 for (int h = 0; h < H; ++h)
                     acc = (OP == OP_LN) ? __fadd2_rn(acc, f[h]) : __ffma2_rn(f[h], f[h], acc);
@@ -160,9 +204,10 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
         if (t == 0 && issued < li + stages + 1) {
             // every thread holds this row in registers: refill its stage
             fence_proxy_async_smem();
-            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stages, stage_bytes,
-                              row_bytes, issued);
+            pipe_claim<OP, T>(a, &next_row, r1, slot_row[g], full[g], ring, stage_bytes, row_bytes,
+                              claim_s);
             ++issued;
+            claim_s = claim_s + 1 == stages ? 0 : claim_s + 1;
         }
 
         float rstd, m0 = 0.f, c = 0.f;
@@ -176,10 +221,11 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
             for (int k = 0; k < PACKS; ++k) {
                 if (t + k * GT < P) {
                     float2 f[H];
-                    io2::unpack(raw[k], f);
+                    vals(k, f);
 #pragma unroll
                     for (int h = 0; h < H; ++h) {
                         const float2 e = __fadd2_rn(f[h], nm);
+                        if constexpr (kWide) v[k][h] = e;
                         e1 = __fadd2_rn(e1, e);
                         e2 = __ffma2_rn(e, e, e2);
                     }
@@ -199,25 +245,29 @@ __global__ void __launch_bounds__(GT *G, (1024 / (GT * G)) > 0 ? (1024 / (GT * G
             if (t == 0 && a.rstd) a.rstd[row] = rstd;
         }
 
-        // pass 3: normalize, scale (and shift), round once, store
+        // pass 3: normalize, scale (and shift), round once, store; LayerNorm
+        // computes ((x - m0) - c) * rstd * gamma + beta either way
         T *Y = static_cast<T *>(a.y) + row * a.ldy;
-        const float2 r2 = f2(rstd), nm = f2(-m0), nc = f2(-c);
+        const float2 r2 = f2(rstd), nm = f2(kWide ? 0.f : -m0), nc = f2(-c);
 #pragma unroll
         for (int k = 0; k < PACKS; ++k) {
             const int idx = t + k * GT;
             if (idx < P) {
                 float2 f[H], g2[H], out[H];
-                io2::unpack(raw[k], f);
-                if (smem_params) sprm.p0_pack(idx, g2);
+                vals(k, f);
+                if (smem_params == PARAMS_SMEM_RAW) rprm.p0_pack(idx, g2);
+                else if (smem_params) sprm.p0_pack(idx, g2);
                 else gprm.p0_pack(idx, g2);
                 if (OP == OP_LN) {
                     float2 b2[H];
-                    if (smem_params) sprm.p1_pack(idx, b2);
+                    if (smem_params == PARAMS_SMEM_RAW) rprm.p1_pack(idx, b2);
+                    else if (smem_params) sprm.p1_pack(idx, b2);
                     else gprm.p1_pack(idx, b2);
 #pragma unroll
-                    for (int h = 0; h < H; ++h)
-                        out[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(__fadd2_rn(f[h], nm), nc), r2),
-                                            g2[h], b2[h]);
+                    for (int h = 0; h < H; ++h) {
+                        const float2 e = kWide ? f[h] : __fadd2_rn(f[h], nm);
+                        out[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(e, nc), r2), g2[h], b2[h]);
+                    }
                 } else {
 #pragma unroll
                     for (int h = 0; h < H; ++h) out[h] = __fmul2_rn(__fmul2_rn(f[h], r2), g2[h]);
