@@ -20,9 +20,12 @@
 // first element x[0, c, 0]: the shift keeps channels with a large mean and a
 // small spread free of cancellation.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "bn_common.cuh"
@@ -313,10 +316,25 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a, co
 constexpr int BNC_THREADS = 512;
 constexpr int kBnMaxPpc = 16;  // planes per CTA (one mbarrier each per buffer)
 
-template <typename T>
+// How a CTA's planes of one channel arrive: BnBox<false>, one bulk copy per
+// plane, each on its own barrier; BnBox<true>, one tiled tensor copy (TMA) of
+// the box HW as k x HW / k, one channel, ppc planes, on one barrier.
+template <bool BOX> struct BnBox {};
+template <> struct BnBox<true> {
+    CUtensorMap map;  // 64-byte aligned, first
+    uint32_t bytes;   // the box's bytes (out-of-range planes included)
+};
+
+// The loads of channel c's planes n0 .. n0 + np - 1 into `buf`.
+template <typename T, bool BOX>
 __device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uint64_t *bars,
                                                 int64_t c, int64_t n0, int np, int q,
-                                                uint32_t plane_bytes) {
+                                                uint32_t plane_bytes, const BnBox<BOX> &box) {
+    if constexpr (BOX) {
+        mbar_arrive_expect_tx(&bars[0], box.bytes);
+        tma_load_4d(buf, &box.map, 0, 0, (int)c, (int)n0, &bars[0]);
+        return;
+    }
     for (int j = 0; j < np; ++j) {
         mbar_arrive_expect_tx(&bars[j], plane_bytes);
         bulk_g2s(buf + (size_t)j * q, static_cast<const T *>(a.x) + ((n0 + j) * a.C + c) * a.HW,
@@ -326,14 +344,15 @@ __device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uin
 
 // Four 512-thread CTAs per SM (at most 32 registers): with fewer, the 8-CTA
 // clusters of a 64-channel batch no longer all fit at once.
-template <typename T>
-__global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs a, const int ppc) {
+template <typename T, bool BOX>
+__global__ void __launch_bounds__(BNC_THREADS, 4)
+    bn_cluster_kernel(const BnArgs a, const int ppc, const __grid_constant__ BnBox<BOX> box) {
     namespace cg = cooperative_groups;
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     constexpr int V = IO<T>::V;
     constexpr int NW = BNC_THREADS / 32;
-    extern __shared__ __align__(16) uint4 sx[];  // two buffers of ppc planes
+    extern __shared__ __align__(128) uint4 sx[];  // two buffers of ppc planes
     __shared__ __align__(8) uint64_t bar[2][kBnMaxPpc];
     __shared__ float s1[2][NW];
     __shared__ float s2[2][NW];
@@ -354,7 +373,8 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     const int q = (int)(HW / V);  // 16-byte packs per plane
     const int tp = np * q;        // packs of this CTA's planes
     const uint32_t plane_bytes = (uint32_t)(HW * (int64_t)sizeof(T));
-    const size_t buf_packs = (size_t)ppc * q;
+    // each buffer starts at a multiple of 128 bytes (a tensor copy's rule)
+    const size_t buf_packs = ((size_t)ppc * q + 7) & ~(size_t)7;
     const float cnt = (float)np * (float)HW;
     const float ctot = (float)(a.batch * HW);
 
@@ -371,7 +391,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
     pdl_launch_dependents();
     if (tid == 0) {
         s_fail = 0;
-        for (int j = 0; j < np; ++j) {
+        for (int j = 0; j < (BOX ? 1 : np); ++j) {
             mbar_init(&bar[0][j], 1);
             mbar_init(&bar[1][j], 1);
         }
@@ -379,7 +399,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         for (int b = 0; b < 2; ++b) {
             const int64_t c = first_c + b * K_clusters;
             if (np > 0 && c < C) {
-                bn_issue_planes<T>(a, sx + b * buf_packs, bar[b], c, n0, np, q, plane_bytes);
+                bn_issue_planes<T, BOX>(a, sx + b * buf_packs, bar[b], c, n0, np, q, plane_bytes, box);
                 if (b == 0) last_issued0 = 0;
                 else last_issued1 = 1;
             }
@@ -403,10 +423,15 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         bool have = false;
         float2 a1 = f2(0.f), a2 = f2(0.f);
         int idx = tid;
+        // with a box, its one barrier covers every plane
+        if (BOX && idx < tp && !mbar_wait_bounded(&bar[b][0], par, a.wait_limit)) {
+            s_fail = 1;  // read by thread 0 after the next __syncthreads
+            atomicOr(a.fault, FAULT_WAIT);
+        }
         for (int j = 0; j < np; ++j) {
             const int end = (j + 1) * q;
             if (idx >= end) continue;
-            if (!mbar_wait_bounded(&bar[b][j], par, a.wait_limit)) {
+            if (!BOX && !mbar_wait_bounded(&bar[b][j], par, a.wait_limit)) {
                 s_fail = 1;  // read by thread 0 after the next __syncthreads
                 atomicOr(a.fault, FAULT_WAIT);
             }
@@ -494,7 +519,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         const int64_t next = c + 2 * K_clusters;
         if (tid == 0 && np > 0 && next < C && !s_fail) {
             fence_proxy_async_smem();
-            bn_issue_planes<T>(a, sx + b * buf_packs, bar[b], next, n0, np, q, plane_bytes);
+            bn_issue_planes<T, BOX>(a, sx + b * buf_packs, bar[b], next, n0, np, q, plane_bytes, box);
             if (b == 0) last_issued0 = i + 2;
             else last_issued1 = i + 2;
         }
@@ -506,7 +531,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
         for (int b = 0; b < 2; ++b) {
             const int li = b == 0 ? last_issued0 : last_issued1;
             if (li < 0) continue;
-            for (int j = 0; j < np; ++j)
+            for (int j = 0; j < (BOX ? 1 : np); ++j)
                 if (!mbar_wait_bounded(&bar[b][j], (uint32_t)((li >> 1) & 1), 1u << 22))
                     atomicOr(a.fault, FAULT_DRAIN);
         }
@@ -520,20 +545,68 @@ __global__ void __launch_bounds__(BNC_THREADS, 4) bn_cluster_kernel(const BnArgs
 // are more channels than resident clusters, each cluster pipelines its
 // channels through two buffers.  Otherwise the streaming two kernels when
 // the planes are 16-byte aligned and one unit long; else the scalar plan.
+#ifndef NRM_BN_TMAP
+#define NRM_BN_TMAP 1
+#endif
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nothing
+// links against the driver library); null when unavailable.
+inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of the cluster kernel's loads: x seen as [batch][C][HW / k][k]
+// (k innermost), box k x HW / k x 1 x ppc, so one tiled copy brings a CTA its
+// ppc planes of one channel, laid out plane after plane as the per-plane
+// copies would.  False (per-plane copies) when no view fits the tensor-copy
+// rules: innermost box side a multiple of 16 bytes, every box side at most
+// 256, strides multiples of 16 bytes (buffers sit at multiples of 128 bytes).
 template <typename T>
-cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
-    *launched = false;
-    auto kernel = bn_cluster_kernel<T>;
-    // clusters of 4 CTAs when a CTA's two buffers fit (measured at
-    // [32, 64, 56, 56]: binary32 11.8 us against 12.5 us with 8, bfloat16
-    // 10.3 against 10.9), else 8; a forced size (2, 4 or 8) wins
-    int cs = a.cluster_size;
-    if (cs != 2 && cs != 4 && cs != 8)
-        cs = 2 * (size_t)((a.batch + 3) / 4) * (size_t)a.HW * sizeof(T) <= (size_t)200 * 1024 ? 4 : 8;
-    while (cs > 1 && cs > a.batch) cs >>= 1;
-    const int64_t ppc = (a.batch + cs - 1) / cs;
-    const size_t buf = (size_t)ppc * (size_t)a.HW * sizeof(T);
-    if (ppc > kBnMaxPpc || 2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
+bool bn_box_map(const BnArgs &a, int64_t ppc, size_t buf, CUtensorMap *m, uint32_t *box_bytes) {
+    const int64_t es = (int64_t)sizeof(T), HW = a.HW;
+    if (!NRM_BN_TMAP || !bn_aligned16(a.x) || (HW * es) % 16 || buf % 128 || ppc > 256 ||
+        a.batch > 0x7fffffff || a.C > 0x7fffffff)
+        return false;
+    int64_t k = 0;
+    for (int64_t d = 256; d >= 1 && !k; --d)
+        if (HW % d == 0 && (d * es) % 16 == 0 && HW / d <= 256) k = d;
+    const auto enc = tmap_encoder();
+    if (!k || !enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)k, (cuuint64_t)(HW / k), (cuuint64_t)a.C,
+                                (cuuint64_t)a.batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)(k * es), (cuuint64_t)(HW * es),
+                                   (cuuint64_t)(a.C * HW * es)};
+    const cuuint32_t box[4] = {(cuuint32_t)k, (cuuint32_t)(HW / k), 1u, (cuuint32_t)ppc};
+    const cuuint32_t unit[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt = sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : bn_dtype<T>() == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (enc(m, dt, 4, const_cast<void *>(a.x), dims, strides, box, unit,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    *box_bytes = (uint32_t)(ppc * HW * es);  // at most buf
+    return true;
+}
+
+// Launch of one instance (per-plane copies, or one box) for cs CTAs per
+// cluster of ppc planes each, buffers of buf bytes.
+template <typename T, bool BOX>
+cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched, int cs,
+                                int64_t ppc, size_t buf, const BnBox<BOX> &box) {
+    auto kernel = bn_cluster_kernel<T, BOX>;
     static std::mutex mu;  // one per instance
     static int attr_done[64];
     int dev = 0;
@@ -582,8 +655,36 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     cfg.gridDim = dim3((unsigned)(k * cs));
     *launched = true;
     cfg.numAttrs = 2;  // the occupancy queries above take the cluster shape alone
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc, box);
     return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+template <typename T>
+cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
+    *launched = false;
+    // clusters of 4 CTAs when a CTA's two buffers fit (measured at
+    // [32, 64, 56, 56]: binary32 11.8 us against 12.5 us with 8, bfloat16
+    // 10.3 against 10.9), else 8; a forced size (2, 4 or 8) wins
+    int cs = a.cluster_size;
+    if (cs != 2 && cs != 4 && cs != 8)
+        cs = 2 * (size_t)((a.batch + 3) / 4) * (size_t)a.HW * sizeof(T) <= (size_t)200 * 1024 ? 4 : 8;
+    while (cs > 1 && cs > a.batch) cs >>= 1;
+    const int64_t ppc = (a.batch + cs - 1) / cs;
+    // buffer bytes, rounded up to 128 as the kernel lays the buffers out
+    const size_t buf = ((size_t)ppc * (size_t)a.HW * sizeof(T) + 127) & ~(size_t)127;
+    if (ppc > kBnMaxPpc || 2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
+    // 16-bit planes arrive as one tiled tensor copy per CTA and channel where
+    // the shape allows ([32, 64, 56, 56] bfloat16: 10.66 -> 9.58 us; the
+    // per-plane copies' fixed cost dominates small planes); binary32 keeps
+    // the per-plane copies, whose planes are reduced as each lands (12.5 us
+    // with one box against 11.8)
+    if constexpr (sizeof(T) == 2) {
+        BnBox<true> box;
+        std::memset(&box, 0, sizeof(box));
+        if (bn_box_map<T>(a, ppc, buf, &box.map, &box.bytes))
+            return launch_bn_cluster_k<T, true>(a, s, launched, cs, ppc, buf, box);
+    }
+    return launch_bn_cluster_k<T, false>(a, s, launched, cs, ppc, buf, BnBox<false>{});
 }
 
 template <typename T>

@@ -41,6 +41,20 @@ __device__ __forceinline__ void bn_write_channel_stats(const BnArgs &a, int64_t 
     }
 }
 
+// One tiled copy of a 4-D box (TMA, cp.async.bulk.tensor) described by the
+// tensor map `tmap` (a __grid_constant__ kernel parameter) at coordinates
+// (c0, c1, c2, c3), innermost first, into this CTA's shared memory (128-byte
+// aligned), counted on `bar` (the whole box's bytes, out-of-range elements
+// included, which arrive as zeros).
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Division of 32-bit unsigned integers by a run-time constant d (1 <= d <
 // 2^31) with a multiply-high, shift and add: the round-up method of
 // Granlund and Montgomery, "Division by Invariant Integers using

@@ -312,22 +312,26 @@ BN_PLANS = [nrm.PLAN_AUTO, nrm.PLAN_CTA, nrm.PLAN_TMA, nrm.PLAN_GENERIC, nrm.PLA
 BN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("cs", [2, 4, 8])
 @pytest.mark.parametrize("shape", [(1, 1, 8, 8), (3, 5, 13, 12), (9, 6, 20, 20), (64, 3, 8, 8),
-                                   (32, 4, 56, 56), (5, 2, 1, 4)])
-def test_bn_cluster_sizes(orc, shape, cs):
+                                   (32, 4, 56, 56), (5, 2, 1, 4), (7, 3, 16, 24)])
+def test_bn_cluster_sizes(orc, shape, cs, dtype):
     # the cluster plan at every cluster size; ranks beyond the batch hold no
-    # planes
-    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape)
+    # planes.  16-bit planes arrive as one tensor copy per CTA where the shape
+    # allows, the planes of a last CTA past the batch read as zeros
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
     nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
-    # the cluster plan takes at most 16 planes per CTA and two buffers of
-    # at most 200 KB; otherwise another plan runs
+    # the cluster plan takes packed planes, at most 16 planes per CTA and two
+    # buffers of at most 200 KB; otherwise another plan runs
     batch, hw = shape[0], shape[2] * shape[3]
+    es = 4 if dtype == "f32" else 2
     while cs > 1 and cs > batch:
         cs //= 2
     ppc = -(-batch // cs)
-    fits = ppc <= 16 and 2 * ppc * hw * 4 <= 200 * 1024
+    buf = -(-ppc * hw * es // 128) * 128
+    fits = (hw * es) % 16 == 0 and ppc <= 16 and 2 * buf <= 200 * 1024
     assert (nrm.last_plan()[0] == nrm.PLAN_TMA) == fits
     RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
 
