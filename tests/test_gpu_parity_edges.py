@@ -315,11 +315,12 @@ BN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("cs", [2, 4, 8])
 @pytest.mark.parametrize("shape", [(1, 1, 8, 8), (3, 5, 13, 12), (9, 6, 20, 20), (64, 3, 8, 8),
-                                   (32, 4, 56, 56), (5, 2, 1, 4), (7, 3, 16, 24)])
+                                   (32, 4, 56, 56), (5, 2, 1, 4), (7, 3, 16, 24), (4, 2, 8, 257)])
 def test_bn_cluster_sizes(orc, shape, cs, dtype):
     # the cluster plan at every cluster size; ranks beyond the batch hold no
     # planes.  16-bit planes arrive as one tensor copy per CTA where the shape
-    # allows, the planes of a last CTA past the batch read as zeros
+    # allows, the planes of a last CTA past the batch read as zeros; 8 x 257
+    # planes have no box view (257 is prime) and keep the per-plane copies
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
     nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
