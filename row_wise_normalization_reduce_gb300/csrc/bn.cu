@@ -346,13 +346,14 @@ __device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uin
 // clusters of a 64-channel batch no longer all fit at once.
 template <typename T, bool BOX>
 __global__ void __launch_bounds__(BNC_THREADS, 4)
-    bn_cluster_kernel(const BnArgs a, const int ppc, const __grid_constant__ BnBox<BOX> box) {
+    bn_cluster_kernel(const BnArgs a, const int ppc, const int nbuf,
+                      const __grid_constant__ BnBox<BOX> box) {
     namespace cg = cooperative_groups;
     using io2 = IO2<T>;
     constexpr int H = io2::H;
     constexpr int V = IO<T>::V;
     constexpr int NW = BNC_THREADS / 32;
-    extern __shared__ __align__(128) uint4 sx[];  // two buffers of ppc planes
+    extern __shared__ __align__(128) uint4 sx[];  // nbuf (1 or 2) buffers of ppc planes
     __shared__ __align__(8) uint64_t bar[2][kBnMaxPpc];
     __shared__ float s1[2][NW];
     __shared__ float s2[2][NW];
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
             mbar_init(&bar[1][j], 1);
         }
         fence_mbar_init();
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < nbuf; ++b) {
             const int64_t c = first_c + b * K_clusters;
             if (np > 0 && c < C) {
                 bn_issue_planes<T, BOX>(a, sx + b * buf_packs, bar[b], c, n0, np, q, plane_bytes, box);
@@ -409,9 +410,10 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
 
     int i = 0;
     for (int64_t c = first_c; c < C; c += K_clusters, ++i) {
-        const int b = i & 1;
+        // channel i sits in buffer i mod nbuf, that buffer's (i / nbuf)-th use
+        const int b = nbuf == 2 ? (i & 1) : 0;
         const uint4 *buf = sx + b * buf_packs;
-        const uint32_t par = (uint32_t)((i >> 1) & 1);
+        const uint32_t par = (uint32_t)((nbuf == 2 ? i >> 1 : i) & 1);
         const float K = bn_elem<T>(a.x, c * HW);  // x[0, c, 0]
         // second half of the previous channel's barrier: every peer has folded
         // that channel's partials before any partial is written again
@@ -516,12 +518,12 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
             }
         }
         __syncthreads();  // every thread is done with this buffer; s_fail is visible
-        const int64_t next = c + 2 * K_clusters;
+        const int64_t next = c + nbuf * K_clusters;
         if (tid == 0 && np > 0 && next < C && !s_fail) {
             fence_proxy_async_smem();
             bn_issue_planes<T, BOX>(a, sx + b * buf_packs, bar[b], next, n0, np, q, plane_bytes, box);
-            if (b == 0) last_issued0 = i + 2;
-            else last_issued1 = i + 2;
+            if (b == 0) last_issued0 = i + nbuf;
+            else last_issued1 = i + nbuf;
         }
     }
     if (i > 0) cluster_wait();  // peers are done reading this CTA's last partials
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
             const int li = b == 0 ? last_issued0 : last_issued1;
             if (li < 0) continue;
             for (int j = 0; j < (BOX ? 1 : np); ++j)
-                if (!mbar_wait_bounded(&bar[b][j], (uint32_t)((li >> 1) & 1), 1u << 22))
+                if (!mbar_wait_bounded(&bar[b][j], (uint32_t)((nbuf == 2 ? li >> 1 : li) & 1), 1u << 22))
                     atomicOr(a.fault, FAULT_DRAIN);
         }
     }
@@ -547,6 +549,10 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
 // the planes are 16-byte aligned and one unit long; else the scalar plan.
 #ifndef NRM_BN_TMAP
 #define NRM_BN_TMAP 1
+#endif
+// one-buffer cluster plan for channels too large for two buffers per CTA
+#ifndef NRM_BN_ONE_BUFFER
+#define NRM_BN_ONE_BUFFER 1
 #endif
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (nothing
@@ -602,10 +608,13 @@ bool bn_box_map(const BnArgs &a, int64_t ppc, size_t buf, CUtensorMap *m, uint32
 }
 
 // Launch of one instance (per-plane copies, or one box) for cs CTAs per
-// cluster of ppc planes each, buffers of buf bytes.
+// cluster of ppc planes each, buffers of buf bytes.  two_buf: the CTAs may
+// hold two buffers (channels pipelined through them when not every channel
+// has a resident cluster); else one, each cluster taking its channels one
+// after another.
 template <typename T, bool BOX>
 cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched, int cs,
-                                int64_t ppc, size_t buf, const BnBox<BOX> &box) {
+                                int64_t ppc, size_t buf, bool two_buf, const BnBox<BOX> &box) {
     auto kernel = bn_cluster_kernel<T, BOX>;
     static std::mutex mu;  // one per instance
     static int attr_done[64];
@@ -614,8 +623,11 @@ cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched,
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+            // 16-CTA clusters are a non-portable size
             if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     200 * 1024) == cudaSuccess)
+                                     kSmemMax) == cudaSuccess &&
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                    cudaSuccess)
                 attr_done[dev] = 1;
             else
                 cudaGetLastError();
@@ -642,11 +654,15 @@ cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched,
         return cudaSuccess;
     }
     int64_t k = a.C;
+    int nbuf = 1;
     if (clusters < a.C || (a.max_clusters > 0 && a.max_clusters < a.C)) {
-        cfg.dynamicSmemBytes = 2 * buf;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            return cudaSuccess;
+        if (two_buf) {
+            cfg.dynamicSmemBytes = 2 * buf;
+            nbuf = 2;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                return cudaSuccess;
+            }
         }
         k = clusters;
         if (a.max_clusters > 0 && a.max_clusters < k) k = a.max_clusters;
@@ -655,24 +671,52 @@ cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched,
     cfg.gridDim = dim3((unsigned)(k * cs));
     *launched = true;
     cfg.numAttrs = 2;  // the occupancy queries above take the cluster shape alone
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc, box);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, (int)ppc, nbuf, box);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 template <typename T>
 cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     *launched = false;
+    if (a.C > 0x7fffffff / 16) return cudaSuccess;
+    // A CTA holds ppc = ceil(batch / cs) planes of a channel in a buffer of
+    // buf bytes (rounded up to 128, as the kernel lays the buffers out).
+    auto ppc_of = [&](int cs) { return (a.batch + cs - 1) / cs; };
+    auto buf_of = [&](int cs) {
+        return ((size_t)ppc_of(cs) * (size_t)a.HW * sizeof(T) + 127) & ~(size_t)127;
+    };
+    auto fits = [&](int cs, int nb) {
+        return ppc_of(cs) <= kBnMaxPpc && nb * buf_of(cs) <= (size_t)(nb == 2 ? 200 : 220) * 1024;
+    };
     // clusters of 4 CTAs when a CTA's two buffers fit (measured at
     // [32, 64, 56, 56]: binary32 11.8 us against 12.5 us with 8, bfloat16
-    // 10.3 against 10.9), else 8; a forced size (2, 4 or 8) wins
+    // 10.3 against 10.9), else 8; for 16-bit planes too large for that, one
+    // buffer per CTA in clusters of 4, 8 or 16, each cluster taking its
+    // channels one after another ([64, 64, 112, 112] bfloat16, 8 CTAs of
+    // 196 KB: 66.3 us against 87.7 us for the one-pass plan; binary32, 16
+    // CTAs of 196 KB: 110.4 us against 98.6, so binary32 leaves these shapes
+    // to the one-pass plan).  A forced size wins.
     int cs = a.cluster_size;
-    if (cs != 2 && cs != 4 && cs != 8)
-        cs = 2 * (size_t)((a.batch + 3) / 4) * (size_t)a.HW * sizeof(T) <= (size_t)200 * 1024 ? 4 : 8;
-    while (cs > 1 && cs > a.batch) cs >>= 1;
-    const int64_t ppc = (a.batch + cs - 1) / cs;
-    // buffer bytes, rounded up to 128 as the kernel lays the buffers out
-    const size_t buf = ((size_t)ppc * (size_t)a.HW * sizeof(T) + 127) & ~(size_t)127;
-    if (ppc > kBnMaxPpc || 2 * buf > (size_t)200 * 1024 || a.C > 0x7fffffff / 8) return cudaSuccess;
+    bool two_buf = true;
+    if (cs == 2 || cs == 4 || cs == 8 || cs == 16) {
+        while (cs > 1 && cs > a.batch) cs >>= 1;
+        two_buf = fits(cs, 2);
+        if (!two_buf && !(NRM_BN_ONE_BUFFER && fits(cs, 1))) return cudaSuccess;
+    } else {
+        cs = 0;
+        for (int c : {4, 8})
+            if (!cs && fits(c, 2)) cs = c;
+        if (!cs && NRM_BN_ONE_BUFFER && sizeof(T) == 2) {
+            two_buf = false;
+            for (int c : {4, 8, 16})
+                if (!cs && fits(c, 1)) cs = c;
+        }
+        if (!cs) return cudaSuccess;
+        while (cs > 1 && cs > a.batch) cs >>= 1;
+        two_buf = fits(cs, 2);
+    }
+    const int64_t ppc = ppc_of(cs);
+    const size_t buf = buf_of(cs);
     // 16-bit planes arrive as one tiled tensor copy per CTA and channel where
     // the shape allows ([32, 64, 56, 56] bfloat16: 10.66 -> 9.58 us; the
     // per-plane copies' fixed cost dominates small planes); binary32 keeps
@@ -682,9 +726,9 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
         BnBox<true> box;
         std::memset(&box, 0, sizeof(box));
         if (bn_box_map<T>(a, ppc, buf, &box.map, &box.bytes))
-            return launch_bn_cluster_k<T, true>(a, s, launched, cs, ppc, buf, box);
+            return launch_bn_cluster_k<T, true>(a, s, launched, cs, ppc, buf, two_buf, box);
     }
-    return launch_bn_cluster_k<T, false>(a, s, launched, cs, ppc, buf, BnBox<false>{});
+    return launch_bn_cluster_k<T, false>(a, s, launched, cs, ppc, buf, two_buf, BnBox<false>{});
 }
 
 template <typename T>

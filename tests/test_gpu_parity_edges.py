@@ -313,7 +313,7 @@ BN_IDS = ["auto", "stream", "cluster", "scalar", "flow"]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("cs", [2, 4, 8])
+@pytest.mark.parametrize("cs", [2, 4, 8, 16])
 @pytest.mark.parametrize("shape", [(1, 1, 8, 8), (3, 5, 13, 12), (9, 6, 20, 20), (64, 3, 8, 8),
                                    (32, 4, 56, 56), (5, 2, 1, 4), (7, 3, 16, 24), (4, 2, 8, 257)])
 def test_bn_cluster_sizes(orc, shape, cs, dtype):
@@ -325,15 +325,30 @@ def test_bn_cluster_sizes(orc, shape, cs, dtype):
     nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
     gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
     # the cluster plan takes packed planes, at most 16 planes per CTA and two
-    # buffers of at most 200 KB; otherwise another plan runs
+    # buffers of at most 200 KB, or one of at most 220 KB; otherwise another
+    # plan runs
     batch, hw = shape[0], shape[2] * shape[3]
     es = 4 if dtype == "f32" else 2
     while cs > 1 and cs > batch:
         cs //= 2
     ppc = -(-batch // cs)
     buf = -(-ppc * hw * es // 128) * 128
-    fits = (hw * es) % 16 == 0 and ppc <= 16 and 2 * buf <= 200 * 1024
+    fits = (hw * es) % 16 == 0 and ppc <= 16 and buf <= 220 * 1024
     assert (nrm.last_plan()[0] == nrm.PLAN_TMA) == fits
+    RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
+
+
+@pytest.mark.parametrize("shape,dtype,cs", [
+    ((64, 20, 64, 64), "f32", 8), ((64, 20, 96, 96), "f32", 16), ((64, 9, 112, 112), "f32", 16),
+    ((64, 20, 96, 96), "bf16", 0), ((64, 9, 112, 112), "bf16", 0), ((64, 20, 64, 64), "f16", 16)])
+def test_bn_cluster_one_buffer(orc, shape, dtype, cs):
+    # channels too large for two buffers per CTA: one buffer each, clusters of
+    # up to 16 CTAs, more channels than resident clusters (each cluster takes
+    # its channels one after another); the automatic size (cs 0) for 16-bit
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
+    nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
+    gpu = RN.run_gpu("bn", inp, 1e-5, 0.1)
+    assert nrm.last_plan()[0] == nrm.PLAN_TMA
     RN.compare("bn", inp, gpu, RN.run_oracle(orc, "bn", inp, 1e-5, 0.1))
 
 
