@@ -720,16 +720,11 @@ class SyncBnStep:
 
 
 def secondary(args, device, stream, l2):
-    import dataclasses
-    bn_bf16 = dataclasses.replace(W.BN_F32_32x64x56x56, name="bn_train_bf16_32x64x56x56",
-                                  dtype="bf16")
-    bn_bf16_big = dataclasses.replace(W.BN_F32_64x64x112x112, name="bn_train_bf16_64x64x112x112",
-                                      dtype="bf16")
     steps = [(w, None) for w in (
         W.LN_BF16_4096x4096, W.RMS_F16_2048x4096, W.LN_BF16_1024x16384, W.BN_F32_32x64x56x56,
         W.LN_F32_64x1024, W.BN_INFER_F32_32x64x56x56, W.BN_BWD_F32_32x64x56x56,
         W.BN_F32_64x64x112x112, W.BN_BWD_F32_64x64x112x112, W.SOFTMAX_F32_128x4096,
-        W.SOFTMAX_BF16_4096x4096, bn_bf16, bn_bf16_big)]
+        W.SOFTMAX_BF16_4096x4096, W.BN_BF16_32x64x56x56, W.BN_BF16_64x64x112x112)]
     steps += [(None, StridedLnStep), (None, SyncBnStep)]
     out = []
     for w, cls in steps:

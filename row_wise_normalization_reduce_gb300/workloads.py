@@ -71,6 +71,15 @@ BN_BWD_F32_64x64x112x112 = Workload(
     "bn_bwd_f32_64x64x112x112", "bn_bwd", "f32", (64, 64, 112, 112), seed=9, eps=1e-5,
     note="as bn_bwd_f32_32x64x56x56")
 
+# 16-bit BatchNorm (the same draws as the binary32 workloads of each shape,
+# cast to bfloat16).
+BN_BF16_32x64x56x56 = Workload(
+    "bn_train_bf16_32x64x56x56", "bn", "bf16", (32, 64, 56, 56), seed=4, eps=1e-5,
+    momentum=0.1, note="as bn_train_f32_32x64x56x56, in bfloat16")
+BN_BF16_64x64x112x112 = Workload(
+    "bn_train_bf16_64x64x112x112", "bn", "bf16", (64, 64, 112, 112), seed=8, eps=1e-5,
+    momentum=0.1, note="as bn_train_f32_64x64x112x112, in bfloat16")
+
 # Softmax: the LLM-ops page's benchmark shape (section 1 table: Batch=128,
 # Seq=4096, binary32), and the 4096 x 4096 bf16 shape of the norm headline
 # for a working set larger than L2.  The page gives no input values; logits
@@ -85,7 +94,7 @@ SOFTMAX_BF16_4096x4096 = Workload(
 ALL = [LN_F32_64x1024, RMS_F16_2048x4096, ADD_RMS_BF16_4096x4096, LN_BF16_1024x16384,
        BN_F32_32x64x56x56, LN_BF16_4096x4096, BN_INFER_F32_32x64x56x56, BN_BWD_F32_32x64x56x56,
        BN_F32_64x64x112x112, BN_BWD_F32_64x64x112x112, SOFTMAX_F32_128x4096,
-       SOFTMAX_BF16_4096x4096]
+       SOFTMAX_BF16_4096x4096, BN_BF16_32x64x56x56, BN_BF16_64x64x112x112]
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -68,6 +68,8 @@ def test_both_arms_name_the_same_config_and_bytes():
     assert bench.algorithmic_bytes(w, stats=False) == 2 * 4096 * 4096 * 2 + 2 * 4096 * 2
     w = W.BN_F32_32x64x56x56
     assert bench.algorithmic_bytes(w) == 2 * 32 * 64 * 56 * 56 * 4 + 2 * 64 * 4 + 6 * 64 * 4
+    w = W.BN_BF16_32x64x56x56  # 16-bit x, y, gamma, beta; binary32 statistics
+    assert bench.algorithmic_bytes(w) == 2 * 32 * 64 * 56 * 56 * 2 + 2 * 64 * 2 + 6 * 64 * 4
 
 
 def test_reference_arm_line_matches_gpu_arm_keys():
