@@ -405,12 +405,17 @@ def test_bn_without_optionals(orc):
     assert np.max(np.abs(gy - ref["y_wide"])) <= 2e-5
 
 
-def test_bn_cluster_wait_give_up_path(orc):
-    # wait limit 0: every bulk-copy wait of the cluster plan gives up at once;
+@pytest.mark.parametrize("shape,dtype,cs", [
+    ((16, 12, 28, 28), "f32", 0),    # two buffers, a bulk copy per plane
+    ((16, 12, 28, 28), "bf16", 0),   # one tensor copy per CTA
+    ((64, 20, 64, 64), "f32", 8),    # one buffer, channels one after another
+    ((64, 20, 96, 96), "bf16", 0)])  # one buffer and tensor copies
+def test_bn_cluster_wait_give_up_path(orc, shape, dtype, cs):
+    # wait limit 0: every copy wait of the cluster plan gives up at once;
     # the kernel must raise the fault bit, keep every CTA in its cluster
     # barriers, drain its copies and return; the next call must be correct.
-    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=(16, 12, 28, 28))
-    nrm.force_plan(nrm.PLAN_TMA)
+    inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
+    nrm.force_plan(nrm.PLAN_TMA, 0, 0, cs, 0)
     x = inp["x"].cuda()
     assert nrm.device_fault(clear=True) == 0
     old = nrm.set_wait_limit(0)
