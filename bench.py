@@ -706,10 +706,15 @@ class SyncBnStep:
         self.sm = torch.empty(c, device=device)
         self.sr = torch.empty(c, device=device)
         self.i = 0
+        x, _ = self.sets[0]
+        nrm.bn_fwd_partial_stats(x, out=self.parts[0], workspace=self.ws)
+        torch.cuda.synchronize()
+        # partial statistics in one cluster launch, else two (units and fold)
+        one = nrm.last_plan()[0] == nrm.PLAN_TMA
         self()
         torch.cuda.synchronize()
-        self.plan = "partial+apply"
-        self.launches_per_step = 3
+        self.plan = ("cluster-stats" if one else "unit-stats+fold") + "+apply"
+        self.launches_per_step = 2 if one else 3
 
     def __call__(self):
         x, y = self.sets[self.i % self.nsets]

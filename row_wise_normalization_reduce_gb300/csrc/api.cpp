@@ -847,6 +847,21 @@ int bn_fwd_partial_stats(const void *x, double *stats, int64_t batch, int64_t C,
     const float2 *ws = static_cast<const float2 *>(workspace);
     cudaError_t e;
     int used;
+    // the cluster plan in statistics-only mode: one launch, x read once, the
+    // channel's statistics folded over the cluster (binary32, shifted by
+    // x[0, c, 0]) and written in binary64; else the streaming units and a
+    // binary64 fold
+    const int forced = g_force_kind.load(std::memory_order_relaxed);
+    if (forced == PLAN_AUTO || forced == PLAN_TMA) {
+        BnArgs ac = a;
+        ac.fault = fault_word();
+        ac.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+        ac.stats_out = stats;
+        if (forced == PLAN_TMA) ac.cluster_size = g_force_stages.load(std::memory_order_relaxed);
+        bool launched = false;
+        e = launch_bn_cluster_stats(ac, dtype, stream, &launched);
+        if (launched || e != cudaSuccess) return record_bn(e, PLAN_TMA);
+    }
     if (HW % V == 0 && aligned(x, 16) && HW / V < kBnUnitPlaneLimit) {
         int nch = 0, cpk = 0, q = 0;
         e = launch_bn_unit_stats_host(a, dtype, dev.sms, stream, &nch, &cpk, &q);

@@ -344,7 +344,7 @@ __device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uin
 
 // Four 512-thread CTAs per SM (at most 32 registers): with fewer, the 8-CTA
 // clusters of a 64-channel batch no longer all fit at once.
-template <typename T, bool BOX>
+template <typename T, bool BOX, bool STATS>
 __global__ void __launch_bounds__(BNC_THREADS, 4)
     bn_cluster_kernel(const BnArgs a, const int ppc, const int nbuf,
                       const __grid_constant__ BnBox<BOX> box) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
     __shared__ float s1[2][NW];
     __shared__ float s2[2][NW];
     __shared__ float part[2][3];  // count, mean, M2 of this CTA's planes (shifted by K)
-    __shared__ float stat[2][3];  // combined shifted mean, rstd, biased variance
+    __shared__ float stat[2][4];  // combined shifted mean, rstd, biased variance, M2
     __shared__ int s_fail;        // some wait of this CTA gave up
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
                 stat[b][0] = st.mean;
                 stat[b][1] = 1.0f / sqrtf(var + a.eps);
                 stat[b][2] = var;
+                stat[b][3] = st.m2;
             }
         }
         // nobody reads a peer's partial of this channel after this point:
@@ -497,24 +498,33 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
         cluster_arrive();
         __syncthreads();
         const float md = stat[b][0], rstd = stat[b][1];
-        if (rank == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[b][2], rstd);
+        if constexpr (STATS) {
+            // statistics only: the channel's binary64 (count, mean, M2)
+            if (rank == 0 && tid == 0) {
+                a.stats_out[3 * c + 0] = (double)ctot;
+                a.stats_out[3 * c + 1] = (double)K + (double)md;
+                a.stats_out[3 * c + 2] = (double)stat[b][3];
+            }
+        } else {
+            if (rank == 0 && tid == 0) bn_write_channel_stats(a, c, K, md, stat[b][2], rstd);
 
-        // normalize from shared memory: y = ((x - K) - md) * (rstd * gamma) + beta
-        const float g = bn_param<T>(a.gamma, c, 1.f);
-        const float bb = bn_param<T>(a.beta, c, 0.f);
-        const float2 nk = f2(-K), nmd = f2(-md), A2 = f2(rstd * g), b2 = f2(bb);
-        idx = tid;
-        for (int j = 0; j < np && idx < tp; ++j) {
-            const int end = (j + 1) * q;
-            uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + ((n0 + j) * C + c) * HW) -
-                        (size_t)j * q;
-            for (; idx < end; idx += BNC_THREADS) {
-                float2 f[H], o[H];
-                io2::unpack(buf[idx], f);
+            // normalize from shared memory: y = ((x - K) - md) * (rstd * gamma) + beta
+            const float g = bn_param<T>(a.gamma, c, 1.f);
+            const float bb = bn_param<T>(a.beta, c, 0.f);
+            const float2 nk = f2(-K), nmd = f2(-md), A2 = f2(rstd * g), b2 = f2(bb);
+            idx = tid;
+            for (int j = 0; j < np && idx < tp; ++j) {
+                const int end = (j + 1) * q;
+                uint4 *yp = reinterpret_cast<uint4 *>(static_cast<T *>(a.y) + ((n0 + j) * C + c) * HW) -
+                            (size_t)j * q;
+                for (; idx < end; idx += BNC_THREADS) {
+                    float2 f[H], o[H];
+                    io2::unpack(buf[idx], f);
 #pragma unroll
-                for (int h = 0; h < H; ++h)
-                    o[h] = __ffma2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), A2, b2);
-                __stcs(yp + idx, io2::pack(o));
+                    for (int h = 0; h < H; ++h)
+                        o[h] = __ffma2_rn(__fadd2_rn(__fadd2_rn(f[h], nk), nmd), A2, b2);
+                    __stcs(yp + idx, io2::pack(o));
+                }
             }
         }
         __syncthreads();  // every thread is done with this buffer; s_fail is visible
@@ -612,10 +622,10 @@ bool bn_box_map(const BnArgs &a, int64_t ppc, size_t buf, CUtensorMap *m, uint32
 // hold two buffers (channels pipelined through them when not every channel
 // has a resident cluster); else one, each cluster taking its channels one
 // after another.
-template <typename T, bool BOX>
+template <typename T, bool BOX, bool STATS>
 cudaError_t launch_bn_cluster_k(const BnArgs &a, cudaStream_t s, bool *launched, int cs,
                                 int64_t ppc, size_t buf, bool two_buf, const BnBox<BOX> &box) {
-    auto kernel = bn_cluster_kernel<T, BOX>;
+    auto kernel = bn_cluster_kernel<T, BOX, STATS>;
     static std::mutex mu;  // one per instance
     static int attr_done[64];
     int dev = 0;
@@ -722,13 +732,19 @@ cudaError_t launch_bn_cluster(const BnArgs &a, cudaStream_t s, bool *launched) {
     // per-plane copies' fixed cost dominates small planes); binary32 keeps
     // the per-plane copies, whose planes are reduced as each lands (12.5 us
     // with one box against 11.8)
+    // statistics only (a.stats_out): an instance without the normalize
     if constexpr (sizeof(T) == 2) {
         BnBox<true> box;
         std::memset(&box, 0, sizeof(box));
         if (bn_box_map<T>(a, ppc, buf, &box.map, &box.bytes))
-            return launch_bn_cluster_k<T, true>(a, s, launched, cs, ppc, buf, two_buf, box);
+            return a.stats_out
+                       ? launch_bn_cluster_k<T, true, true>(a, s, launched, cs, ppc, buf, two_buf, box)
+                       : launch_bn_cluster_k<T, true, false>(a, s, launched, cs, ppc, buf, two_buf, box);
     }
-    return launch_bn_cluster_k<T, false>(a, s, launched, cs, ppc, buf, two_buf, BnBox<false>{});
+    return a.stats_out ? launch_bn_cluster_k<T, false, true>(a, s, launched, cs, ppc, buf, two_buf,
+                                                            BnBox<false>{})
+                       : launch_bn_cluster_k<T, false, false>(a, s, launched, cs, ppc, buf, two_buf,
+                                                             BnBox<false>{});
 }
 
 template <typename T>
@@ -794,6 +810,23 @@ cudaError_t launch_bn_train_t(const BnArgs &a, int num_sms, cudaStream_t s, int 
 }
 
 }  // namespace
+
+cudaError_t launch_bn_cluster_stats(const BnArgs &a, int dtype, cudaStream_t s, bool *launched) {
+    *launched = false;
+    if (!a.stats_out || !a.fault) return cudaSuccess;
+    switch (dtype) {
+    case DT_F32:
+        if (a.HW % 4 || !bn_aligned16(a.x)) return cudaSuccess;
+        return launch_bn_cluster<float>(a, s, launched);
+    case DT_F16:
+        if (a.HW % 8 || !bn_aligned16(a.x)) return cudaSuccess;
+        return launch_bn_cluster<__half>(a, s, launched);
+    case DT_BF16:
+        if (a.HW % 8 || !bn_aligned16(a.x)) return cudaSuccess;
+        return launch_bn_cluster<__nv_bfloat16>(a, s, launched);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_bn_unit_stats(const BnArgs &a, int dtype, int num_sms, cudaStream_t s,
                                  BnChunks *u) {

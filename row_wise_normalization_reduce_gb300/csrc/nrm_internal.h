@@ -122,6 +122,8 @@ struct BnArgs {
     int cluster_size = 0; // cluster plan: CTAs per cluster (0: 8), a measurement hook
     int max_clusters = 0; // cluster plan: at most this many clusters (0: one per channel
                           // when they all fit at once), a measurement hook
+    double *stats_out = nullptr;  // cluster plan: write each channel's binary64
+                                  // (count, mean, M2) at [3c] instead of normalizing
 };
 
 // BatchNorm plans: automatic, streaming two kernels (registers + dependent
@@ -249,6 +251,10 @@ cudaError_t launch_bn_fold_stats(const float2 *ws, const void *x, double *stats,
 cudaError_t launch_bn_fold_sums(const float2 *ws, const float *rstd, double *sums,
                                 int64_t per_channel, int64_t C, cudaStream_t s);
 cudaError_t launch_bn_apply_stats(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
+// The cluster plan in statistics-only mode (a.stats_out set): one launch
+// writes every channel's (count, mean, M2); *launched false when the plan
+// cannot take the shape.
+cudaError_t launch_bn_cluster_stats(const BnArgs &a, int dtype, cudaStream_t s, bool *launched);
 cudaError_t launch_bn_apply_sums(const BnSyncArgs &a, int dtype, int num_sms, cudaStream_t s);
 
 }  // namespace nrm

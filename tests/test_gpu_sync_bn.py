@@ -25,16 +25,23 @@ SPLITS = [(4, 8, 14, 14, [2, 2]), (6, 3, 9, 11, [1, 2, 3]), (8, 16, 28, 28, [3, 
           (2, 4, 5, 5, [1, 1])]
 
 
+# partial statistics: the cluster plan in statistics-only mode (automatic, for
+# packed planes) or the streaming units and a binary64 fold (forced)
+@pytest.mark.parametrize("plan", [nrm.PLAN_AUTO, nrm.PLAN_CTA], ids=["auto", "stream"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("split", SPLITS, ids=lambda s: "x".join(map(str, s[:4])) + "_" +
                          "-".join(map(str, s[4])))
-def test_sync_bn_forward_parts_match_whole_batch(orc, split, dtype):
+def test_sync_bn_forward_parts_match_whole_batch(orc, split, dtype, plan):
     shape, sizes = tuple(split[:4]), split[4]
     inp = W.make_inputs(W.BN_F32_32x64x56x56, shape=shape, dtype=dtype)
     x = inp["x"].cuda()
     g, b = inp["gamma"].cuda(), inp["beta"].cuda()
     shards = torch.split(x, sizes, dim=0)
-    parts = torch.stack([nrm.bn_fwd_partial_stats(s) for s in shards])
+    nrm.force_plan(plan)
+    try:
+        parts = torch.stack([nrm.bn_fwd_partial_stats(s) for s in shards])
+    finally:
+        nrm.force_plan(nrm.PLAN_AUTO)
     ys, rms, rvs = [], [], []
     for s in shards:
         rm = inp["running_mean"].cuda()
