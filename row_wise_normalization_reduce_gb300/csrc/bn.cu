@@ -557,6 +557,8 @@ __global__ void __launch_bounds__(BNC_THREADS, 4)
 // are more channels than resident clusters, each cluster pipelines its
 // channels through two buffers.  Otherwise the streaming two kernels when
 // the planes are 16-byte aligned and one unit long; else the scalar plan.
+// one tiled tensor copy per CTA and channel for 16-bit planes (0: per-plane
+// bulk copies; a measurement hook)
 #ifndef NRM_BN_TMAP
 #define NRM_BN_TMAP 1
 #endif
