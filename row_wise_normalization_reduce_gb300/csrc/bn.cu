@@ -196,6 +196,9 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, c
         }
         pdl_wait();
     }
+    // the normalize kernel may launch once every CTA of this grid has started
+    // (it waits for this grid's completion before it reads the partials)
+    pdl_launch_dependents();
     int par = 0;
     for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
         const BnUnit w = bn_unit(u, idx);
@@ -211,7 +214,6 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_stats_kernel(const BnArgs a, c
         const float2 r = bn_unit_partial<T>(v, w.len, K, s1[par], s2[par]);
         if (tid == 0) ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] = r;
     }
-    pdl_launch_dependents();
     // A later group's statistics kernel overlaps the previous group's
     // normalize kernel; it finishes only after that kernel has, so the end of
     // the last kernel of a call implies the end of all of them.

@@ -61,6 +61,12 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_bwd_sums_kernel(const BnBwdArg
     const int tid = threadIdx.x;
     const int64_t units = a.batch * u.G * u.nch, HW = a.HW;
     float2 *ws = static_cast<float2 *>(a.ws);
+    // stage 2 may launch once every CTA of this grid has started (it waits
+    // for this grid's completion before it reads the partials): started at
+    // the top, it takes the SMs as this grid's last wave leaves them
+    // ([32, 64, 56, 56] binary32: 19.58 -> 18.70 us against triggering at
+    // the end)
+    pdl_launch_dependents();
     int par = 0;
     for (int64_t idx = blockIdx.x; idx < units; idx += gridDim.x, par ^= 1) {
         const BnUnit w = bn_unit(u, idx);
@@ -92,7 +98,6 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_bwd_sums_kernel(const BnBwdArg
         const float2 S = cta_sum_all<NW>(make_float2(hsum(sg), hsum(sgx)), s2[par]);
         if (tid == 0) ws[w.c * (a.batch * u.nch) + w.n * u.nch + w.k] = S;
     }
-    pdl_launch_dependents();
     pdl_wait();  // finish after the previous group's stage 2 (see bn.cu)
 }
 
