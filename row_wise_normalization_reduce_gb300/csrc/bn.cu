@@ -290,13 +290,16 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a, co
 // ---------------------------------------------------------------------------
 // Thread-block clusters over channels (a single-launch plan).
 //
-// Cluster k (cs CTAs) handles channels k, k + K, k + 2K, ... (K clusters).
-// The cs CTAs split the batch: CTA rank r owns planes n in [r*ppc,
-// min((r+1)*ppc, batch)) of the channel.  Each CTA has two shared-memory
-// buffers: while channel i is reduced and written from one buffer, the planes
-// of channel i+1 stream into the other (one bulk asynchronous copy per plane,
-// each completing on its own mbarrier), so x is read from HBM once and loads
-// overlap the stores.
+// Cluster k (cs CTAs, 2 to 16) handles channels k, k + K, k + 2K, ... (K
+// clusters).  The cs CTAs split the batch: CTA rank r owns planes n in
+// [r*ppc, min((r+1)*ppc, batch)) of the channel.  When every channel has a
+// resident cluster a CTA needs one shared-memory buffer; otherwise it holds
+// two when they fit, and while channel i is reduced and written from one
+// buffer the planes of channel i+1 stream into the other; else one, the
+// cluster taking its channels one after another.  The planes arrive as one
+// bulk asynchronous copy per plane, each completing on its own mbarrier, or
+// (16-bit planes, BOX) as one tiled tensor copy of all of them on one
+// mbarrier; x is read from HBM once.
 //
 // Statistics in one pass, plane by plane as the copies land: thread t keeps
 // (count, sum e, sum e^2) of e = x - K_t over its packs, K_t its own first
@@ -308,7 +311,9 @@ __global__ void __launch_bounds__(BNS_THREADS) bn_norm_kernel(const BnArgs a, co
 // a cluster barrier every CTA folds the cs partials over distributed shared
 // memory in rank order (all agree bit for bit).  Then it normalizes its
 // planes, y = ((x - K) - md) * (rstd * gamma) + beta, and writes y.  Rank 0
-// writes save_mean/save_rstd and the running statistics.  The barrier that
+// writes save_mean/save_rstd and the running statistics.  In statistics-only
+// mode (STATS, for synchronized BatchNorm) rank 0 instead writes the
+// channel's binary64 (count, mean, M2) and nothing is normalized.  The barrier that
 // protects the partials is split: each CTA arrives right after its fold and
 // waits only before it writes the next channel's partial (or exits), so it
 // overlaps the stores of y.  Every bulk-copy wait is bounded; on a give-up
