@@ -316,8 +316,14 @@ int bn_bwd(const void *dy, const void *x, const void *gamma, const float *save_m
  * With one part these reduce to bn_fwd_train / bn_bwd.
  *
  * bn_fwd_partial_stats: stats[3*c + {0,1,2}] = (count, mean, M2) of channel c
- *   over this process's x[batch, C, HW], binary64, written.  workspace: at
- *   least batch * C * 8 bytes, 16-byte aligned, scratch.
+ *   over this process's x[batch, C, HW], binary64, written.  Where the
+ *   planes are packed 16-byte aligned rows, one launch of the training
+ *   forward's cluster plan without its normalize: the channel's statistics
+ *   folded over the cluster in binary32 (shifted by x[0, c, 0], as in the
+ *   forward) and written in binary64; otherwise (or with NRM_PLAN_CTA or
+ *   NRM_PLAN_GENERIC forced) per-chunk or per-plane partials folded in
+ *   binary64.  workspace: at least bn_fwd_train_workspace_size(...) bytes,
+ *   16-byte aligned, scratch.
  * bn_fwd_apply_stats: parts = nparts arrays as above, concatenated in rank
  *   order ([nparts][C][3]); they are combined in that order (Chan's pairwise
  *   rule, binary64), so every process computes the same statistics.  Then as
@@ -386,8 +392,9 @@ typedef enum {
  * plan (per-plane statistics into the workspace, then a dependent launch that
  * normalizes), NRM_PLAN_TMA one cluster of CTAs per channel (shared memory and
  * distributed shared memory, no workspace; as measurement hooks, `stages`
- * of 2, 4 or 8 sets the CTAs per cluster and a non-zero `threads` caps the
- * number of clusters, each then taking several channels in turn),
+ * of 2, 4, 8 or 16 sets the CTAs per cluster and a non-zero `threads` caps
+ * the number of clusters, each then taking several channels in turn, through
+ * two buffers per CTA where they fit, else one),
  * NRM_PLAN_PERSIST the one-pass
  * plan (a reset of the workspace's control words, then one kernel whose
  * CTAs take statistics items and normalize items in a fixed interleaved
