@@ -351,11 +351,12 @@ __device__ __forceinline__ void bn_issue_planes(const BnArgs &a, uint4 *buf, uin
 
 // binary32: four 512-thread CTAs per SM (at most 32 registers): with fewer,
 // the 8-CTA clusters of a 64-channel batch no longer all fit at once.
-// 16-bit: two (the compiler takes about 42 registers; [32, 64, 56, 56]
-// bfloat16 9.67 -> 9.33 us, [64, 64, 112, 112] 67.3 -> 65.5 us; binary32
-// measured 11.78 -> 11.88 us that way and keeps four).
+// 16-bit and statistics only: two (the compiler takes about 42 registers;
+// [32, 64, 56, 56] bfloat16 9.67 -> 9.33 us, [64, 64, 112, 112] 67.3 ->
+// 65.5 us; the binary32 normalize measured 11.78 -> 11.88 us that way and
+// keeps four).
 template <typename T, bool BOX, bool STATS>
-__global__ void __launch_bounds__(BNC_THREADS, sizeof(T) == 2 ? 2 : 4)
+__global__ void __launch_bounds__(BNC_THREADS, (sizeof(T) == 2 || STATS) ? 2 : 4)
     bn_cluster_kernel(const BnArgs a, const int ppc, const int nbuf,
                       const __grid_constant__ BnBox<BOX> box) {
     namespace cg = cooperative_groups;
