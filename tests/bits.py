@@ -14,7 +14,8 @@ def f16_bits_to_f64(bits):
 
 def bf16_bits_to_f64(bits):
     b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN payloads widen as NaN
+        return b.view(np.float32).astype(np.float64)
 
 
 def bits_to_f64(dt, a):
@@ -48,7 +49,8 @@ def dt_code(dtype: torch.dtype) -> int:
 
 def f64_to_bits_numpy_f16(v):
     """Independent RN-even double -> binary16 (numpy's conversion)."""
-    return np.asarray(v, np.float64).astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore", invalid="ignore"):  # out of range rounds to infinity
+        return np.asarray(v, np.float64).astype(np.float16).view(np.uint16)
 
 
 def f32_to_bits_torch_bf16(v):
