@@ -88,6 +88,20 @@ def test_forced_plans(orc, op, dt, plan):
     assert got[0] == plan[0]
 
 
+@pytest.mark.parametrize("op", ["ln", "rms", "add_rms"])
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", [(512, 4), (1024, 2)], ids=lambda c: f"{c[0]}x{c[1]}")
+def test_persist_exact_rows(orc, op, dt, shape):
+    # rows of exactly THREADS x PACKS packs (every thread's packs in range);
+    # 400 rows give every persistent CTA two or three rows
+    th, pk = shape
+    n = th * pk * (4 if dt == "f32" else 8)
+    inp = W.generic_rows(op, dt, 400, n, seed=th + pk, scale=1.5, shift=0.5)
+    nrm.force_plan(nrm.PLAN_PERSIST, th, pk)
+    _check(orc, op, inp)
+    assert nrm.last_plan()[0] == nrm.PLAN_PERSIST
+
+
 # cluster split (threads, packs per thread, CTAs per cluster): every compiled
 # instance
 CLUSTER_SHAPES = [(128, 1, 2), (128, 1, 4), (128, 2, 2), (128, 2, 4), (128, 4, 2), (128, 4, 4),
